@@ -1,0 +1,69 @@
+// gemm.h -- GEMM and elementwise launchers of libgbq (internal).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gbq.h"
+
+namespace gbq {
+
+// Epilogues of the exact int8 GEMM.
+enum EpiMode {
+    EPI_ACC_I32 = 0,       // out int32 [M, ld_out]: the exact accumulator
+    EPI_DEQUANT_BF16 = 1,  // out bf16: bf16(fmaf(fp32(acc) * x_scale[m], w_scale[n], bias[n]))
+    EPI_ROWSCALE_F32 = 2,  // out fp32: fp32(acc) * x_scale[m]
+};
+
+// Orientation of the int8 weight operand.
+enum WLayout {
+    W_KMAJOR = 0,  // W8 [N][K]: output index n = W row, contraction along a row (the forward)
+    W_NMAJOR = 1,  // W8 [Kc][N]: contraction over W rows, output index = W column (the dx route)
+};
+
+struct I8GemmProblem {
+    const void *b_f16;        // activations as exact fp16 integers [M][K]
+    const int8_t *w0;         // W source for output rows [0, n_split)
+    const int8_t *w1;         // W source for output rows [n_split, N) (may equal w0 with n_split = N)
+    int64_t ld_w;             // bytes between W rows
+    int64_t w_rows_total0, w_rows_total1;  // rows of each source tensor (TMA bounds)
+    int64_t M, N, K;
+    int64_t n_split;
+    int w_layout;
+    int epi;
+    void *out;
+    int64_t ld_out;           // elements
+    const float *x_scale;     // [M]
+    const float *w_scale0;    // [n_split] (indexed by row within source 0)
+    const float *w_scale1;    // [N - n_split]
+    const void *bias;         // bf16 [N] or nullptr (EPI_DEQUANT_BF16)
+    unsigned int *status;
+    int num_sms;
+};
+
+// Enqueue the exact int8 GEMM (tcgen05, fp16-coded operands, chunked fp32 -> int32).
+int launch_i8gemm(const I8GemmProblem &p, cudaStream_t st);
+
+// bf16 GEMM dx[M][K] = dy[M][N] @ w[N][K] (fp32 accumulation).
+int launch_bf16_gemm_nn(const void *dy, const void *w, void *dx, int64_t M, int64_t N, int64_t K,
+                        unsigned int *status, int num_sms, cudaStream_t st);
+
+// Decode GEMV (M <= 8): y[m][n] = dequant(sum_k q[m][k] w8[n][k]) from a rotated+quantized x.
+int launch_gemv(const void *x, const int8_t *w8, const float *w_scale, const void *bias, void *y, int64_t M,
+                int64_t N, int64_t K, int logn, int groups, int num_sms, cudaStream_t st);
+
+// Elementwise helpers.
+cudaError_t launch_dequant(const int32_t *acc, int64_t ld_acc, const float *xs, const float *ws, const void *bias,
+                           void *y, int64_t ld_y, int64_t M, int64_t N, cudaStream_t st);
+cudaError_t launch_s8_to_f16(const int8_t *q, void *out, int64_t n, cudaStream_t st);
+cudaError_t launch_scale_rows_s8(const int8_t *w8, const float *s, void *w, int64_t N, int64_t K, cudaStream_t st);
+
+size_t gemm_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t H);
+
+// Shared with abi.cu.
+int encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint64_t inner, uint64_t outer,
+                   uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
+int gbq_fail(int code, const char *msg);
+
+}  // namespace gbq

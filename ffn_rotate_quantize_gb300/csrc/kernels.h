@@ -1,0 +1,34 @@
+// kernels.h -- host-side launchers of the libgbq kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "rotate_impl.cuh"
+
+namespace gbq {
+
+// Per-row identity "rotation" quantizer (R = I), optional per-column scale on the input.
+struct IdArgs {
+    const void *in;           // bf16 [M, ld_in]
+    const float *col_scale;   // fp32 [K] or nullptr
+    int64_t ld_in;
+    void *out;                // int8 or f16-coded int [M, K]
+    float *out_scale;         // fp32 [M]
+    int64_t M, K;
+};
+
+// Launch a rotate(+quantize) kernel.  Returns cudaErrorNotSupported for a
+// combination that has no instantiation or does not fit one CTA.
+cudaError_t launch_rotq(int logn, int in_kind, int out_kind, RotArgs a, cudaStream_t st);   // OUT_S8 / OUT_F16Q
+cudaError_t launch_rotb(int logn, int in_kind, RotArgs a, cudaStream_t st);                 // OUT_BF16
+cudaError_t launch_quant_identity(int out_kind, IdArgs a, cudaStream_t st);
+
+// Threads of one rotq launch row (G groups of n/CPT threads).
+inline int rotq_row_threads(int logn, int G) {
+    const int n = 1 << logn;
+    const int cpt = logn >= 7 ? 1 : 2;
+    return G * (n / cpt);
+}
+
+}  // namespace gbq

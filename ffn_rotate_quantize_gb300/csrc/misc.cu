@@ -1,0 +1,143 @@
+// misc.cu -- memory-bound elementwise kernels of libgbq and workspace sizing.
+#include "common.cuh"
+#include "gemm.h"
+
+namespace gbq {
+namespace {
+
+// y[m, n] = bf16(fmaf(fp32(acc[m, n]) * xs[m], ws[n], bias[n]))  (the page's dequant epilogue,
+// "API": out = acc * x_scale[m] * w_scale[n] + bias[n]); 4 columns per thread when aligned.
+__global__ void dequant_kernel(const int32_t *__restrict__ acc, int64_t ld_acc, const float *__restrict__ xs,
+                               const float *__restrict__ ws, const __nv_bfloat16 *__restrict__ bias,
+                               __nv_bfloat16 *__restrict__ y, int64_t ld_y, int64_t M, int64_t N, int vec4) {
+    const int64_t per_row = vec4 ? N / 4 : N;
+    const int64_t total = M * per_row;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t m = i / per_row;
+        const int64_t c = i - m * per_row;
+        const float x = __ldg(xs + m);
+        if (vec4) {
+            const int64_t n = 4 * c;
+            const int4 a = __ldg(reinterpret_cast<const int4 *>(acc + m * ld_acc + n));
+            const float4 w = __ldg(reinterpret_cast<const float4 *>(ws + n));
+            float b[4] = {0.f, 0.f, 0.f, 0.f};
+            if (bias) {
+                const uint2 bb = __ldg(reinterpret_cast<const uint2 *>(bias + n));
+                b[0] = __uint_as_float(bb.x << 16);
+                b[1] = __uint_as_float(bb.x & 0xFFFF0000u);
+                b[2] = __uint_as_float(bb.y << 16);
+                b[3] = __uint_as_float(bb.y & 0xFFFF0000u);
+            }
+            const float r0 = __fmaf_rn(__fmul_rn(__int2float_rn(a.x), x), w.x, b[0]);
+            const float r1 = __fmaf_rn(__fmul_rn(__int2float_rn(a.y), x), w.y, b[1]);
+            const float r2 = __fmaf_rn(__fmul_rn(__int2float_rn(a.z), x), w.z, b[2]);
+            const float r3 = __fmaf_rn(__fmul_rn(__int2float_rn(a.w), x), w.w, b[3]);
+            __nv_bfloat162 lo = __floats2bfloat162_rn(r0, r1), hi = __floats2bfloat162_rn(r2, r3);
+            uint2 o;
+            o.x = *reinterpret_cast<uint32_t *>(&lo);
+            o.y = *reinterpret_cast<uint32_t *>(&hi);
+            *reinterpret_cast<uint2 *>(y + m * ld_y + n) = o;
+        } else {
+            const int64_t n = c;
+            const float b = bias ? __bfloat162float(bias[n]) : 0.0f;
+            const float r = __fmaf_rn(__fmul_rn(__int2float_rn(acc[m * ld_acc + n]), x), __ldg(ws + n), b);
+            y[m * ld_y + n] = __float2bfloat16_rn(r);
+        }
+    }
+}
+
+// Exact int8 -> fp16 (the tensor-core coding of quantized activations), 16 per thread-step.
+__global__ void s8_to_f16_kernel(const int8_t *__restrict__ q, __half *__restrict__ out, int64_t n16) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(q) + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            o[2 * k] = s8pair_to_f16x2(__byte_perm(w[k], 0, 0x4140));      // bytes 0,1 -> 0x00B100B0
+            o[2 * k + 1] = s8pair_to_f16x2(__byte_perm(w[k], 0, 0x4342));  // bytes 2,3
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(out) + 2 * i;
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+// w[n, k] = bf16(fp32(w8[n, k]) * s[n]): dequant_weight with an identity rotation.
+__global__ void scale_rows_s8_kernel(const int8_t *__restrict__ w8, const float *__restrict__ s,
+                                     __nv_bfloat16 *__restrict__ w, int64_t N, int64_t K) {
+    const int64_t per_row = K / 16;
+    const int64_t total = N * per_row;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t n = i / per_row;
+        const float sc = __ldg(s + n);
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(w8) + i);
+        const int8_t *b = reinterpret_cast<const int8_t *>(&v);
+        uint32_t o[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn((float)b[2 * k], sc), __fmul_rn((float)b[2 * k + 1], sc));
+            o[k] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(w) + 2 * i;
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+int grid_for(int64_t work, int threads) {
+    int64_t g = (work + threads - 1) / threads;
+    if (g > 152 * 16) g = 152 * 16;
+    return (int)(g < 1 ? 1 : g);
+}
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+}  // namespace
+
+cudaError_t launch_dequant(const int32_t *acc, int64_t ld_acc, const float *xs, const float *ws, const void *bias,
+                           void *y, int64_t ld_y, int64_t M, int64_t N, cudaStream_t st) {
+    const int vec4 = (N % 4 == 0 && ld_acc % 4 == 0 && ld_y % 4 == 0 && ((uintptr_t)acc & 15) == 0 &&
+                      ((uintptr_t)y & 7) == 0 && ((uintptr_t)ws & 15) == 0 && ((uintptr_t)bias & 7) == 0)
+                         ? 1
+                         : 0;
+    const int64_t work = M * (vec4 ? N / 4 : N);
+    dequant_kernel<<<grid_for(work, 256), 256, 0, st>>>(acc, ld_acc, xs, ws,
+                                                         reinterpret_cast<const __nv_bfloat16 *>(bias),
+                                                         reinterpret_cast<__nv_bfloat16 *>(y), ld_y, M, N, vec4);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_s8_to_f16(const int8_t *q, void *out, int64_t n, cudaStream_t st) {
+    if (n % 16) return cudaErrorInvalidValue;
+    s8_to_f16_kernel<<<grid_for(n / 16, 256), 256, 0, st>>>(q, reinterpret_cast<__half *>(out), n / 16);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scale_rows_s8(const int8_t *w8, const float *s, void *w, int64_t N, int64_t K, cudaStream_t st) {
+    if (K % 16) return cudaErrorInvalidValue;
+    scale_rows_s8_kernel<<<grid_for(N * K / 16, 256), 256, 0, st>>>(w8, s, reinterpret_cast<__nv_bfloat16 *>(w), N, K);
+    return cudaGetLastError();
+}
+
+// Workspace layouts (each region 256-byte aligned):
+//   LINEAR / INT8_GEMM : q f16 [M][K], x_scale f32 [M]
+//   FFN                : qx f16 [M][d], x_scale [M], g|u bf16 [M][2H], qh f16 [M][H], h_scale [M]
+//   LINEAR_DX_INT8     : qd f16 [M][N], t f32 [M], dx_rot f32 [M][K]
+size_t gemm_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t H) {
+    if (M < 0 || N < 0 || K < 0 || H < 0) return 0;
+    switch (op) {
+        case GBQ_OP_LINEAR:
+        case GBQ_OP_INT8_GEMM:
+            return align256((size_t)M * K * 2) + align256((size_t)M * 4);
+        case GBQ_OP_FFN:
+            return align256((size_t)M * K * 2) + align256((size_t)M * 4) + align256((size_t)M * 2 * H * 2) +
+                   align256((size_t)M * H * 2) + align256((size_t)M * 4);
+        case GBQ_OP_LINEAR_DX_INT8:
+            return align256((size_t)M * N * 2) + align256((size_t)M * 4) + align256((size_t)M * K * 4);
+        default:
+            return 0;
+    }
+}
+
+}  // namespace gbq

@@ -1,0 +1,105 @@
+// rotate_b.cu -- rotate-only instantiations (bf16 output) and the identity quantizer.
+#include "rotate_launch.cuh"
+
+namespace gbq {
+
+cudaError_t launch_rotb(int logn, int in_kind, RotArgs a, cudaStream_t st) {
+    switch (in_kind) {
+        case IN_BF16: return launch_rotq_logn<IN_BF16, OUT_BF16>(logn, a, st);
+        case IN_F32: return launch_rotq_logn<IN_F32, OUT_BF16>(logn, a, st);
+        case IN_S8_ROWSCALE: return launch_rotq_logn<IN_S8_ROWSCALE, OUT_BF16>(logn, a, st);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Per-row quantizer with R = I (the dy side of linear_dx_int8, and identity
+// rotation descriptors).  One CTA of 256 threads per row; each thread keeps its
+// (up to 16) chunks of 8 values in registers across load -> amax -> quantize.
+// Optional fp32 column scale: v = bf16(dy[m,n]) * s[n] in fp32 (the weight scale
+// moved onto the contraction index, "The backward: dL/dx, weight-only").
+// ---------------------------------------------------------------------------
+constexpr int kIdThreads = 256;
+constexpr int kIdMaxChunks = 16;  // K <= 256 * 16 * 8 = 32768
+
+template <int OUT>
+__global__ void __launch_bounds__(kIdThreads) quant_identity_kernel(IdArgs p) {
+    __shared__ float s_warp[kIdThreads / 32];
+    const int64_t row = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int nchunks = (int)(p.K / 8);
+    const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(p.in) + row * p.ld_in);
+    float v[kIdMaxChunks][8];
+    float m = 0.0f;
+#pragma unroll
+    for (int c = 0; c < kIdMaxChunks; ++c) {
+        const int ch = tid + c * kIdThreads;
+        if (ch < nchunks) {
+            const uint4 w = __ldg(src + ch);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                v[c][2 * h] = __uint_as_float(ws[h] << 16);
+                v[c][2 * h + 1] = __uint_as_float(ws[h] & 0xFFFF0000u);
+            }
+            if (p.col_scale) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[c][e] = __fmul_rn(v[c][e], __ldg(p.col_scale + 8 * ch + e));
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[c][e]));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((tid & 31) == 0) s_warp[tid >> 5] = m;
+    __syncthreads();
+    float amax = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kIdThreads / 32; ++w) amax = fmaxf(amax, s_warp[w]);
+    const float s = __fdiv_rn(amax, 127.0f);
+    if (tid == 0) p.out_scale[row] = s;
+#pragma unroll
+    for (int c = 0; c < kIdMaxChunks; ++c) {
+        const int ch = tid + c * kIdThreads;
+        if (ch >= nchunks) continue;
+        int q[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            int qq = 0;
+            if (s != 0.0f) qq = max(-127, min(127, __float2int_rn(__fdiv_rn(v[c][e], s))));
+            q[e] = qq;
+        }
+        if constexpr (OUT == OUT_S8) {
+            uint2 w;
+            w.x = (uint32_t)(q[0] & 0xFF) | ((uint32_t)(q[1] & 0xFF) << 8) | ((uint32_t)(q[2] & 0xFF) << 16) |
+                  ((uint32_t)(q[3] & 0xFF) << 24);
+            w.y = (uint32_t)(q[4] & 0xFF) | ((uint32_t)(q[5] & 0xFF) << 8) | ((uint32_t)(q[6] & 0xFF) << 16) |
+                  ((uint32_t)(q[7] & 0xFF) << 24);
+            reinterpret_cast<uint2 *>(reinterpret_cast<int8_t *>(p.out) + row * p.K)[ch] = w;
+        } else {
+            uint32_t w[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                __half2 h2 = __halves2half2(__int2half_rn(q[2 * h]), __int2half_rn(q[2 * h + 1]));
+                w[h] = *reinterpret_cast<uint32_t *>(&h2);
+            }
+            reinterpret_cast<uint4 *>(reinterpret_cast<__half *>(p.out) + row * p.K)[ch] =
+                make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
+cudaError_t launch_quant_identity(int out_kind, IdArgs a, cudaStream_t st) {
+    if (a.K % 8 != 0 || a.K / 8 > (int64_t)kIdThreads * kIdMaxChunks) return cudaErrorNotSupported;
+    if (a.M > 0x7fffffff) return cudaErrorInvalidValue;
+    if (out_kind == OUT_S8)
+        quant_identity_kernel<OUT_S8><<<(unsigned)a.M, kIdThreads, 0, st>>>(a);
+    else if (out_kind == OUT_F16Q)
+        quant_identity_kernel<OUT_F16Q><<<(unsigned)a.M, kIdThreads, 0, st>>>(a);
+    else
+        return cudaErrorNotSupported;
+    return cudaGetLastError();
+}
+
+}  // namespace gbq

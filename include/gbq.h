@@ -1,0 +1,230 @@
+/*
+ * gbq.h -- C ABI of libgbq: rotated INT8 linear layers, a SwiGLU FFN and the
+ * input-gradient backward, as hand-written CUDA for GB300 (sm_103a).
+ *
+ * The method is the one on the PyPI page "xpu-kernels 0.2.0"
+ * (pypi.org/project/xpu-kernels/0.2.0): ConvRot Kronecker-Hadamard rotation
+ * of the activation, per-token INT8 quantization, an int8 x int8 -> int32
+ * GEMM against a weight stored pre-rotated, and a dequant epilogue.
+ *
+ * Conventions (shared by every entry point):
+ *   - All tensors are row-major and contiguous unless a leading dimension
+ *     (ld_*) is given.  Sizes are int64_t.  bf16 tensors are passed as
+ *     void* holding IEEE bfloat16 values.
+ *   - Every pointer is a DEVICE pointer owned by the caller (for example a
+ *     torch tensor's data_ptr()).  The library never allocates, frees or
+ *     keeps a reference to caller memory after the call returns, and no
+ *     entry point allocates device memory (all scratch comes from the
+ *     caller's `workspace`, sized by gbq_workspace_size()).
+ *   - Pointers must be 16-byte aligned; K (the contraction length) must be
+ *     a multiple of 64 for GEMM entry points.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *     only enqueues work; nothing is synchronised.  Use gbq_sync().
+ *   - Return value: 0 on success, a negative GBQ_E* code otherwise, with a
+ *     human-readable message in gbq_last_error() (thread-local).  On an
+ *     argument error nothing is launched.  No kernel traps: a device-side
+ *     wait that exceeds its iteration limit records a code that
+ *     gbq_device_status() returns.
+ *
+ * Rotation descriptor: R = I_groups (x) (H_a (x) H_b) / sqrt(a*b) with
+ * K = a*b*groups.  H_n = H4^(x)j for n = 4^j (H4 as printed in the page's
+ * "Algorithm: fused ConvRot rotation"), H_n = H2 (x) H4^(x)j for n = 2*4^j
+ * (H2 on the most significant index bit; the page is silent there).
+ * a = b = 1 is the identity.  Supported: a = b in {1, 16, 32, 64, 128}.
+ * R is symmetric and orthogonal, so rotating x and the weight rows by the
+ * same R leaves x @ W^T unchanged.
+ */
+#ifndef GBQ_H
+#define GBQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct gbq_rot {
+    int32_t a;      /* Hadamard factor on the high index part (power of two) */
+    int32_t b;      /* Hadamard factor on the low, contiguous index part     */
+    int32_t groups; /* number of contiguous blocks of a*b columns            */
+} gbq_rot;
+
+#define GBQ_OK 0
+#define GBQ_EINVAL (-22)      /* bad argument: null/misaligned pointer, bad size, bad rotation */
+#define GBQ_ENOSPC (-28)      /* workspace smaller than gbq_workspace_size() */
+#define GBQ_ENODEV (-19)      /* no usable sm_103 device */
+#define GBQ_ECUDA (-5)        /* a CUDA runtime call or launch failed */
+#define GBQ_ENOTSUP (-95)     /* valid but unsupported combination (e.g. rotation shape) */
+
+/* Device-status bits reported by gbq_device_status(). */
+#define GBQ_DEV_WAIT_TIMEOUT 0x1u /* an mbarrier wait hit its iteration limit */
+
+/* ---- library / device ------------------------------------------------ */
+
+/* Selects nothing, checks that the current device is an sm_103 GPU and sets up
+ * per-device state (device status word, driver entry point for TMA
+ * descriptors).  Called implicitly by every entry point; safe to call again. */
+int gbq_init(void);
+/* Name of the current device ("" before a successful gbq_init). */
+const char *gbq_device_name(void);
+/* Message for the last failing call on this host thread ("" if none). */
+const char *gbq_last_error(void);
+/* Waits for `stream`, then copies the device status word to *status and
+ * clears it (0 = no kernel recorded an error since the last read). */
+int gbq_device_status(void *stream, uint32_t *status);
+/* cudaStreamSynchronize(stream), with the error mapped to a GBQ code. */
+int gbq_sync(void *stream);
+
+/* ---- workspace sizing ------------------------------------------------- */
+
+enum gbq_op {
+    GBQ_OP_LINEAR = 1,      /* gbq_linear / gbq_linear_acc (M,N,K)        */
+    GBQ_OP_INT8_GEMM = 2,   /* gbq_int8_gemm (M,N,K)                     */
+    GBQ_OP_FFN = 3,         /* gbq_ffn_fused (M, d=K, H)                 */
+    GBQ_OP_LINEAR_DX_INT8 = 4 /* gbq_linear_dx_int8 (M,N,K)             */
+};
+/* Bytes of device workspace the entry point for `op` needs at these sizes. */
+size_t gbq_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t H);
+
+/* ---- rotate + quantize (activation side) ------------------------------ */
+
+/*
+ * q, x_scale = quantize(R x) per row ("Use from C": bf16 [M,K] -> int8 [M,K]
+ * + fp32 [M] row scales; "Algorithm: fused ConvRot rotation").
+ * x: bf16 [M,K].  q: int8 [M,K].  x_scale: fp32 [M].
+ * Per row, in fp32: v = R x_m; amax = max|v|; s = amax/127;
+ * q = clamp(rne(v/s), -127, 127); a row with s == 0 gets q = 0.
+ */
+int gbq_quantize_act(const void *x, int8_t *q, float *x_scale, int64_t M, int64_t K,
+                     gbq_rot rot, void *stream);
+
+/*
+ * The activation fused into the quantizer ("Use from Python":
+ * quantize_act(x2, act)): h = silu(g) * u in fp32 from bf16 g, u [M,H], then
+ * q, h_scale = quantize(R h) as in gbq_quantize_act.
+ */
+int gbq_quantize_act_glu(const void *g, const void *u, int8_t *q, float *h_scale,
+                         int64_t M, int64_t H, gbq_rot rot, void *stream);
+
+/*
+ * "dequant_act_quantize" ("Use from Python"): from the int32 gate and up
+ * accumulators (leading dimension ld_acc), g = bf16(acc_g*x_scale*s_gate),
+ * u = bf16(acc_u*x_scale*s_up), h = silu(g)*u, then quantize(R h).
+ * Bit-identical to gbq_dequant + gbq_quantize_act_glu.
+ */
+int gbq_dequant_act_quantize(const int32_t *acc_g, const int32_t *acc_u, int64_t ld_acc,
+                             const float *x_scale, const float *s_gate, const float *s_up,
+                             int8_t *q, float *h_scale, int64_t M, int64_t H, gbq_rot rot,
+                             void *stream);
+
+/* ---- weight preparation ---------------------------------------------- */
+
+/*
+ * w8, w_scale = prepare_weight(w) ("Use from Python": bf16 [N,K] -> int8 +
+ * fp32 [N], once).  The rotation is baked into the rows: W8 = quantize(W R^T)
+ * with the same per-row quantizer as gbq_quantize_act.
+ */
+int gbq_prepare_weight(const void *w, int8_t *w8, float *w_scale, int64_t N, int64_t K,
+                       gbq_rot rot, void *stream);
+
+/* ---- linear layer ----------------------------------------------------- */
+
+/*
+ * acc = int8 GEMM of pre-quantized operands: acc[m,n] = sum_k q[m,k] w8[n,k]
+ * (the page's torch._int_mm step).  q int8 [M,K], w8 int8 [N,K], acc int32
+ * [M,N] with leading dimension ld_acc.  Exact.  Workspace: GBQ_OP_INT8_GEMM.
+ */
+int gbq_int8_gemm(const int8_t *q, const int8_t *w8, int32_t *acc, int64_t ld_acc,
+                  int64_t M, int64_t N, int64_t K, void *workspace, size_t ws_bytes,
+                  void *stream);
+
+/*
+ * acc, x_scale = linear_acc(x, w8) ("Use from Python": int32 [M,N], no bf16
+ * round trip).  x bf16 [M,K]; acc int32 [M,N] (ld_acc); x_scale fp32 [M].
+ * Workspace: GBQ_OP_LINEAR.
+ */
+int gbq_linear_acc(const void *x, const int8_t *w8, int32_t *acc, int64_t ld_acc,
+                   float *x_scale, int64_t M, int64_t N, int64_t K, gbq_rot rot,
+                   void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * y = dequant(acc) ("API": out = acc * x_scale[m] * w_scale[n] + bias[n]).
+ * acc int32 [M,N] (ld_acc), y bf16 [M,N] (ld_y; a column slice of a wider
+ * output is allowed, the page's dequant_slice).  bias bf16 [N] or NULL.
+ * Per element: t = fp32(acc) * x_scale[m]; y = bf16(fmaf(t, w_scale[n], bias[n])).
+ */
+int gbq_dequant(const int32_t *acc, int64_t ld_acc, const float *x_scale,
+                const float *w_scale, const void *bias, void *y, int64_t ld_y,
+                int64_t M, int64_t N, void *stream);
+
+/*
+ * y = linear(x, w8, w_scale, bias) ("Use from Python": bf16 [..,K] -> bf16
+ * [..,N]); rotate+quantize, int8 GEMM and the dequant epilogue fused in the
+ * GEMM.  Bit-identical to gbq_dequant(gbq_linear_acc(x)).  M = 1..8 runs the
+ * decode GEMV path (weight streaming).  Workspace: GBQ_OP_LINEAR.
+ */
+int gbq_linear(const void *x, const int8_t *w8, const float *w_scale, const void *bias,
+               void *y, int64_t M, int64_t N, int64_t K, gbq_rot rot, void *workspace,
+               size_t ws_bytes, void *stream);
+
+/* ---- SwiGLU FFN ------------------------------------------------------- */
+
+/*
+ * y = down(quantize(R_h(silu(gate(x)) * up(x)))) -- the page's fused MLP
+ * (MUL_MAT + MUL_MAT + GLU/SWIGLU, then the down projection) with
+ * "dequant_act_quantize" as its middle.
+ * x bf16 [M,d]; wg8, wu8 int8 [H,d] with s_gate, s_up fp32 [H] (prepared with
+ * rot_d); wd8 int8 [d,H] with s_down fp32 [d] (prepared with rot_h);
+ * y bf16 [M,d].  No biases.  Bit-identical to the unfused chain
+ * linear_acc -> dequant -> quantize_act_glu -> linear.
+ * Workspace: GBQ_OP_FFN with (M, K=d, H).
+ */
+int gbq_ffn_fused(const void *x, const int8_t *wg8, const float *s_gate, const int8_t *wu8,
+                  const float *s_up, const int8_t *wd8, const float *s_down, void *y,
+                  int64_t M, int64_t d, int64_t H, gbq_rot rot_d, gbq_rot rot_h,
+                  void *workspace, size_t ws_bytes, void *stream);
+
+/* ---- backward dL/dx ---------------------------------------------------- */
+
+/*
+ * w = dequant_weight(w8, w_scale) ("The backward": recover W once).
+ * w8 int8 [N,K], w_scale fp32 [N] -> w bf16 [N,K] = bf16((w8[n,:]*s[n]) R),
+ * i.e. un-rotated back to the original basis (with rot = identity the
+ * literal w8*s).  Memory-bound.
+ */
+int gbq_dequant_weight(const int8_t *w8, const float *w_scale, void *w, int64_t N, int64_t K,
+                       gbq_rot rot, void *stream);
+
+/*
+ * dx = dy @ w ("The backward": bf16 GEMM, no transpose, no bias).
+ * dy bf16 [M,N], w bf16 [N,K], dx bf16 [M,K]; fp32 accumulation.
+ * N must be a multiple of 64, K a multiple of 16.
+ */
+int gbq_linear_dx(const void *dy, const void *w, void *dx, int64_t M, int64_t N, int64_t K,
+                  void *stream);
+
+/*
+ * dx = linear_dx_int8(dy, w8, w_scale) ("The backward"): dy'[m,n] =
+ * dy[m,n]*s[n]; per-row int8 quantize of dy' (no rotation) -> qd, t;
+ * acc[m,k] = sum_n qd[m,n] w8[n,k] (exact); dx = bf16((fp32(acc)*t[m]) R).
+ * dy bf16 [M,N]; w8 int8 [N,K]; w_scale fp32 [N]; dx bf16 [M,K].
+ * Workspace: GBQ_OP_LINEAR_DX_INT8.
+ */
+int gbq_linear_dx_int8(const void *dy, const int8_t *w8, const float *w_scale, void *dx,
+                       int64_t M, int64_t N, int64_t K, gbq_rot rot, void *workspace,
+                       size_t ws_bytes, void *stream);
+
+/* ---- rotate-only bf16 path --------------------------------------------- */
+
+/*
+ * xr = bf16(R x) ("Use from C": the BF16 path needs only the rotation).
+ * x, xr bf16 [M,K].
+ */
+int gbq_rotate_bf16(const void *x, void *xr, int64_t M, int64_t K, gbq_rot rot, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBQ_H */

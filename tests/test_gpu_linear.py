@@ -1,0 +1,130 @@
+"""GPU parity of the int8 GEMM, dequant epilogue, linear_acc and linear (through the C ABI)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from ffn_rotate_quantize_gb300 import inputs as I
+from parity import assert_bf16_parity, assert_int8_parity, bf16_dev, bf16_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ops():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from ffn_rotate_quantize_gb300 import ops as G
+    G.init()
+    return G
+
+
+@pytest.fixture(autouse=True)
+def _device_status_clean(ops):
+    yield
+    assert ops.device_status() == 0
+
+
+def d(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+# Shapes span several 128x128 tiles, ragged tails in M and N, K below, at and above
+# one 1024-long exact chunk, and the K of the down projection.
+GEMM_SHAPES = [(300, 392, 4096), (1, 128, 64), (129, 130, 1088), (64, 256, 16384), (257, 384, 1024)]
+
+
+@pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
+def test_int8_gemm_bit_exact(ops, M, N, K):
+    rng = np.random.default_rng(M + N + K)
+    q = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    w = rng.integers(-127, 128, (N, K)).astype(np.int8)
+    acc = ops.int8_gemm(d(q), d(w)).cpu().numpy()
+    assert np.array_equal(acc.astype(np.int64), O.gemm_s8(q, w))
+
+
+@pytest.mark.parametrize("K", [1024, 4096, 16384])
+def test_int8_gemm_extreme_magnitudes(ops, K):
+    """All-|127| operands: partial sums reach 127^2*K, far past 2^24 in fp32."""
+    M, N = 130, 256
+    rng = np.random.default_rng(K)
+    q = np.where(rng.random((M, K)) < 0.5, 127, -127).astype(np.int8)
+    q[:3] = 127
+    w = np.where(rng.random((N, K)) < 0.5, 127, -127).astype(np.int8)
+    w[:3] = 127
+    w[3:6] = -127
+    acc = ops.int8_gemm(d(q), d(w)).cpu().numpy()
+    assert np.array_equal(acc.astype(np.int64), O.gemm_s8(q, w))
+    assert acc[0, 0] == 127 * 127 * K and acc[0, 3] == -127 * 127 * K
+
+
+def test_int8_gemm_one_hot_rows(ops):
+    """Rotated one-hot rows quantize to +-127 patterns whose products reach 127^2*K."""
+    rot, K = (64, 64, 1), 4096
+    x = np.zeros((8, K), np.float32)
+    for r in range(8):
+        x[r, 37 * r] = 1.0
+    q, _ = O.rotate_quantize(I.bf16_bits(x), rot)
+    acc = ops.int8_gemm(d(q), d(q)).cpu().numpy().astype(np.int64)
+    assert np.array_equal(acc, np.diag(np.full(8, 127 * 127 * K)))
+
+
+def _case(M, K, N, seed, rot, outliers=True):
+    c = I.linear_case(M, K, N, n_outliers=max(1, K // 100) if outliers else 0, outlier_scale=30.0,
+                      bias_std=0.01, seed=seed)
+    w8, ws = O.prepare_weight(c["w"], rot)
+    return c, w8, ws
+
+
+LINEAR_CASES = [(300, 4096, 392, (64, 64, 1)), (16, 256, 256, (16, 16, 1)), (129, 1024, 200, (32, 32, 1)),
+                (64, 16384, 256, (128, 128, 1)), (40, 3072, 128, (16, 16, 12))]
+
+
+@pytest.mark.parametrize("M,K,N,rot", LINEAR_CASES)
+def test_linear_and_linear_acc(ops, M, K, N, rot):
+    c, w8, ws = _case(M, K, N, seed=M + K, rot=rot)
+    x, bias = bf16_dev(c["x"]), bf16_dev(c["bias"])
+    acc, xs = ops.linear_acc(x, d(w8), rot)
+    y = ops.linear(x, d(w8), d(ws), bias, rot)
+    torch.cuda.synchronize()
+    qr, sr = O.rotate_quantize(c["x"], rot)
+    acc_r = O.gemm_s8(qr, w8)
+    y_r = O.dequant(acc_r, sr, ws, c["bias"])
+    # The GPU's own quantized x: rows whose codes match the oracle's must give the exact accumulator.
+    qg, _ = ops.quantize_act(x, rot)
+    same = np.all(qg.cpu().numpy() == qr, axis=1)
+    assert same.mean() > 0.9
+    assert np.array_equal(acc.cpu().numpy()[same].astype(np.int64), acc_r[same])
+    assert_bf16_parity(bf16_np(y), y_r)
+    # dequant(linear_acc(x)) == linear(x), bit for bit ("Use from Python").
+    y2 = ops.dequant(acc, xs, d(ws), bias)
+    assert torch.equal(y2.view(torch.int16), y.view(torch.int16))
+
+
+def test_tiny_config_exact(ops):
+    """x [16,256], W [256,256], R = H16 (x) H16 / 16, bias."""
+    c = I.config_case("tiny_linear")
+    rot = c["config"]["rot"]
+    w8g, wsg = ops.prepare_weight(bf16_dev(c["w"]), rot)
+    w8, ws = O.prepare_weight(c["w"], rot)
+    assert_int8_parity(w8g.cpu().numpy(), w8)
+    y = ops.linear(bf16_dev(c["x"]), w8g, wsg, bf16_dev(c["bias"]), rot)
+    assert_bf16_parity(bf16_np(y), O.linear(c["x"], w8, ws, c["bias"], rot))
+
+
+def test_dequant_standalone_and_slice(ops):
+    rng = np.random.default_rng(9)
+    M, N = 77, 520
+    acc = rng.integers(-2 ** 27, 2 ** 27, (M, N)).astype(np.int32)
+    xs = (rng.random(M) * 1e-4).astype(np.float32)
+    ws = (rng.random(N) * 1e-3).astype(np.float32)
+    bias = I.bf16_bits(rng.standard_normal(N).astype(np.float32) * 0.01)
+    y = ops.dequant(d(acc), d(xs), d(ws), bf16_dev(bias))
+    ref = O.dequant(acc.astype(np.int64), xs, ws, bias)
+    assert np.array_equal(bf16_np(y), ref)  # identical fp32 operations -> identical bits
+    # a strided column slice of a wider accumulator (the page's dequant_slice)
+    s0, s1 = 128, 392
+    ys = ops.dequant(d(acc)[:, s0:s1], d(xs), d(ws[s0:s1]), bf16_dev(bias[s0:s1]))
+    assert np.array_equal(bf16_np(ys), ref[:, s0:s1])
+    yn = ops.dequant(d(acc), d(xs), d(ws), None)
+    assert np.array_equal(bf16_np(yn), O.dequant(acc.astype(np.int64), xs, ws, None))
