@@ -164,6 +164,32 @@ int encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base
     return GBQ_OK;
 }
 int gbq_fail(int code, const char *msg) { return fail(code, "%s", msg); }
+
+// ---- launch timing: library-owned event pairs, recorded only while enabled.
+namespace {
+constexpr int kProfMax = 8192;
+bool g_prof_on = false;
+int g_prof_n = 0;
+int g_prof_kind[kProfMax];
+cudaEvent_t g_prof_ev[2][kProfMax];
+bool g_prof_created = false;
+std::mutex g_prof_mu;
+}  // namespace
+
+void prof_begin(int kind, cudaStream_t st) {
+    if (!g_prof_on) return;
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    if (g_prof_n >= kProfMax) return;
+    g_prof_kind[g_prof_n] = kind;
+    cudaEventRecord(g_prof_ev[0][g_prof_n], st);
+}
+void prof_end(cudaStream_t st) {
+    if (!g_prof_on) return;
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    if (g_prof_n >= kProfMax) return;
+    cudaEventRecord(g_prof_ev[1][g_prof_n], st);
+    ++g_prof_n;
+}
 }  // namespace gbq
 
 // ============================================================ entry points
@@ -200,6 +226,41 @@ int gbq_device_status(void *stream, uint32_t *status) {
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(e, "gbq_device_status");
     *status = host;
+    return GBQ_OK;
+}
+
+int gbq_prof_enable(int on) {
+    INIT(d);
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    if (on && !g_prof_created) {
+        for (int i = 0; i < 2; ++i)
+            for (int j = 0; j < kProfMax; ++j) {
+                cudaError_t e = cudaEventCreate(&g_prof_ev[i][j]);
+                if (e != cudaSuccess) return cuda_fail(e, "gbq_prof_enable");
+            }
+        g_prof_created = true;
+    }
+    g_prof_n = 0;
+    g_prof_on = on != 0;
+    return GBQ_OK;
+}
+
+int gbq_prof_read(int kind, int *launches, double *total_ms) {
+    REQUIRE(launches && total_ms, "gbq_prof_read: NULL output");
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    int n = 0;
+    double ms = 0.0;
+    for (int i = 0; i < g_prof_n; ++i) {
+        if (g_prof_kind[i] != kind) continue;
+        cudaError_t e = cudaEventSynchronize(g_prof_ev[1][i]);
+        float t = 0.f;
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&t, g_prof_ev[0][i], g_prof_ev[1][i]);
+        if (e != cudaSuccess) return cuda_fail(e, "gbq_prof_read");
+        ms += t;
+        ++n;
+    }
+    *launches = n;
+    *total_ms = ms;
     return GBQ_OK;
 }
 
@@ -485,8 +546,8 @@ int gbq_linear(const void *x, const int8_t *w8, const float *w_scale, const void
     if (rc) return rc;
     INIT(d);
     cudaStream_t st = (cudaStream_t)stream;
-    if (M <= 8 && logn != 0 && (N % 8) == 0) {
-        rc = launch_gemv(x, w8, w_scale, bias, y, M, N, K, logn, rot.groups, d->sms, st);
+    if (M <= 4 && logn != 0) {
+        rc = launch_gemv(x, w8, w_scale, bias, y, M, N, K, logn, rot.groups, d->sms, st, d->status);
         if (rc != GBQ_ENOTSUP) return rc;
     }
     Ws w{(uint8_t *)workspace, ws_bytes};

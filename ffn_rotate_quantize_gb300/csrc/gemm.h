@@ -50,8 +50,9 @@ int launch_bf16_gemm_nn(const void *dy, const void *w, void *dx, int64_t M, int6
                         unsigned int *status, int num_sms, cudaStream_t st);
 
 // Decode GEMV (M <= 8): y[m][n] = dequant(sum_k q[m][k] w8[n][k]) from a rotated+quantized x.
+// Returns GBQ_ENOTSUP (nothing launched) for shapes it does not cover.
 int launch_gemv(const void *x, const int8_t *w8, const float *w_scale, const void *bias, void *y, int64_t M,
-                int64_t N, int64_t K, int logn, int groups, int num_sms, cudaStream_t st);
+                int64_t N, int64_t K, int logn, int groups, int num_sms, cudaStream_t st, unsigned int *status);
 
 // Elementwise helpers.
 cudaError_t launch_dequant(const int32_t *acc, int64_t ld_acc, const float *xs, const float *ws, const void *bias,
@@ -60,6 +61,10 @@ cudaError_t launch_s8_to_f16(const int8_t *q, void *out, int64_t n, cudaStream_t
 cudaError_t launch_scale_rows_s8(const int8_t *w8, const float *s, void *w, int64_t N, int64_t K, cudaStream_t st);
 
 size_t gemm_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t H);
+
+// Launch timing hooks (abi.cu): bracket one kernel launch on stream st.
+void prof_begin(int kind, cudaStream_t st);
+void prof_end(cudaStream_t st);
 
 // Shared with abi.cu.
 int encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint64_t inner, uint64_t outer,

@@ -1,9 +1,212 @@
-// gemm_bf16.cu -- bf16 GEMM for linear_dx.
+// gemm_bf16.cu -- bf16 GEMM dx = dy @ W for linear_dx (fp32 accumulation).
+//
+// What it computes ("The backward: dL/dx, weight-only" on the PyPI page
+// "xpu-kernels 0.2.0"): for y = x @ W^T the input gradient is dx = dy @ W with
+// dy bf16 [M,N], the recovered weight W bf16 [N,K], dx bf16 [M,K].
+//
+// Design: tcgen05 kind::f16 with both operands in shared memory.  A = dy tile
+// (128 rows of M, K-major along N, 128-byte swizzle); B = W tile (256 output
+// columns, contraction along W's rows, i.e. MN-major: four TMA boxes of
+// 64 columns x 64 rows, 128-byte swizzle, LBO = 8 KB between 64-column blocks,
+// SBO = 1 KB between 8-row groups).  Tile 128 x 256 x 64 per stage, 4 stages,
+// accumulators double-buffered in TMEM (2 x 256 columns) so the epilogue of
+// one tile overlaps the main loop of the next.  One persistent CTA per SM.
+// Warps: 0 TMA producer, 1 TMEM owner + MMA issuer, 4-7 epilogue.
+#include "common.cuh"
 #include "gemm.h"
 
 namespace gbq {
-int launch_bf16_gemm_nn(const void *, const void *, void *, int64_t, int64_t, int64_t, unsigned int *, int,
-                        cudaStream_t) {
-    return gbq_fail(GBQ_ENOTSUP, "gbq_linear_dx: not built yet");
+namespace {
+
+constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;
+constexpr int kThreads = 256;
+constexpr uint32_t kAStage = kBM * kBK * 2;  // 16 KB
+constexpr uint32_t kBStage = kBN * kBK * 2;  // 32 KB
+constexpr size_t kSmem = (size_t)kStages * (kAStage + kBStage) + 1024 + 1024;
+
+struct alignas(64) Params {
+    CUtensorMap tm_a;  // dy [M][N] bf16, box {64, 128}
+    CUtensorMap tm_b;  // W  [N][K] bf16, box {64 (K), 64 (N rows)}
+    int64_t M, N, K;
+    __nv_bfloat16 *dx;
+    unsigned int *status;
+};
+
+struct Bars {
+    uint64_t full[kStages], empty[kStages], accfull[2], accempty[2], drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+__global__ void __launch_bounds__(kThreads, 1) bf16_gemm_kernel(const __grid_constant__ Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    uint8_t *abuf = smem;
+    uint8_t *bbuf = smem + kStages * kAStage;
+    Bars *bars = reinterpret_cast<Bars *>(bbuf + kStages * kBStage);
+    volatile int *abort = &bars->abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t m_tiles = (p.M + kBM - 1) / kBM;
+    const int64_t n_tiles = (p.K + kBN - 1) / kBN;
+    const int64_t num_tiles = m_tiles * n_tiles;
+    const int KT = (int)(p.N / kBK);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars->accfull[b], 1);
+            mbar_init(&bars->accempty[b], 4);
+        }
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&p.tm_a);
+        tma_prefetch_desc(&p.tm_b);
+    }
+    if (warp == 1) tmem_alloc(&bars->tmem_base, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int64_t t = blockIdx.x; t < num_tiles && !*abort; t += gridDim.x) {
+                const int m0 = (int)((t % m_tiles) * kBM);
+                const int k0 = (int)((t / m_tiles) * kBN);
+                for (int kt = 0; kt < KT; ++kt) {
+                    if (!mbar_wait(&bars->empty[stage], phase ^ 1, p.status, abort)) break;
+                    mbar_arrive_expect_tx(&bars->full[stage], kAStage + kBStage);
+                    tma_load_2d(abuf + stage * kAStage, &p.tm_a, &bars->full[stage], kt * kBK, m0);
+#pragma unroll
+                    for (int j = 0; j < kBN / 64; ++j)
+                        tma_load_2d(bbuf + stage * kBStage + j * 8192, &p.tm_b, &bars->full[stage], k0 + 64 * j,
+                                    kt * kBK);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16(kBM, kBN, 1, 0, 1);
+            int stage = 0;
+            uint32_t phase = 0, tcount = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++tcount) {
+                const uint32_t ab = tcount & 1u;
+                ok = mbar_wait(&bars->accempty[ab], ((tcount >> 1) & 1u) ^ 1u, p.status, abort);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t d = tmem + ab * 256;
+                for (int kt = 0; kt < KT; ++kt) {
+                    ok = mbar_wait(&bars->full[stage], phase, p.status, abort);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(abuf + stage * kAStage);
+                    const uint32_t b0 = smem_u32(bbuf + stage * kBStage);
+#pragma unroll
+                    for (int k16 = 0; k16 < kBK / 16; ++k16) {
+                        const uint64_t ad = smem_desc(a0 + k16 * 32, 16, 1024, kLayoutSw128);
+                        const uint64_t bd = smem_desc(b0 + k16 * 2048, 8192, 1024, kLayoutSw128);
+                        mma_ss_f16(d, ad, bd, idesc, (kt > 0 || k16 > 0) ? 1u : 0u);
+                    }
+                    tc_commit(&bars->empty[stage]);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (ok) tc_commit(&bars->accfull[ab]);
+            }
+            tc_commit(&bars->drain);
+            mbar_wait(&bars->drain, 0, p.status, abort);
+        }
+    } else if (warp >= 4) {
+        const int q = warp & 3;
+        const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
+        uint32_t tcount = 0;
+        for (int64_t t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tcount) {
+            const int64_t m0 = (t % m_tiles) * kBM;
+            const int64_t k0 = (t / m_tiles) * kBN;
+            const uint32_t ab = tcount & 1u;
+            if (!mbar_wait(&bars->accfull[ab], (tcount >> 1) & 1u, p.status, abort)) break;
+            tc_fence_after();
+            const int64_t m = m0 + q * 32 + lane;
+#pragma unroll 1
+            for (int j = 0; j < kBN / 32; ++j) {
+                uint32_t r[32];
+                tmem_ld32(lane_addr + ab * 256 + 32 * j, r);
+                tc_wait_ld();
+                const int64_t kb = k0 + 32 * j;
+                if (m < p.M && kb < p.K) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+                        w[i] = *reinterpret_cast<uint32_t *>(&h);
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.dx + m * p.K + kb);
+                    if (kb + 32 <= p.K) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                    } else {
+                        for (int i = 0; i < 16 && kb + 2 * i < p.K; ++i)
+                            reinterpret_cast<uint32_t *>(p.dx + m * p.K + kb)[i] = w[i];
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->accempty[ab]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
 }
+
+}  // namespace
+
+int launch_bf16_gemm_nn(const void *dy, const void *w, void *dx, int64_t M, int64_t N, int64_t K,
+                        unsigned int *status, int num_sms, cudaStream_t st) {
+    Params p;
+    memset(&p, 0, sizeof(p));
+    int rc = encode_tmap_2d(&p.tm_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dy, (uint64_t)N, (uint64_t)M, (uint64_t)N * 2,
+                            kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc) return rc;
+    rc = encode_tmap_2d(&p.tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w, (uint64_t)K, (uint64_t)N, (uint64_t)K * 2, 64,
+                        kBK, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc) return rc;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.dx = reinterpret_cast<__nv_bfloat16 *>(dx);
+    p.status = status;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(bf16_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+        if (e != cudaSuccess) return gbq_fail(GBQ_ECUDA, cudaGetErrorString(e));
+        attr = true;
+    }
+    const int64_t tiles = ((M + kBM - 1) / kBM) * ((K + kBN - 1) / kBN);
+    const int grid = (int)(tiles < num_sms ? tiles : num_sms);
+    prof_begin(2, st);
+    bf16_gemm_kernel<<<grid, kThreads, kSmem, st>>>(p);
+    prof_end(st);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? GBQ_OK : gbq_fail(GBQ_ECUDA, cudaGetErrorString(e));
+}
+
 }  // namespace gbq

@@ -387,7 +387,9 @@ int launch_i8gemm(const I8GemmProblem &q, cudaStream_t st) {
     }
     const int64_t tiles = ((q.M + kBN - 1) / kBN) * ((q.N + kBM - 1) / kBM);
     const int grid = (int)(tiles < q.num_sms ? tiles : q.num_sms);
+    prof_begin(1, st);
     i8gemm_kernel<<<grid, kThreads, kSmemBytes, st>>>(p);
+    prof_end(st);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return gbq_fail(GBQ_ECUDA, cudaGetErrorString(e));
     return GBQ_OK;

@@ -1,9 +1,237 @@
-// gemv.cu -- decode GEMV path (M <= 8).
+// gemv.cu -- decode path (M <= 4): y = dequant(quantize(R x) @ W8^T), weight streaming.
+//
+// What it computes: the rotated-INT8 linear layer of the PyPI page
+// "xpu-kernels 0.2.0" ("Use from Python": linear), for a handful of tokens,
+// where the cost is reading the int8 weight once from HBM.
+//
+// Design: one CTA per SM, each owning a contiguous slice of weight rows.  At
+// entry one thread issues bulk copies (cp.async.bulk, mbarrier-tracked) of the
+// whole slice into a shared-memory ring, so the HBM stream starts before any
+// arithmetic.  While the bytes are in flight, the CTA rotates and quantizes x
+// with the same core (and the same fp32 operation order) as the standalone
+// rotate+quantize kernel, so its codes are bit-identical to gbq_quantize_act.
+// Then warps take weight rows, do 16-byte shared loads and int8 dp4a dot
+// products against the quantized x, reduce across lanes and apply the dequant
+// epilogue (fp32(acc) * x_scale, fmaf with the row scale and bias, bf16).
 #include "gemm.h"
+#include "rotate_impl.cuh"
 
 namespace gbq {
-int launch_gemv(const void *, const int8_t *, const float *, const void *, void *, int64_t, int64_t, int64_t, int,
-                int, int, cudaStream_t) {
-    return GBQ_ENOTSUP;
+namespace {
+
+constexpr int kGvThreads = 256;
+constexpr int kGvStages = 4;
+constexpr int kGvMaxM = 4;
+constexpr size_t kGvSmem = 220 * 1024;
+
+struct GemvArgs {
+    const void *x;
+    const int8_t *w8;
+    const float *ws;
+    const __nv_bfloat16 *bias;
+    __nv_bfloat16 *y;
+    int64_t M, N, K;
+    int G;
+    int rows_per_cta;
+    int rows_per_stage;
+    uint32_t stage_bytes;   // rows_per_stage * K, multiple of 128
+    uint32_t x_off, t_off, misc_off;
+    unsigned int *status;
+};
+
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
 }
+
+template <int LOGN>
+__global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(GemvArgs p) {
+    constexpr int NN = 1 << LOGN;
+    constexpr int CPT = (LOGN >= 7) ? 1 : 2;
+    constexpr int TPG = NN / CPT;
+    constexpr int GSTRIDE = NN * (NN + 4) + 16;
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t *stages = smem;
+    int8_t *xq = reinterpret_cast<int8_t *>(smem + p.x_off);
+    float *T = reinterpret_cast<float *>(smem + p.t_off);
+    float *xs_s = reinterpret_cast<float *>(smem + p.misc_off);
+    unsigned *amax_s = reinterpret_cast<unsigned *>(xs_s + kGvMaxM);
+    uint64_t *full = reinterpret_cast<uint64_t *>(amax_s + kGvMaxM);
+    int *abort_flag = reinterpret_cast<int *>(full + kGvStages);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int64_t r0 = (int64_t)blockIdx.x * p.rows_per_cta;
+    const int64_t r1 = min(p.N, r0 + p.rows_per_cta);
+    const int nrows = (int)(r1 - r0);
+    const int nchunks = (nrows + p.rows_per_stage - 1) / p.rows_per_stage;
+
+    if (tid == 0) {
+        for (int s = 0; s < kGvStages; ++s) mbar_init(&full[s], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (tid < kGvMaxM) amax_s[tid] = 0u;
+    __syncthreads();
+    auto issue = [&](int c) {
+        const int rows = min(p.rows_per_stage, nrows - c * p.rows_per_stage);
+        const uint32_t bytes = (uint32_t)rows * (uint32_t)p.K;
+        uint64_t *bar = &full[c % kGvStages];
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_g2s(stages + (size_t)(c % kGvStages) * p.stage_bytes, p.w8 + (r0 + (int64_t)c * p.rows_per_stage) * p.K,
+                 bytes, bar);
+    };
+    if (tid == 0)
+        for (int c = 0; c < nchunks && c < kGvStages; ++c) issue(c);
+
+    // ---- rotate + quantize x (identical arithmetic to rotq_kernel<LOGN, IN_BF16, *>) ----
+    const int row_threads = p.G * TPG;
+    const bool in_row = tid < row_threads;
+    const int g = in_row ? tid / TPG : 0;
+    const int t = in_row ? tid - g * TPG : 0;
+    RotArgs ra{};
+    ra.in0 = p.x;
+    ra.ld_in = p.K;
+    for (int m = 0; m < p.M; ++m) {
+        float v[CPT][NN];
+        rot_group_core<LOGN, IN_BF16>(ra, m, in_row, g, t, T + (size_t)g * GSTRIDE, v);
+        float mx = 0.0f;
+#pragma unroll
+        for (int e = 0; e < CPT; ++e)
+#pragma unroll
+            for (int j = 0; j < NN; ++j) mx = fmaxf(mx, fabsf(v[e][j]));
+        constexpr int W = TPG < 32 ? TPG : 32;
+#pragma unroll
+        for (int o = W / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (in_row && (t & (W - 1)) == 0) atomicMax(&amax_s[m], __float_as_uint(mx));
+        __syncthreads();
+        const float s = __fdiv_rn(__uint_as_float(amax_s[m]), 127.0f);
+        if (tid == 0) xs_s[m] = s;
+        if (in_row) {
+#pragma unroll
+            for (int e = 0; e < CPT; ++e) {
+                const int r = t + e * TPG;
+                uint32_t *dst = reinterpret_cast<uint32_t *>(xq + (int64_t)m * p.K + (int64_t)g * NN * NN + r * NN);
+#pragma unroll
+                for (int j4 = 0; j4 < NN / 4; ++j4) {
+                    uint32_t w = 0;
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        int q = 0;
+                        if (s != 0.0f) q = max(-127, min(127, __float2int_rn(__fdiv_rn(v[e][4 * j4 + h], s))));
+                        w |= (uint32_t)(q & 0xFF) << (8 * h);
+                    }
+                    dst[j4] = w;
+                }
+            }
+        }
+        __syncthreads();
+    }
+
+    // ---- stream the weight slice: dp4a dot products ----
+    const int kq = (int)(p.K / 16);
+    for (int c = 0; c < nchunks; ++c) {
+        if (!mbar_wait(&full[c % kGvStages], (uint32_t)((c / kGvStages) & 1), p.status, abort_flag)) break;
+        const int rows = min(p.rows_per_stage, nrows - c * p.rows_per_stage);
+        const uint8_t *st = stages + (size_t)(c % kGvStages) * p.stage_bytes;
+        for (int j = warp; j < rows; j += kGvThreads / 32) {
+            const uint4 *wr = reinterpret_cast<const uint4 *>(st + (size_t)j * p.K);
+            int acc[kGvMaxM] = {0, 0, 0, 0};
+            for (int i = lane; i < kq; i += 32) {
+                const uint4 w = wr[i];
+#pragma unroll
+                for (int m = 0; m < kGvMaxM; ++m) {
+                    if (m < p.M) {
+                        const uint4 xv = reinterpret_cast<const uint4 *>(xq + (int64_t)m * p.K)[i];
+                        acc[m] = __dp4a((int)w.x, (int)xv.x, acc[m]);
+                        acc[m] = __dp4a((int)w.y, (int)xv.y, acc[m]);
+                        acc[m] = __dp4a((int)w.z, (int)xv.z, acc[m]);
+                        acc[m] = __dp4a((int)w.w, (int)xv.w, acc[m]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < kGvMaxM; ++m)
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], o);
+            const int64_t n = r0 + (int64_t)c * p.rows_per_stage + j;
+            if (lane < p.M) {
+                int a = acc[0];
+#pragma unroll
+                for (int m = 1; m < kGvMaxM; ++m)
+                    if (lane == m) a = acc[m];
+                const float b = p.bias ? __bfloat162float(p.bias[n]) : 0.0f;
+                const float tv = __fmul_rn(__int2float_rn(a), xs_s[lane]);
+                p.y[(int64_t)lane * p.N + n] = __float2bfloat16_rn(__fmaf_rn(tv, __ldg(p.ws + n), b));
+            }
+        }
+        __syncthreads();
+        if (tid == 0 && c + kGvStages < nchunks) issue(c + kGvStages);
+    }
+}
+
+template <int LOGN>
+int launch_gemv_t(const GemvArgs &base, int num_sms, cudaStream_t st) {
+    constexpr int NN = 1 << LOGN;
+    constexpr int CPT = (LOGN >= 7) ? 1 : 2;
+    constexpr int TPG = NN / CPT;
+    GemvArgs a = base;
+    if (a.G * TPG > kGvThreads) return GBQ_ENOTSUP;
+    const size_t x_bytes = (size_t)a.M * a.K;
+    const size_t t_bytes = (size_t)a.G * (NN * (NN + 4) + 16) * 4;
+    const size_t misc = 2 * kGvMaxM * 4 + kGvStages * 8 + 16;
+    const size_t fixed = ((x_bytes + 127) & ~(size_t)127) + ((t_bytes + 127) & ~(size_t)127) + 128;
+    if (fixed + (size_t)kGvStages * a.K > kGvSmem) return GBQ_ENOTSUP;
+    int64_t rpc = (a.N + num_sms - 1) / num_sms;
+    const int64_t grid = (a.N + rpc - 1) / rpc;
+    const int64_t rps_cap = (int64_t)((kGvSmem - fixed) / kGvStages) / a.K;
+    const int64_t rps = rps_cap < rpc ? rps_cap : rpc;
+    a.rows_per_cta = (int)rpc;
+    a.rows_per_stage = (int)rps;
+    a.stage_bytes = (uint32_t)(((size_t)rps * a.K + 127) & ~(size_t)127);
+    a.x_off = (uint32_t)((size_t)kGvStages * a.stage_bytes);
+    a.t_off = a.x_off + (uint32_t)((x_bytes + 127) & ~(size_t)127);
+    a.misc_off = a.t_off + (uint32_t)((t_bytes + 127) & ~(size_t)127);
+    const size_t smem = a.misc_off + misc;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(gemv_kernel<LOGN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGvSmem) !=
+            cudaSuccess)
+            return gbq_fail(GBQ_ECUDA, "gemv: cannot set shared memory size");
+        attr = true;
+    }
+    prof_begin(3, st);
+    gemv_kernel<LOGN><<<(unsigned)grid, kGvThreads, smem, st>>>(a);
+    prof_end(st);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? GBQ_OK : gbq_fail(GBQ_ECUDA, cudaGetErrorString(e));
+}
+
+}  // namespace
+
+int launch_gemv(const void *x, const int8_t *w8, const float *w_scale, const void *bias, void *y, int64_t M, int64_t N,
+                int64_t K, int logn, int groups, int num_sms, cudaStream_t st, unsigned int *status) {
+    if (M < 1 || M > kGvMaxM || K % 128 != 0) return GBQ_ENOTSUP;
+    GemvArgs a{};
+    a.x = x;
+    a.w8 = w8;
+    a.ws = w_scale;
+    a.bias = reinterpret_cast<const __nv_bfloat16 *>(bias);
+    a.y = reinterpret_cast<__nv_bfloat16 *>(y);
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.G = groups;
+    a.status = status;
+    switch (logn) {
+        case 4: return launch_gemv_t<4>(a, num_sms, st);
+        case 5: return launch_gemv_t<5>(a, num_sms, st);
+        case 6: return launch_gemv_t<6>(a, num_sms, st);
+        default: return GBQ_ENOTSUP;
+    }
+}
+
 }  // namespace gbq

@@ -8,6 +8,9 @@
 
 namespace gbq {
 
+void prof_begin(int kind, cudaStream_t st);
+void prof_end(cudaStream_t st);
+
 // Per-row identity "rotation" quantizer (R = I), optional per-column scale on the input.
 struct IdArgs {
     const void *in;           // bf16 [M, ld_in]

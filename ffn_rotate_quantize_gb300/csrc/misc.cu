@@ -102,21 +102,27 @@ cudaError_t launch_dequant(const int32_t *acc, int64_t ld_acc, const float *xs, 
                          ? 1
                          : 0;
     const int64_t work = M * (vec4 ? N / 4 : N);
+    prof_begin(4, st);
     dequant_kernel<<<grid_for(work, 256), 256, 0, st>>>(acc, ld_acc, xs, ws,
                                                          reinterpret_cast<const __nv_bfloat16 *>(bias),
                                                          reinterpret_cast<__nv_bfloat16 *>(y), ld_y, M, N, vec4);
+    prof_end(st);
     return cudaGetLastError();
 }
 
 cudaError_t launch_s8_to_f16(const int8_t *q, void *out, int64_t n, cudaStream_t st) {
     if (n % 16) return cudaErrorInvalidValue;
+    prof_begin(4, st);
     s8_to_f16_kernel<<<grid_for(n / 16, 256), 256, 0, st>>>(q, reinterpret_cast<__half *>(out), n / 16);
+    prof_end(st);
     return cudaGetLastError();
 }
 
 cudaError_t launch_scale_rows_s8(const int8_t *w8, const float *s, void *w, int64_t N, int64_t K, cudaStream_t st) {
     if (K % 16) return cudaErrorInvalidValue;
+    prof_begin(4, st);
     scale_rows_s8_kernel<<<grid_for(N * K / 16, 256), 256, 0, st>>>(w8, s, reinterpret_cast<__nv_bfloat16 *>(w), N, K);
+    prof_end(st);
     return cudaGetLastError();
 }
 

@@ -93,12 +93,13 @@ __global__ void __launch_bounds__(kIdThreads) quant_identity_kernel(IdArgs p) {
 cudaError_t launch_quant_identity(int out_kind, IdArgs a, cudaStream_t st) {
     if (a.K % 8 != 0 || a.K / 8 > (int64_t)kIdThreads * kIdMaxChunks) return cudaErrorNotSupported;
     if (a.M > 0x7fffffff) return cudaErrorInvalidValue;
+    if (out_kind != OUT_S8 && out_kind != OUT_F16Q) return cudaErrorNotSupported;
+    prof_begin(0, st);
     if (out_kind == OUT_S8)
         quant_identity_kernel<OUT_S8><<<(unsigned)a.M, kIdThreads, 0, st>>>(a);
-    else if (out_kind == OUT_F16Q)
-        quant_identity_kernel<OUT_F16Q><<<(unsigned)a.M, kIdThreads, 0, st>>>(a);
     else
-        return cudaErrorNotSupported;
+        quant_identity_kernel<OUT_F16Q><<<(unsigned)a.M, kIdThreads, 0, st>>>(a);
+    prof_end(st);
     return cudaGetLastError();
 }
 

@@ -96,28 +96,17 @@ struct RotqMaxThreads {
     static constexpr int value = LOGN >= 6 ? 256 : 512;
 };
 
-template <int LOGN, int IN, int OUT>
-__global__ void __launch_bounds__(RotqMaxThreads<LOGN>::value) rotq_kernel(RotArgs p) {
+// The rotation of one group (pass 1, transpose through T, pass 2) for the
+// thread (row, g, t); leaves this thread's CPT rows of the rotated group in v.
+// Every thread of the CTA must call it (it contains one __syncthreads()).
+template <int LOGN, int IN>
+__device__ __forceinline__ void rot_group_core(const RotArgs &p, int64_t row, bool active, int g, int t, float *T,
+                                               float (&v)[(LOGN >= 7) ? 1 : 2][1 << LOGN]) {
     constexpr int N = 1 << LOGN;
-    constexpr int CPT = (LOGN >= 7) ? 1 : 2;  // columns (pass 1) / rows (pass 2) per thread
-    constexpr int TPG = N / CPT;              // threads per group
-    constexpr int P = N + 4;                  // padded fp32 row stride in the swap tile
-    constexpr int GSTRIDE = N * P + 16;       // floats per group tile
-
-    extern __shared__ __align__(16) float smem[];
-    const int G = p.G;
-    const int row_threads = G * TPG;
-    const int tid = threadIdx.x;
-    const int rloc = tid / row_threads;
-    const int rem = tid - rloc * row_threads;
-    const int g = rem / TPG;
-    const int t = rem - g * TPG;
-    const int64_t row = (int64_t)blockIdx.x * p.rows_per_cta + rloc;
-    const bool active = row < p.M;
-    float *T = smem + (size_t)(rloc * G + g) * GSTRIDE;
-    unsigned *s_amax = reinterpret_cast<unsigned *>(smem + (size_t)p.rows_per_cta * G * GSTRIDE);
-    if (tid < p.rows_per_cta) s_amax[tid] = 0u;
-
+    constexpr int CPT = (LOGN >= 7) ? 1 : 2;
+    constexpr int TPG = N / CPT;
+    constexpr int P = N + 4;
+    (void)TPG;
     // ---------------- pass 1: CPT columns j = CPT*t + e, all N rows i ----------------
     float c[CPT][N];
     const int64_t goff = (int64_t)g * N * N;
@@ -183,24 +172,26 @@ __global__ void __launch_bounds__(RotqMaxThreads<LOGN>::value) rotq_kernel(RotAr
 #pragma unroll
     for (int e = 0; e < CPT; ++e) hadamard_regs<LOGN>(c[e]);
 
+    if (active) {
 #pragma unroll
-    for (int i = 0; i < N; ++i) {
-        if constexpr (CPT == 2) {
-            *reinterpret_cast<float2 *>(&T[i * P + 2 * t]) = make_float2(c[0][i], c[1][i]);
-        } else {
-            T[i * P + t] = c[0][i];
+        for (int i = 0; i < N; ++i) {
+            if constexpr (CPT == 2) {
+                *reinterpret_cast<float2 *>(&T[i * P + 2 * t]) = make_float2(c[0][i], c[1][i]);
+            } else {
+                T[i * P + t] = c[0][i];
+            }
         }
     }
     __syncthreads();
 
     // ---------------- pass 2: CPT rows r = t + e*TPG, all N columns ----------------
-    float v[CPT][N];
 #pragma unroll
     for (int e = 0; e < CPT; ++e) {
         const int r = t + e * TPG;
 #pragma unroll
         for (int j4 = 0; j4 < N / 4; ++j4) {
-            const float4 f = *reinterpret_cast<const float4 *>(&T[r * P + 4 * j4]);
+            const float4 f = active ? *reinterpret_cast<const float4 *>(&T[r * P + 4 * j4])
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
             v[e][4 * j4 + 0] = f.x;
             v[e][4 * j4 + 1] = f.y;
             v[e][4 * j4 + 2] = f.z;
@@ -212,6 +203,35 @@ __global__ void __launch_bounds__(RotqMaxThreads<LOGN>::value) rotq_kernel(RotAr
             for (int j = 0; j < N; ++j) v[e][j] = __fmul_rn(v[e][j], 0.5f);  // the two H2 levels: (1/sqrt2)^2
         }
     }
+
+}
+
+template <int LOGN, int IN, int OUT>
+__global__ void __launch_bounds__(RotqMaxThreads<LOGN>::value) rotq_kernel(RotArgs p) {
+    constexpr int N = 1 << LOGN;
+    constexpr int CPT = (LOGN >= 7) ? 1 : 2;  // columns (pass 1) / rows (pass 2) per thread
+    constexpr int TPG = N / CPT;              // threads per group
+    constexpr int P = N + 4;                  // padded fp32 row stride in the swap tile
+    constexpr int GSTRIDE = N * P + 16;       // floats per group tile
+    (void)P;
+
+    extern __shared__ __align__(16) float smem[];
+    const int G = p.G;
+    const int row_threads = G * TPG;
+    const int tid = threadIdx.x;
+    const int rloc = tid / row_threads;
+    const int rem = tid - rloc * row_threads;
+    const int g = rem / TPG;
+    const int t = rem - g * TPG;
+    const int64_t row = (int64_t)blockIdx.x * p.rows_per_cta + rloc;
+    const bool active = row < p.M;
+    float *T = smem + (size_t)(rloc * G + g) * GSTRIDE;
+    unsigned *s_amax = reinterpret_cast<unsigned *>(smem + (size_t)p.rows_per_cta * G * GSTRIDE);
+    if (tid < p.rows_per_cta) s_amax[tid] = 0u;
+    const int64_t goff = (int64_t)g * N * N;
+
+    float v[CPT][N];
+    rot_group_core<LOGN, IN>(p, row, active, g, t, T, v);
 
     if constexpr (OUT == OUT_BF16) {
         if (!active) return;

@@ -21,7 +21,9 @@ cudaError_t launch_rotq_t(RotArgs a, cudaStream_t st) {
     }
     const int64_t grid = (a.M + a.rows_per_cta - 1) / a.rows_per_cta;
     if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+    prof_begin(0, st);
     rotq_kernel<LOGN, IN, OUT><<<(unsigned)grid, rt * a.rows_per_cta, smem, st>>>(a);
+    prof_end(st);
     return cudaGetLastError();
 }
 

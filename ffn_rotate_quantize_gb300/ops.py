@@ -50,6 +50,22 @@ def device_status(stream=None) -> int:
     return st.value
 
 
+K_ROTATE, K_I8GEMM, K_BF16GEMM, K_GEMV, K_ELEMWISE = 0, 1, 2, 3, 4
+
+
+def prof_enable(on: bool = True) -> None:
+    """Bracket every library kernel launch with CUDA events (library-owned) from now on."""
+    check(lib().gbq_prof_enable(1 if on else 0))
+
+
+def prof_read(kind: int):
+    """(launches, total ms) of the timed launches of one kernel class."""
+    n = ctypes.c_int(0)
+    ms = ctypes.c_double(0.0)
+    check(lib().gbq_prof_read(kind, ctypes.byref(n), ctypes.byref(ms)))
+    return n.value, ms.value
+
+
 def workspace_size(op: int, M: int, N: int = 0, K: int = 0, H: int = 0) -> int:
     return int(lib().gbq_workspace_size(op, M, N, K, H))
 

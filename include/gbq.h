@@ -161,8 +161,8 @@ int gbq_dequant(const int32_t *acc, int64_t ld_acc, const float *x_scale,
 /*
  * y = linear(x, w8, w_scale, bias) ("Use from Python": bf16 [..,K] -> bf16
  * [..,N]); rotate+quantize, int8 GEMM and the dequant epilogue fused in the
- * GEMM.  Bit-identical to gbq_dequant(gbq_linear_acc(x)).  M = 1..8 runs the
- * decode GEMV path (weight streaming).  Workspace: GBQ_OP_LINEAR.
+ * GEMM.  Bit-identical to gbq_dequant(gbq_linear_acc(x)).  M = 1..4 runs the
+ * decode GEMV path (weight streaming) for a = b <= 64.  Workspace: GBQ_OP_LINEAR.
  */
 int gbq_linear(const void *x, const int8_t *w8, const float *w_scale, const void *bias,
                void *y, int64_t M, int64_t N, int64_t K, gbq_rot rot, void *workspace,
@@ -222,6 +222,25 @@ int gbq_linear_dx_int8(const void *dy, const int8_t *w8, const float *w_scale, v
  * x, xr bf16 [M,K].
  */
 int gbq_rotate_bf16(const void *x, void *xr, int64_t M, int64_t K, gbq_rot rot, void *stream);
+
+/* ---- kernel timing ------------------------------------------------------ */
+
+/* Kernel classes for gbq_prof_read(). */
+enum gbq_kernel {
+    GBQ_K_ROTATE = 0,   /* rotate(+quantize) kernels            */
+    GBQ_K_I8GEMM = 1,   /* exact int8 tensor-core GEMM          */
+    GBQ_K_BF16GEMM = 2, /* bf16 tensor-core GEMM (linear_dx)    */
+    GBQ_K_GEMV = 3,     /* decode GEMV                          */
+    GBQ_K_ELEMWISE = 4  /* dequant / operand coding / scaling   */
+};
+/* on != 0: from now on every kernel launch of the library is bracketed by a
+ * pair of CUDA events recorded on the launch's stream (up to 8192 launches;
+ * later ones are not timed).  Clears the previous record.  The events are
+ * created once per process on the first enable.  on == 0 stops recording. */
+int gbq_prof_enable(int on);
+/* Synchronises the recorded events and returns, for kernel class `kind`, the
+ * number of timed launches and the sum of their durations in milliseconds. */
+int gbq_prof_read(int kind, int *launches, double *total_ms);
 
 #ifdef __cplusplus
 }
