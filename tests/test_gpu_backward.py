@@ -38,7 +38,7 @@ def test_linear_dx(ops, M, N, K, rot):
     w8, s = O.prepare_weight(c["w"], rot)
     what = O.dequant_weight(w8, s, rot)
     dx = ops.linear_dx(bf16_dev(c["dy"]), bf16_dev(what))
-    assert_bf16_parity(bf16_np(dx), O.linear_dx(c["dy"], what))
+    assert_bf16_parity(bf16_np(dx), O.linear_dx(c["dy"], what), acc_len=N)
 
 
 @pytest.mark.parametrize("M,N,K,rot", DX_CASES)
