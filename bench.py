@@ -150,61 +150,73 @@ def run_ours(args):
     peaks = load_peaks()
     bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
 
-    # ---------------- inputs (untimed) ----------------
-    c3 = I.linear_case(PREFILL["M"], PREFILL["K"], PREFILL["N"], n_outliers=I.outlier_count(PREFILL["K"]),
-                       outlier_scale=30.0, bias_std=0.01, seed=0)
-    x3, b3 = bf(c3["x"]), bf(c3["bias"])
-    w83, s3 = G.prepare_weight(bf(c3["w"]), PREFILL["rot"])
-    del c3
-    c2 = I.linear_case(DECODE["M"], DECODE["K"], DECODE["N"], n_outliers=I.outlier_count(DECODE["K"]),
-                       outlier_scale=30.0, bias_std=None, seed=0)
-    x2 = bf(c2["x"])
-    w82, s2 = G.prepare_weight(bf(c2["w"]), DECODE["rot"])
-    # 16 copies of the decode weight (268 MB > L2) so every decode call streams from HBM
-    w82c = [w82.clone() for _ in range(16)]
-    c4 = I.ffn_case(FFN["M"], FFN["d"], FFN["H"], seed=0)
-    x4 = bf(c4["x"])
-    wg8, sg = G.prepare_weight(bf(c4["wg"]), FFN["rot_d"])
-    wu8, su = G.prepare_weight(bf(c4["wu"]), FFN["rot_d"])
-    wd8, sd = G.prepare_weight(bf(c4["wd"]), FFN["rot_h"])
-    del c4
-    c5 = I.backward_case(BWD["M"], BWD["N"], BWD["K"], seed=0)
-    dy5 = bf(c5["dy"])
-    w85, s5 = G.prepare_weight(bf(c5["w"]), BWD["rot"])
-    del c5
+    # ---------------- inputs (untimed), only for the selected rows ----------------
+    only = set(args.only.split(",")) if args.only else None
+    want = lambda *names: only is None or any(n in only for n in names)
     M3, N3, K3 = PREFILL["M"], PREFILL["N"], PREFILL["K"]
-    ws_lin = torch.empty(G.workspace_size(G.OP_LINEAR, M3, N3, K3), dtype=torch.uint8, device=dev)
-    ws_dec = torch.empty(max(G.workspace_size(G.OP_LINEAR, 1, DECODE["N"], DECODE["K"]), 256), dtype=torch.uint8,
-                         device=dev)
-    ws_ffn = torch.empty(G.workspace_size(G.OP_FFN, FFN["M"], 0, FFN["d"], FFN["H"]), dtype=torch.uint8, device=dev)
-    ws_dx8 = torch.empty(G.workspace_size(G.OP_LINEAR_DX_INT8, BWD["M"], BWD["N"], BWD["K"]), dtype=torch.uint8,
-                         device=dev)
-    y3 = torch.empty((M3, N3), dtype=torch.bfloat16, device=dev)
-    acc3 = torch.empty((M3, N3), dtype=torch.int32, device=dev)
-    xs3 = torch.empty((M3,), dtype=torch.float32, device=dev)
-    y3b = torch.empty_like(y3)
-    y2 = torch.empty((1, DECODE["N"]), dtype=torch.bfloat16, device=dev)
-    y4 = torch.empty((FFN["M"], FFN["d"]), dtype=torch.bfloat16, device=dev)
-    what = torch.empty((BWD["N"], BWD["K"]), dtype=torch.bfloat16, device=dev)
-    dx = torch.empty((BWD["M"], BWD["K"]), dtype=torch.bfloat16, device=dev)
-    dx8 = torch.empty_like(dx)
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-
-    ops = [
-        ("linear", lambda i: G.linear(x3, w83, s3, b3, PREFILL["rot"], ws_lin, out=y3)),
-        ("linear_acc", lambda i: G.lib().gbq_linear_acc(
-            G._ptr(x3), G._ptr(w83), G._ptr(acc3), N3, G._ptr(xs3), M3, N3, K3, G._rot(PREFILL["rot"]),
-            G._ptr(ws_lin), ws_lin.numel(), G._stream())),
-        ("dequant", lambda i: G.dequant(acc3, xs3, s3, b3, out=y3b)),
-        ("decode_gemv", lambda i: G.linear(x2, w82c[i % len(w82c)], s2, None, DECODE["rot"], ws_dec, out=y2)),
-        ("ffn_fused", lambda i: G.ffn_fused(x4, wg8, sg, wu8, su, wd8, sd, FFN["rot_d"], FFN["rot_h"], ws_ffn,
-                                            out=y4)),
-        ("dequant_weight", lambda i: G.lib().gbq_dequant_weight(
-            G._ptr(w85), G._ptr(s5), G._ptr(what), BWD["N"], BWD["K"], G._rot(BWD["rot"]), G._stream())),
-        ("linear_dx", lambda i: G.linear_dx(dy5, what, out=dx)),
-        ("linear_dx_int8", lambda i: G.linear_dx_int8(dy5, w85, s5, BWD["rot"], ws_dx8, out=dx8)),
-    ]
+    ops = []
+    if want("linear", "linear_acc", "dequant") or not args.only:
+        c3 = I.linear_case(M3, K3, N3, n_outliers=I.outlier_count(K3), outlier_scale=30.0, bias_std=0.01, seed=0)
+        x3, b3 = bf(c3["x"]), bf(c3["bias"])
+        w83, s3 = G.prepare_weight(bf(c3["w"]), PREFILL["rot"])
+        del c3
+        ws_lin = torch.empty(G.workspace_size(G.OP_LINEAR, M3, N3, K3), dtype=torch.uint8, device=dev)
+        y3 = torch.empty((M3, N3), dtype=torch.bfloat16, device=dev)
+        acc3 = torch.empty((M3, N3), dtype=torch.int32, device=dev)
+        xs3 = torch.empty((M3,), dtype=torch.float32, device=dev)
+        y3b = torch.empty_like(y3)
+        if want("linear"):
+            ops.append(("linear", lambda i: G.linear(x3, w83, s3, b3, PREFILL["rot"], ws_lin, out=y3)))
+        if want("linear_acc", "dequant"):
+            ops.append(("linear_acc", lambda i: G.lib().gbq_linear_acc(
+                G._ptr(x3), G._ptr(w83), G._ptr(acc3), N3, G._ptr(xs3), M3, N3, K3, G._rot(PREFILL["rot"]),
+                G._ptr(ws_lin), ws_lin.numel(), G._stream())))
+        if want("dequant"):
+            ops.append(("dequant", lambda i: G.dequant(acc3, xs3, s3, b3, out=y3b)))
+    if want("decode_gemv"):
+        c2 = I.linear_case(DECODE["M"], DECODE["K"], DECODE["N"], n_outliers=I.outlier_count(DECODE["K"]),
+                           outlier_scale=30.0, bias_std=None, seed=0)
+        x2 = bf(c2["x"])
+        w82, s2 = G.prepare_weight(bf(c2["w"]), DECODE["rot"])
+        # 16 copies of the decode weight (268 MB > L2) so every decode call streams from HBM
+        w82c = [w82.clone() for _ in range(16)]
+        ws_dec = torch.empty(max(G.workspace_size(G.OP_LINEAR, 1, DECODE["N"], DECODE["K"]), 256),
+                             dtype=torch.uint8, device=dev)
+        y2 = torch.empty((1, DECODE["N"]), dtype=torch.bfloat16, device=dev)
+        ops.append(("decode_gemv", lambda i: G.linear(x2, w82c[i % len(w82c)], s2, None, DECODE["rot"], ws_dec,
+                                                      out=y2)))
+    if want("ffn_fused"):
+        c4 = I.ffn_case(FFN["M"], FFN["d"], FFN["H"], seed=0)
+        x4 = bf(c4["x"])
+        wg8, sg = G.prepare_weight(bf(c4["wg"]), FFN["rot_d"])
+        wu8, su = G.prepare_weight(bf(c4["wu"]), FFN["rot_d"])
+        wd8, sd = G.prepare_weight(bf(c4["wd"]), FFN["rot_h"])
+        del c4
+        ws_ffn = torch.empty(G.workspace_size(G.OP_FFN, FFN["M"], 0, FFN["d"], FFN["H"]), dtype=torch.uint8,
+                             device=dev)
+        y4 = torch.empty((FFN["M"], FFN["d"]), dtype=torch.bfloat16, device=dev)
+        ops.append(("ffn_fused", lambda i: G.ffn_fused(x4, wg8, sg, wu8, su, wd8, sd, FFN["rot_d"], FFN["rot_h"],
+                                                       ws_ffn, out=y4)))
+    if want("dequant_weight", "linear_dx", "linear_dx_int8"):
+        c5 = I.backward_case(BWD["M"], BWD["N"], BWD["K"], seed=0)
+        dy5 = bf(c5["dy"])
+        w85, s5 = G.prepare_weight(bf(c5["w"]), BWD["rot"])
+        del c5
+        what = torch.empty((BWD["N"], BWD["K"]), dtype=torch.bfloat16, device=dev)
+        dx = torch.empty((BWD["M"], BWD["K"]), dtype=torch.bfloat16, device=dev)
+        dx8 = torch.empty_like(dx)
+        ws_dx8 = torch.empty(G.workspace_size(G.OP_LINEAR_DX_INT8, BWD["M"], BWD["N"], BWD["K"]),
+                             dtype=torch.uint8, device=dev)
+        if want("dequant_weight", "linear_dx"):
+            ops.append(("dequant_weight", lambda i: G.lib().gbq_dequant_weight(
+                G._ptr(w85), G._ptr(s5), G._ptr(what), BWD["N"], BWD["K"], G._rot(BWD["rot"]), G._stream())))
+        if want("linear_dx"):
+            ops.append(("linear_dx", lambda i: G.linear_dx(dy5, what, out=dx)))
+        if want("linear_dx_int8"):
+            ops.append(("linear_dx_int8", lambda i: G.linear_dx_int8(dy5, w85, s5, BWD["rot"], ws_dx8, out=dx8)))
+    opfn = dict(ops)
     work = {  # algorithmic units per call
         "linear": (2.0 * M3 * N3 * K3, "TOPS"),
         "linear_acc": (2.0 * M3 * N3 * K3, "TOPS"),
@@ -263,34 +275,35 @@ def run_ours(args):
 
     rows = {}
     for name, _ in ops:
-        ms = float(np.median([a.elapsed_time(b) for a, b in evs[name]]))
+        ms = float(np.median([e0.elapsed_time(e1) for e0, e1 in evs[name]]))
         units, unit = work[name]
         scale = 1e-12 if unit in ("TOPS", "TFLOP/s") else 1e-9
         val = units / (ms * 1e-3) * scale
         peak = peaks["hbm"] if unit == "GB/s" else peaks["bf16"]
         rows[name] = {"ms": round(ms, 4), "value": round(val, 2), "unit": unit, "frac_of_peak": round(val / peak, 4)}
 
-    total_ms, total_units = aggregate(rows["linear"]["ms"], work["linear"][0], world)
-    value = total_units / (total_ms * 1e-3) * 1e-12
-
-    # Dominant kernels, timed alone with library-owned CUDA events on their launch stream.
-    gemm_ms = kernel_ms(G, torch, flush, G.K_I8GEMM, ops[0][1], reps=10)
-    achieved = work["linear"][0] / (gemm_ms * 1e-3) * 1e-12
-    roof = {"bound": "tensor", "kernel": "i8gemm_kernel (prefill 1024x14336x4096)", "achieved": round(achieved, 2),
-            "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16"], 4), "traffic": None,
-            "ms": round(gemm_ms, 4),
-            "peak_note": f"dense f16/bf16 tensor peak ({peaks['src']}, burst): the int8 contraction runs exactly "
-                         "on the f16 pipe"}
-    gv_ms = kernel_ms(G, torch, flush, G.K_GEMV, ops[3][1], reps=20)
-    ach = DECODE_BYTES / (gv_ms * 1e-3) * 1e-9
-    dec = {"bound": "hbm", "kernel": "gemv_kernel (decode 1x4096x4096)", "achieved": round(ach, 1),
-           "peak": peaks["hbm"], "unit": "GB/s", "frac": round(ach / peaks["hbm"], 4), "ms": round(gv_ms, 4),
-           "traffic": None}
-
-    e2e = measure_e2e(G, torch, dev, x3, w83, s3, b3, ws_lin, args)
+    value, roof, dec, e2e = None, None, None, None
+    if "linear" in opfn:
+        total_ms, total_units = aggregate(rows["linear"]["ms"], work["linear"][0], world)
+        value = total_units / (total_ms * 1e-3) * 1e-12
+        # Dominant kernels, timed alone with library-owned CUDA events on their launch stream.
+        gemm_ms = kernel_ms(G, torch, flush, G.K_I8GEMM, opfn["linear"], reps=10)
+        achieved = work["linear"][0] / (gemm_ms * 1e-3) * 1e-12
+        roof = {"bound": "tensor", "kernel": "i8gemm_kernel (prefill 1024x14336x4096)",
+                "achieved": round(achieved, 2), "peak": peaks["bf16"], "unit": "TFLOP/s",
+                "frac": round(achieved / peaks["bf16"], 4), "traffic": None, "ms": round(gemm_ms, 4),
+                "peak_note": f"dense f16/bf16 tensor peak ({peaks['src']}, burst): the int8 contraction runs "
+                             "exactly on the f16 pipe"}
+        e2e = measure_e2e(G, torch, dev, x3, w83, s3, b3, ws_lin, args)
+    if "decode_gemv" in opfn:
+        gv_ms = kernel_ms(G, torch, flush, G.K_GEMV, opfn["decode_gemv"], reps=20)
+        ach = DECODE_BYTES / (gv_ms * 1e-3) * 1e-9
+        dec = {"bound": "hbm", "kernel": "gemv_kernel (decode 1x4096x4096)", "achieved": round(ach, 1),
+               "peak": peaks["hbm"], "unit": "GB/s", "frac": round(ach / peaks["hbm"], 4), "ms": round(gv_ms, 4),
+               "traffic": None}
 
     out = {
-        "metric": METRIC, "value": round(value, 2), "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": None if value is None else round(value, 2), "unit": "TOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8", "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": M3, "N": N3, "K": K3, "rotation": "H64(x)H64/64",
@@ -300,7 +313,7 @@ def run_ours(args):
                                                          prof.values())},
         "e2e": e2e, "clocks": clk,
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and not args.only:
         out["cpu_baseline"] = cpu_baseline(args)
     if rank == 0:
         print(json.dumps(out), flush=True)
@@ -415,6 +428,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default="", help="comma-separated rows to run (profiling); default: all")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
