@@ -46,6 +46,7 @@ SIGNATURES = {
     "gbq_linear_dx": [c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp],
     "gbq_linear_dx_int8": [c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, Rot, c_vp, c_sz, c_vp],
     "gbq_rotate_bf16": [c_vp, c_vp, c_i64, c_i64, Rot, c_vp],
+    "gbq_linear_noalloc": [c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, Rot, c_vp],
     "gbq_prof_enable": [ctypes.c_int],
     "gbq_prof_read": [ctypes.c_int, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_double)],
 }

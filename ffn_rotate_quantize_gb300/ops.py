@@ -181,6 +181,18 @@ def linear(x: torch.Tensor, w8: torch.Tensor, w_scale, bias, r, workspace=None, 
     return y
 
 
+def linear_noalloc(x: torch.Tensor, w8: torch.Tensor, w_scale, bias, r, out=None, stream=None):
+    """linear() without a workspace: the library's static device scratch is used (see include/gbq.h)."""
+    _req(x, torch.bfloat16, "x")
+    _req(w8, torch.int8, "w8")
+    M, K = x.shape
+    N = w8.shape[0]
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device) if out is None else out
+    check(lib().gbq_linear_noalloc(_ptr(x), _ptr(w8), _ptr(w_scale), _ptr(bias), _ptr(y), M, N, K, _rot(r),
+                                   _stream(stream)))
+    return y
+
+
 # ------------------------------------------------------------------ FFN
 def ffn_fused(x, wg8, s_gate, wu8, s_up, wd8, s_down, rot_d, rot_h, workspace=None, out=None, stream=None):
     """bf16 x [M,d] -> bf16 y [M,d] = down(quantize(R_h(silu(gate(x)) * up(x))))."""

@@ -168,6 +168,28 @@ int gbq_linear(const void *x, const int8_t *w8, const float *w_scale, const void
                void *y, int64_t M, int64_t N, int64_t K, gbq_rot rot, void *workspace,
                size_t ws_bytes, void *stream);
 
+/*
+ * y = linear(x, w8, w_scale, bias) with no workspace argument: the same
+ * computation and kernels as gbq_linear, with the scratch taken from a 16 MiB
+ * static device array inside the library instead of a caller workspace.  The
+ * paper has no counterpart to this entry point; it exists for callers that
+ * cannot allocate device memory at the point of the call (a plugin inside a
+ * framework that owns all device memory through its own pool, or a
+ * latency-critical loop that cannot afford cudaMalloc's implicit
+ * synchronisation).
+ * Limit: M*K*2 + M*4 bytes (each part rounded up to 256) must fit in 16 MiB,
+ * e.g. M*K <= ~8.3 million; larger calls return GBQ_ENOSPC and launch nothing.
+ * Every device that loads the library holds the 16 MiB until the process
+ * exits.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls share the one array and it keeps the
+ * last call's contents (nothing needs clearing: each call writes all the
+ * scratch it reads); calls that overlap on the GPU -- on different streams,
+ * or from different host threads -- race on it.  Allocates nothing.
+ */
+int gbq_linear_noalloc(const void *x, const int8_t *w8, const float *w_scale, const void *bias,
+                       void *y, int64_t M, int64_t N, int64_t K, gbq_rot rot, void *stream);
+
 /* ---- SwiGLU FFN ------------------------------------------------------- */
 
 /*
