@@ -185,6 +185,16 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int ab_bf16, int 
            | ((uint32_t)(M >> 4) << 24);           // M / 16
 }
 
+// Per-warpgroup register budget (all four warps of a warpgroup execute it).
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------- small math
 // Exact int8 -> fp16 for a pair of signed bytes taken from the low bytes of
 // each 16-bit half of `w` (0x00BB00AA form): value = (0x6400 | (b ^ 0x80)) - 1152.

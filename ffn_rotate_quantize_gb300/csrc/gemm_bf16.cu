@@ -11,7 +11,9 @@
 // SBO = 1 KB between 8-row groups).  Tile 128 x 256 x 64 per stage, 4 stages,
 // accumulators double-buffered in TMEM (2 x 256 columns) so the epilogue of
 // one tile overlaps the main loop of the next.  One persistent CTA per SM.
-// Warps: 0 TMA producer, 1 TMEM owner + MMA issuer, 4-7 epilogue.
+// Warps: 0, 2, 3, 8 TMA producers (one per stage: TMA loads issued by one
+// thread are processed one stage at a time), 1 TMEM owner + MMA issuer, 4-7
+// epilogue.
 #include "common.cuh"
 #include "gemm.h"
 
@@ -19,12 +21,21 @@ namespace gbq {
 namespace {
 
 constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;
-constexpr int kThreads = 256;
+constexpr int kThreads = 288;
+constexpr int kProducers = 4;  // warps 0, 2, 3, 8
+static_assert(kStages % kProducers == 0, "each producer owns whole stages");
+
+__device__ __forceinline__ int producer_id(int warp) {
+    if (warp == 0) return 0;
+    if (warp == 2 || warp == 3) return warp - 1;
+    if (warp == 8) return 3;
+    return -1;
+}
 constexpr uint32_t kAStage = kBM * kBK * 2;  // 16 KB
 constexpr uint32_t kBStage = kBN * kBK * 2;  // 32 KB
 constexpr size_t kSmem = (size_t)kStages * (kAStage + kBStage) + 1024 + 1024;
 
-struct alignas(64) Params {
+struct Params {
     CUtensorMap tm_a;  // dy [M][N] bf16, box {64, 128}
     CUtensorMap tm_b;  // W  [N][K] bf16, box {64 (K), 64 (N rows)}
     int64_t M, N, K;
@@ -73,25 +84,26 @@ __global__ void __launch_bounds__(kThreads, 1) bf16_gemm_kernel(const __grid_con
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    if (warp == 0) {
+    if (producer_id(warp) >= 0) {
+        const uint32_t pid = (uint32_t)producer_id(warp);
         if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            for (int64_t t = blockIdx.x; t < num_tiles && !*abort; t += gridDim.x) {
+            uint32_t gs = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
                 const int m0 = (int)((t % m_tiles) * kBM);
                 const int k0 = (int)((t / m_tiles) * kBN);
                 for (int kt = 0; kt < KT; ++kt) {
-                    if (!mbar_wait(&bars->empty[stage], phase ^ 1, p.status, abort)) break;
+                    const uint32_t my = gs++;
+                    if (my % kProducers != pid) continue;
+                    const int stage = (int)(my % kStages);
+                    ok = mbar_wait(&bars->empty[stage], ((my / kStages) & 1u) ^ 1u, p.status, abort);
+                    if (!ok) break;
                     mbar_arrive_expect_tx(&bars->full[stage], kAStage + kBStage);
                     tma_load_2d(abuf + stage * kAStage, &p.tm_a, &bars->full[stage], kt * kBK, m0);
 #pragma unroll
                     for (int j = 0; j < kBN / 64; ++j)
                         tma_load_2d(bbuf + stage * kBStage + j * 8192, &p.tm_b, &bars->full[stage], k0 + 64 * j,
                                     kt * kBK);
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
                 }
             }
         }
@@ -130,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1) bf16_gemm_kernel(const __grid_con
             tc_commit(&bars->drain);
             mbar_wait(&bars->drain, 0, p.status, abort);
         }
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && warp < 8) {
         const int q = warp & 3;
         const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
         uint32_t tcount = 0;

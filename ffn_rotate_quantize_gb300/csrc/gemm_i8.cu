@@ -9,45 +9,63 @@
 //   * int8 values are exact in fp16, products (|p| <= 127^2) are exact, and an
 //     fp32 accumulator is exact while every partial sum stays below 2^24 in
 //     magnitude; 1024 products of magnitude <= 127^2 sum to < 2^24.
-//   * K is cut into chunks of 1024.  Chunks alternate between two fp32 TMEM
-//     accumulators; the epilogue warps drain a finished chunk (fp32 -> int32,
-//     exact) into an int32 running total kept in TMEM, while the MMA works on
-//     the next chunk in the other accumulator.
+//   * K is cut into chunks of 1024.  After each chunk the epilogue warps drain
+//     the fp32 accumulator (fp32 -> int32, exact) into int32 running totals
+//     held in their registers; the MMA resumes once the accumulator is read.
 //
-// Tile: 128 weight rows (TMEM lanes, MMA M) x 128 tokens (MMA N) x 64 K per
-// pipeline stage.  The weight is the A operand and lives in TMEM: converter
-// warps read the TMA-staged int8 tile from shared memory, widen it to fp16
-// (byte-permute + one half2 subtract per pair) and tcgen05.st it into a 4-stage
-// TMEM ring, so the widened weight never costs shared-memory bandwidth.  The
-// activations are the B operand: fp16-coded integers staged by TMA with the
-// 128-byte swizzle.  One persistent CTA per SM walks the tile list.
+// Tile: 128 weight rows (TMEM lanes, MMA M) x 256 tokens (MMA N).  A tcgen05
+// MMA takes about the same time for N = 128 as for N = 256, so only N = 256
+// reaches the tensor-core peak.  The weight is the A operand and lives in TMEM:
+// a converter warpgroup widens the TMA-staged int8 tile to fp16 in 64-deep
+// sub-steps (byte-permute + one half2 subtract per pair) and tcgen05.st's it
+// into an 8-slot ring, so the widened weight never costs shared-memory
+// bandwidth.  The fp16-coded tokens are the B operand (128-byte swizzle, two
+// 256-row boxes per 128-deep stage).  One persistent CTA per SM.
 //
-// Warp roles (384 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA
-// issuer, warps 4-7 converters, warps 8-11 epilogue (each converter/epilogue
-// warp owns the TMEM lane quadrant warp%4).  Every mbarrier wait is bounded.
+// Warp roles (512 threads): warps 0 and 2 TMA producers (alternate stages),
+// warp 1 TMEM owner + MMA issuer, warps 4-7 converters, warps 8-15 epilogue
+// (warp w owns TMEM lane quadrant w%4 and token half (w/4)%2).  Register
+// budgets per warpgroup (setmaxnreg; launch total 512 x 128 = 65,536):
+// 48 + 88 + 184 + 184 = 504 per lane -> 64,512.  Every mbarrier wait is bounded.
 //
-// TMEM columns: [0,128) A ring (4 x 32), [128,256) acc0, [256,384) acc1,
-// [384,512) int32 totals.
+// TMEM columns: [0,256) A ring (8 x 32), [256,512) accumulator.
 #include "common.cuh"
 #include "gemm.h"
 
 namespace gbq {
 namespace {
 
-constexpr int kBM = 128;
-constexpr int kBN = 128;
-constexpr int kBK = 64;
-constexpr int kStages = 6;
-constexpr int kAStages = 4;
-constexpr int kChunkStages = 16;  // 16 * 64 = 1024 K per fp32 accumulator
+constexpr int kBM = 128;                 // weight rows per tile
+constexpr int kBN = 256;                 // tokens per tile
+constexpr int kBK = 128;                 // K per shared-memory stage
+constexpr int kSub = 64;                 // K per converter / A-ring sub-step
+constexpr int kSubs = kBK / kSub;        // sub-steps per stage
+constexpr int kStages = 2;
+constexpr int kAStages = 8;
+constexpr int kChunkSubs = 1024 / kSub;  // sub-steps per exact fp32 chunk
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColA = 0, kColAcc0 = 128, kColAcc1 = 256, kColTot = 384;
-constexpr int kThreads = 384;
-constexpr uint32_t kBStageBytes = kBN * kBK * 2;  // 16 KB fp16 tokens
-constexpr uint32_t kWStageBytes = kBM * kBK;      // 8 KB int8 weights
+constexpr uint32_t kColA = 0, kColAcc = 256;
+constexpr int kProducers = 2;  // warps 0 and 2
+constexpr int kThreads = 512;
+constexpr int kEpiWarps = 8;
+constexpr int kRegsWG0 = 48, kRegsConv = 88, kRegsEpi = 184;
+static_assert(128 * (kRegsWG0 + kRegsConv + 2 * kRegsEpi) <= 65536, "register split exceeds the launch total");
+static_assert(kStages % kProducers == 0, "each producer owns whole stages");
+static_assert(kChunkSubs % kSubs == 0, "chunks end on stage boundaries");
+
+// Producer index of a warp, or -1.
+__device__ __forceinline__ int producer_id(int warp) {
+    if (warp == 0) return 0;
+    if (warp == 2) return 1;
+    return -1;
+}
+
+constexpr uint32_t kTokBox = 256 * 128;             // one 256-row x 128-byte token box (64 K)
+constexpr uint32_t kBStageBytes = kSubs * kTokBox;  // 64 KB fp16 tokens
+constexpr uint32_t kWStageBytes = kBM * kBK;        // 16 KB int8 weights (one 128 x 128-byte box)
 constexpr size_t kSmemBytes = (size_t)kStages * (kBStageBytes + kWStageBytes) + 1024 /*barriers*/ + 1024 /*align*/;
 
-struct alignas(64) Params {
+struct Params {
     CUtensorMap tm_b;
     CUtensorMap tm_w0;
     CUtensorMap tm_w1;
@@ -69,8 +87,8 @@ struct Bars {
     uint64_t empty[kStages];
     uint64_t afull[kAStages];
     uint64_t aempty[kAStages];
-    uint64_t accfull[2];
-    uint64_t accempty[2];
+    uint64_t accfull;
+    uint64_t accempty;
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -107,21 +125,21 @@ __global__ void __launch_bounds__(kThreads, 1) i8gemm_kernel(const __grid_consta
     const int64_t m_tiles = (p.M + kBN - 1) / kBN;
     const int64_t n_tiles = (p.N + kBM - 1) / kBM;
     const int64_t num_tiles = m_tiles * n_tiles;
-    const int KT = (int)(p.K / kBK);
+    const int KT = (int)((p.K + kBK - 1) / kBK);  // stages per tile (the K tail reads zeros)
+    const int tile_subs = KT * kSubs;
+    const int nchunks = (tile_subs + kChunkSubs - 1) / kChunkSubs;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&bars->full[s], 1);
-            mbar_init(&bars->empty[s], 1 + 4);
+            mbar_init(&bars->empty[s], 1 + 4 * kSubs);  // MMA commit + every converter warp per sub-step
         }
         for (int a = 0; a < kAStages; ++a) {
             mbar_init(&bars->afull[a], 4);
             mbar_init(&bars->aempty[a], 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&bars->accfull[b], 1);
-            mbar_init(&bars->accempty[b], 4);
-        }
+        mbar_init(&bars->accfull, 1);
+        mbar_init(&bars->accempty, kEpiWarps);
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
         fence_mbar_init();
@@ -134,143 +152,152 @@ __global__ void __launch_bounds__(kThreads, 1) i8gemm_kernel(const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+    const int wg = warp >> 2;
 
-    if (warp == 0) {
-        // ------------------------------------------------ TMA producer
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            for (int64_t t = blockIdx.x; t < num_tiles && !*abort; t += gridDim.x) {
-                int64_t n0, m0;
-                tile_coords(t, m_tiles, &n0, &m0);
-                const bool src1 = n0 >= p.n_split;
-                const CUtensorMap *tw = src1 ? &p.tm_w1 : &p.tm_w0;
-                const int wrow = (int)(src1 ? n0 - p.n_split : n0);
-                for (int kt = 0; kt < KT; ++kt) {
-                    if (!mbar_wait(&bars->empty[stage], phase ^ 1, p.status, abort)) break;
-                    mbar_arrive_expect_tx(&bars->full[stage], kBStageBytes + kWStageBytes);
-                    if (p.w_layout == W_KMAJOR)
-                        tma_load_2d(wbuf + stage * kWStageBytes, tw, &bars->full[stage], kt * kBK, wrow);
-                    else
-                        tma_load_2d(wbuf + stage * kWStageBytes, tw, &bars->full[stage], wrow, kt * kBK);
-                    tma_load_2d(bbuf + stage * kBStageBytes, &p.tm_b, &bars->full[stage], kt * kBK, (int)m0);
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
-                }
-            }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16(kBM, kBN, 0, 0, 0);
-            int stage = 0, astage = 0;
-            uint32_t phase = 0, aphase = 0;
-            uint32_t chunk = 0;
-            bool ok = true;
-            for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                uint32_t acc_col = kColAcc0;
-                for (int kt = 0; kt < KT && ok; ++kt) {
-                    const int cpos = kt % kChunkStages;
-                    if (cpos == 0) {
-                        const uint32_t ab = chunk & 1u;
-                        ok = mbar_wait(&bars->accempty[ab], ((chunk >> 1) & 1u) ^ 1u, p.status, abort);
+    if (wg == 0) {
+        setmaxnreg_dec<kRegsWG0>();
+        if (producer_id(warp) >= 0) {
+            // ------------------------------------------------ TMA producers (alternate stages)
+            const uint32_t pid = (uint32_t)producer_id(warp);
+            if (lane == 0) {
+                uint32_t gs = 0;
+                bool ok = true;
+                for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                    int64_t n0, m0;
+                    tile_coords(t, m_tiles, &n0, &m0);
+                    const bool src1 = n0 >= p.n_split;
+                    const CUtensorMap *tw = src1 ? &p.tm_w1 : &p.tm_w0;
+                    const int wrow = (int)(src1 ? n0 - p.n_split : n0);
+                    for (int kt = 0; kt < KT; ++kt) {
+                        const uint32_t my = gs++;
+                        if (my % kProducers != pid) continue;
+                        const int stage = (int)(my % kStages);
+                        ok = mbar_wait(&bars->empty[stage], ((my / kStages) & 1u) ^ 1u, p.status, abort);
                         if (!ok) break;
-                        acc_col = ab ? kColAcc1 : kColAcc0;
-                    }
-                    ok = mbar_wait(&bars->full[stage], phase, p.status, abort) &&
-                         mbar_wait(&bars->afull[astage], aphase, p.status, abort);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t b_base = smem_u32(bbuf + stage * kBStageBytes);
+                        uint64_t *fb = &bars->full[stage];
+                        mbar_arrive_expect_tx(fb, kBStageBytes + kWStageBytes);
+                        uint8_t *wdst = wbuf + stage * kWStageBytes;
+                        if (p.w_layout == W_KMAJOR)
+                            tma_load_2d(wdst, tw, fb, kt * kBK, wrow);  // 128 rows x 128 K bytes
+                        else
+                            tma_load_2d(wdst, tw, fb, wrow, kt * kBK);  // 128 contraction rows x 128 columns
+                        uint8_t *bdst = bbuf + stage * kBStageBytes;
 #pragma unroll
-                    for (int k16 = 0; k16 < kBK / 16; ++k16) {
-                        const uint64_t bdesc = smem_desc(b_base + k16 * 32, 16, 1024, kLayoutSw128);
-                        mma_ts_f16(tmem + acc_col, tmem + kColA + astage * 32 + k16 * 8, bdesc, idesc,
-                                   (cpos > 0 || k16 > 0) ? 1u : 0u);
-                    }
-                    tc_commit(&bars->empty[stage]);
-                    tc_commit(&bars->aempty[astage]);
-                    if (cpos == kChunkStages - 1 || kt == KT - 1) {
-                        tc_commit(&bars->accfull[chunk & 1u]);
-                        ++chunk;
-                    }
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
-                    if (++astage == kAStages) {
-                        astage = 0;
-                        aphase ^= 1;
+                        for (int b = 0; b < kSubs; ++b)
+                            tma_load_2d(bdst + b * kTokBox, &p.tm_b, fb, kt * kBK + b * kSub, (int)m0);
                     }
                 }
             }
-            // Let every issued MMA finish before the CTA can release TMEM.
-            tc_commit(&bars->drain);
-            mbar_wait(&bars->drain, 0, p.status, abort);
+        } else if (warp == 1) {
+            // ------------------------------------------------ MMA issuer
+            if (lane == 0) {
+                constexpr uint32_t idesc = idesc_f16(kBM, kBN, 0, 0, 0);
+                uint32_t gs = 0, gsub = 0, chunk = 0;
+                bool ok = true;
+                for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                    for (int kt = 0; kt < KT && ok; ++kt) {
+                        const uint32_t my = gs++;
+                        const int stage = (int)(my % kStages);
+                        ok = mbar_wait(&bars->full[stage], (my / kStages) & 1u, p.status, abort);
+                        if (!ok) break;
+                        const uint32_t b_stage = smem_u32(bbuf + stage * kBStageBytes);
+                        for (int sub = 0; sub < kSubs && ok; ++sub) {
+                            const uint32_t ms = gsub++;
+                            const int tsub = kt * kSubs + sub;  // sub-step within the tile
+                            const int cpos = tsub % kChunkSubs;
+                            if (cpos == 0) {  // a new chunk: the accumulator must have been drained
+                                ok = mbar_wait(&bars->accempty, (chunk & 1u) ^ 1u, p.status, abort);
+                                if (!ok) break;
+                            }
+                            const int as = (int)(ms % kAStages);
+                            ok = mbar_wait(&bars->afull[as], (ms / kAStages) & 1u, p.status, abort);
+                            if (!ok) break;
+                            tc_fence_after();
+#pragma unroll
+                            for (int k16 = 0; k16 < kSub / 16; ++k16) {
+                                const uint64_t bdesc =
+                                    smem_desc(b_stage + sub * kTokBox + k16 * 32, 16, 1024, kLayoutSw128);
+                                mma_ts_f16(tmem + kColAcc, tmem + kColA + as * 32 + k16 * 8, bdesc, idesc,
+                                           (cpos > 0 || k16 > 0) ? 1u : 0u);
+                            }
+                            tc_commit(&bars->aempty[as]);
+                            if (cpos == kChunkSubs - 1 || tsub == tile_subs - 1) {
+                                tc_commit(&bars->accfull);
+                                ++chunk;
+                            }
+                        }
+                        tc_commit(&bars->empty[stage]);
+                    }
+                }
+                // Let every issued MMA finish before the CTA can release TMEM.
+                tc_commit(&bars->drain);
+                mbar_wait(&bars->drain, 0, p.status, abort);
+            }
         }
-    } else if (warp >= 4 && warp < 8) {
+    } else if (wg == 1) {
+        setmaxnreg_dec<kRegsConv>();
         // ------------------------------------------------ int8 -> fp16 converters (A operand into TMEM)
         const int q = warp & 3;
         const int r = q * 32 + lane;  // TMEM lane = A row of the tile
         const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
-        int stage = 0, astage = 0;
-        uint32_t phase = 0, aphase = 0;
+        uint32_t gs = 0, gsub = 0;
         bool ok = true;
         for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-            for (int kt = 0; kt < KT; ++kt) {
-                ok = mbar_wait(&bars->full[stage], phase, p.status, abort);
-                if (!ok) break;
-                uint32_t a[32];
+            for (int kt = 0; kt < KT && ok; ++kt) {
+                const uint32_t mstage = gs++;
+                const int stage = (int)(mstage % kStages);
                 const uint8_t *ws = wbuf + stage * kWStageBytes;
-                if (p.w_layout == W_KMAJOR) {
-                    // Row r: 64 bytes, 64-byte swizzle (16-byte chunk c stored at c ^ ((r >> 1) & 3)).
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int pc = c ^ ((r >> 1) & 3);
-                        const uint4 v = *reinterpret_cast<const uint4 *>(ws + r * 64 + pc * 16);
-                        s8x4_to_f16x4(v.x, a[8 * c + 0], a[8 * c + 1]);
-                        s8x4_to_f16x4(v.y, a[8 * c + 2], a[8 * c + 3]);
-                        s8x4_to_f16x4(v.z, a[8 * c + 4], a[8 * c + 5]);
-                        s8x4_to_f16x4(v.w, a[8 * c + 6], a[8 * c + 7]);
-                    }
-                } else {
-                    // Tile [64 contraction rows][128 output columns], 128-byte swizzle:
-                    // byte (n, r) at n*128 + 16*((r >> 4) ^ (n & 7)) + (r & 15).
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int n = 2 * j;
-                        const uint32_t b0 = ws[n * 128 + 16 * ((r >> 4) ^ (n & 7)) + (r & 15)];
-                        const uint32_t b1 = ws[(n + 1) * 128 + 16 * ((r >> 4) ^ ((n + 1) & 7)) + (r & 15)];
-                        a[j] = s8pair_to_f16x2(b0 | (b1 << 16));
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->empty[stage]);
-                ok = mbar_wait(&bars->aempty[astage], aphase ^ 1, p.status, abort);
+                ok = mbar_wait(&bars->full[stage], (mstage / kStages) & 1u, p.status, abort);
                 if (!ok) break;
-                tc_fence_after();
-                tmem_st32(lane_addr + kColA + astage * 32, a);
-                tc_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->afull[astage]);
-                if (++stage == kStages) {
-                    stage = 0;
-                    phase ^= 1;
-                }
-                if (++astage == kAStages) {
-                    astage = 0;
-                    aphase ^= 1;
+                for (int sub = 0; sub < kSubs; ++sub) {
+                    const uint32_t my = gsub++;
+                    const int astage = (int)(my % kAStages);
+                    uint32_t a[32];
+                    if (p.w_layout == W_KMAJOR) {
+                        // Row r: 128 bytes, 128-byte swizzle (16-byte chunk c stored at c ^ (r & 7));
+                        // this sub-step is the 64-byte half `sub` of the row.
+                        const uint8_t *row = ws + r * 128;
+                        uint4 v[4];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            v[c] = *reinterpret_cast<const uint4 *>(row + (((4 * sub + c) ^ (r & 7)) * 16));
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            s8x4_to_f16x4(v[c].x, a[8 * c + 0], a[8 * c + 1]);
+                            s8x4_to_f16x4(v[c].y, a[8 * c + 2], a[8 * c + 3]);
+                            s8x4_to_f16x4(v[c].z, a[8 * c + 4], a[8 * c + 5]);
+                            s8x4_to_f16x4(v[c].w, a[8 * c + 6], a[8 * c + 7]);
+                        }
+                    } else {
+                        // Box [128 contraction rows][128 output columns], 128-byte swizzle:
+                        // byte (n, r) at n*128 + 16*((r >> 4) ^ (n & 7)) + (r & 15).
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int n = sub * kSub + 2 * j;
+                            const uint32_t b0 = ws[n * 128 + 16 * ((r >> 4) ^ (n & 7)) + (r & 15)];
+                            const uint32_t b1 = ws[(n + 1) * 128 + 16 * ((r >> 4) ^ ((n + 1) & 7)) + (r & 15)];
+                            a[j] = s8pair_to_f16x2(b0 | (b1 << 16));
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->empty[stage]);
+                    ok = mbar_wait(&bars->aempty[astage], ((my / kAStages) & 1u) ^ 1u, p.status, abort);
+                    if (!ok) break;
+                    tc_fence_after();
+                    tmem_st32(lane_addr + kColA + astage * 32, a);
+                    tc_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->afull[astage]);
                 }
             }
         }
-    } else if (warp >= 8) {
+    } else {
+        setmaxnreg_inc<kRegsEpi>();
         // ------------------------------------------------ epilogue: drain chunks, write outputs
         const int q = warp & 3;
-        const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
-        const int nchunks = (KT + kChunkStages - 1) / kChunkStages;
+        const int h = (warp >> 2) & 1;  // token half of the tile
+        const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16) + kColAcc + h * 128;
         uint32_t chunk = 0;
         bool ok = true;
         for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
@@ -283,54 +310,49 @@ __global__ void __launch_bounds__(kThreads, 1) i8gemm_kernel(const __grid_consta
                 ws = n < p.n_split ? __ldg(p.w_scale0 + n) : __ldg(p.w_scale1 + (n - p.n_split));
                 if (p.bias) bias = __bfloat162float(p.bias[n]);
             }
+            int32_t tot[128];  // exact running sums for this thread's 128 token columns
+#pragma unroll
+            for (int i = 0; i < 128; ++i) tot[i] = 0;
             for (int c = 0; c < nchunks; ++c) {
-                const uint32_t ab = chunk & 1u;
-                ok = mbar_wait(&bars->accfull[ab], (chunk >> 1) & 1u, p.status, abort);
+                ok = mbar_wait(&bars->accfull, chunk & 1u, p.status, abort);
                 if (!ok) break;
                 tc_fence_after();
-                const bool last = (c == nchunks - 1);
-                const uint32_t acc_col = ab ? kColAcc1 : kColAcc0;
-#pragma unroll 1
-                for (int j = 0; j < kBN / 32; ++j) {
-                    uint32_t r[32], tot[32];
-                    tmem_ld32(lane_addr + acc_col + 32 * j, r);
-                    if (c > 0) tmem_ld32(lane_addr + kColTot + 32 * j, tot);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t rr[32];
+                    tmem_ld32(lane_addr + 32 * j, rr);
                     tc_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int32_t part = __float2int_rn(__uint_as_float(r[i]));
-                        tot[i] = (uint32_t)((c > 0 ? (int32_t)tot[i] : 0) + part);
-                    }
-                    if (!last) {
-                        tmem_st32(lane_addr + kColTot + 32 * j, tot);
-                        continue;
-                    }
-                    // Final chunk: write the 32 token rows m0 + 32j + i of column n.
-                    const int64_t mb = m0 + 32 * j;
-                    float xs_l = 0.0f;
-                    if (p.epi != EPI_ACC_I32 && mb + lane < p.M) xs_l = __ldg(p.x_scale + mb + lane);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float xs = __shfl_sync(0xffffffffu, xs_l, i);
-                        const int64_t m = mb + i;
-                        if (!n_ok || m >= p.M) continue;
-                        const int32_t acc = (int32_t)tot[i];
-                        if (p.epi == EPI_ACC_I32) {
-                            reinterpret_cast<int32_t *>(p.out)[m * p.ld_out + n] = acc;
-                        } else if (p.epi == EPI_DEQUANT_BF16) {
-                            const float tv = __fmul_rn(__int2float_rn(acc), xs);
-                            const float y = __fmaf_rn(tv, ws, bias);
-                            reinterpret_cast<__nv_bfloat16 *>(p.out)[m * p.ld_out + n] = __float2bfloat16_rn(y);
-                        } else {
-                            reinterpret_cast<float *>(p.out)[m * p.ld_out + n] = __fmul_rn(__int2float_rn(acc), xs);
-                        }
-                    }
+                    for (int i = 0; i < 32; ++i) tot[32 * j + i] += __float2int_rn(__uint_as_float(rr[i]));
                 }
-                if (!last) tc_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->accempty[ab]);
+                if (lane == 0) mbar_arrive(&bars->accempty);  // this warp is done with the accumulator
                 ++chunk;
+            }
+            if (!ok) break;
+            // Write token rows m0 + 128h + 32j + i of output column n.
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t mb = m0 + 128 * h + 32 * j;
+                float xs_l = 0.0f;
+                if (p.epi != EPI_ACC_I32 && mb + lane < p.M) xs_l = __ldg(p.x_scale + mb + lane);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float xs = __shfl_sync(0xffffffffu, xs_l, i);
+                    const int64_t m = mb + i;
+                    if (!n_ok || m >= p.M) continue;
+                    const int32_t acc = tot[32 * j + i];
+                    if (p.epi == EPI_ACC_I32) {
+                        reinterpret_cast<int32_t *>(p.out)[m * p.ld_out + n] = acc;
+                    } else if (p.epi == EPI_DEQUANT_BF16) {
+                        const float tv = __fmul_rn(__int2float_rn(acc), xs);
+                        const float y = __fmaf_rn(tv, ws, bias);
+                        reinterpret_cast<__nv_bfloat16 *>(p.out)[m * p.ld_out + n] = __float2bfloat16_rn(y);
+                    } else {
+                        reinterpret_cast<float *>(p.out)[m * p.ld_out + n] = __fmul_rn(__int2float_rn(acc), xs);
+                    }
+                }
             }
         }
     }
@@ -351,16 +373,16 @@ int launch_i8gemm(const I8GemmProblem &q, cudaStream_t st) {
     int rc;
     // Activations: fp16 [M][K], box 64 x 128, 128-byte swizzle.
     rc = encode_tmap_2d(&p.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, q.b_f16, (uint64_t)q.K, (uint64_t)q.M,
-                        (uint64_t)q.K * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B);
+                        (uint64_t)q.K * 2, kSub, kBN, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
     for (int s = 0; s < 2; ++s) {
         const int8_t *w = s ? q.w1 : q.w0;
         const int64_t rows = s ? q.w_rows_total1 : q.w_rows_total0;
         CUtensorMap *tm = s ? &p.tm_w1 : &p.tm_w0;
-        if (q.w_layout == W_KMAJOR)  // [rows][K], box 64 B x 128 rows, 64-byte swizzle
+        if (q.w_layout == W_KMAJOR)  // [rows][K], box 128 B x 128 rows, 128-byte swizzle
             rc = encode_tmap_2d(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, (uint64_t)q.K, (uint64_t)rows,
-                                (uint64_t)q.ld_w, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_64B);
-        else  // [K rows][ld_w]: box 128 B (output columns) x 64 rows, 128-byte swizzle
+                                (uint64_t)q.ld_w, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+        else  // [K rows][ld_w]: box 128 B (output columns) x kBK rows, 128-byte swizzle
             rc = encode_tmap_2d(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, (uint64_t)q.N, (uint64_t)rows,
                                 (uint64_t)q.ld_w, kBM, kBK, CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc) return rc;
@@ -383,6 +405,12 @@ int launch_i8gemm(const I8GemmProblem &q, cudaStream_t st) {
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(i8gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess) return gbq_fail(GBQ_ECUDA, cudaGetErrorString(e));
+        // The per-warpgroup register split (setmaxnreg) must fit in what the block is launched with.
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, i8gemm_kernel);
+        if (e != cudaSuccess) return gbq_fail(GBQ_ECUDA, cudaGetErrorString(e));
+        if ((long)fa.numRegs * kThreads < 128L * (kRegsWG0 + kRegsConv + 2 * kRegsEpi))
+            return gbq_fail(GBQ_ECUDA, "int8 GEMM: register split exceeds the launch allocation");
         attr = true;
     }
     const int64_t tiles = ((q.M + kBN - 1) / kBN) * ((q.N + kBM - 1) / kBM);

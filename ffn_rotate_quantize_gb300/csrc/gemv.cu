@@ -48,15 +48,13 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
 
 template <int LOGN>
 __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(GemvArgs p) {
-    constexpr int NN = 1 << LOGN;
-    constexpr int CPT = (LOGN >= 7) ? 1 : 2;
-    constexpr int TPG = NN / CPT;
-    constexpr int GSTRIDE = NN * (NN + 4) + 16;
+    using Geo = RotGeom<LOGN>;
+    constexpr int NP = Geo::NP, TPG = Geo::TPG;
 
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *stages = smem;
     int8_t *xq = reinterpret_cast<int8_t *>(smem + p.x_off);
-    float *T = reinterpret_cast<float *>(smem + p.t_off);
+    float2 *T = reinterpret_cast<float2 *>(smem + p.t_off);
     float *xs_s = reinterpret_cast<float *>(smem + p.misc_off);
     unsigned *amax_s = reinterpret_cast<unsigned *>(xs_s + kGvMaxM);
     uint64_t *full = reinterpret_cast<uint64_t *>(amax_s + kGvMaxM);
@@ -87,7 +85,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(GemvArgs p) {
     if (tid == 0)
         for (int c = 0; c < nchunks && c < kGvStages; ++c) issue(c);
 
-    // ---- rotate + quantize x (identical arithmetic to rotq_kernel<LOGN, IN_BF16, *>) ----
+    // ---- rotate + quantize x (the same core and operation order as rotq_kernel) ----
     const int row_threads = p.G * TPG;
     const bool in_row = tid < row_threads;
     const int g = in_row ? tid / TPG : 0;
@@ -96,13 +94,11 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(GemvArgs p) {
     ra.in0 = p.x;
     ra.ld_in = p.K;
     for (int m = 0; m < p.M; ++m) {
-        float v[CPT][NN];
-        rot_group_core<LOGN, IN_BF16>(ra, m, in_row, g, t, T + (size_t)g * GSTRIDE, v);
+        float2 v[NP];
+        rot_group_core<LOGN, IN_BF16>(ra, m, in_row, g, t, T + (size_t)g * Geo::TILE, v);
         float mx = 0.0f;
 #pragma unroll
-        for (int e = 0; e < CPT; ++e)
-#pragma unroll
-            for (int j = 0; j < NN; ++j) mx = fmaxf(mx, fabsf(v[e][j]));
+        for (int j = 0; j < NP; ++j) mx = fmaxf(mx, pair_max_abs(v[j]));
         constexpr int W = TPG < 32 ? TPG : 32;
 #pragma unroll
         for (int o = W / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -111,22 +107,11 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(GemvArgs p) {
         const float s = __fdiv_rn(__uint_as_float(amax_s[m]), 127.0f);
         if (tid == 0) xs_s[m] = s;
         if (in_row) {
+            uint32_t words[2][NP / 4];
+            quant_codes<NP>(v, s, words);
 #pragma unroll
-            for (int e = 0; e < CPT; ++e) {
-                const int r = t + e * TPG;
-                uint32_t *dst = reinterpret_cast<uint32_t *>(xq + (int64_t)m * p.K + (int64_t)g * NN * NN + r * NN);
-#pragma unroll
-                for (int j4 = 0; j4 < NN / 4; ++j4) {
-                    uint32_t w = 0;
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        int q = 0;
-                        if (s != 0.0f) q = max(-127, min(127, __float2int_rn(__fdiv_rn(v[e][4 * j4 + h], s))));
-                        w |= (uint32_t)(q & 0xFF) << (8 * h);
-                    }
-                    dst[j4] = w;
-                }
-            }
+            for (int h = 0; h < 2; ++h) store_codes<OUT_S8, NP / 4>(xq, (int64_t)m * p.K + out_offset<LOGN>(g, t, h),
+                                                                   words[h]);
         }
         __syncthreads();
     }
@@ -175,13 +160,11 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(GemvArgs p) {
 
 template <int LOGN>
 int launch_gemv_t(const GemvArgs &base, int num_sms, cudaStream_t st) {
-    constexpr int NN = 1 << LOGN;
-    constexpr int CPT = (LOGN >= 7) ? 1 : 2;
-    constexpr int TPG = NN / CPT;
+    constexpr int TPG = RotGeom<LOGN>::TPG;
     GemvArgs a = base;
     if (a.G * TPG > kGvThreads) return GBQ_ENOTSUP;
     const size_t x_bytes = (size_t)a.M * a.K;
-    const size_t t_bytes = (size_t)a.G * (NN * (NN + 4) + 16) * 4;
+    const size_t t_bytes = (size_t)a.G * RotGeom<LOGN>::TILE * sizeof(float2);
     const size_t misc = 2 * kGvMaxM * 4 + kGvStages * 8 + 16;
     const size_t fixed = ((x_bytes + 127) & ~(size_t)127) + ((t_bytes + 127) & ~(size_t)127) + 128;
     if (fixed + (size_t)kGvStages * a.K > kGvSmem) return GBQ_ENOTSUP;

@@ -20,9 +20,9 @@ cudaError_t launch_rotb(int logn, int in_kind, RotArgs a, cudaStream_t st) {
 // moved onto the contraction index, "The backward: dL/dx, weight-only").
 // ---------------------------------------------------------------------------
 constexpr int kIdThreads = 256;
-constexpr int kIdMaxChunks = 16;  // K <= 256 * 16 * 8 = 32768
+constexpr int kIdChunkCap = 16;  // K <= 256 * 16 * 8 = 32768
 
-template <int OUT>
+template <int OUT, int kIdMaxChunks>
 __global__ void __launch_bounds__(kIdThreads) quant_identity_kernel(IdArgs p) {
     __shared__ float s_warp[kIdThreads / 32];
     const int64_t row = blockIdx.x;
@@ -48,6 +48,9 @@ __global__ void __launch_bounds__(kIdThreads) quant_identity_kernel(IdArgs p) {
             }
 #pragma unroll
             for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[c][e]));
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[c][e] = 0.0f;
         }
     }
 #pragma unroll
@@ -59,46 +62,80 @@ __global__ void __launch_bounds__(kIdThreads) quant_identity_kernel(IdArgs p) {
     for (int w = 0; w < kIdThreads / 32; ++w) amax = fmaxf(amax, s_warp[w]);
     const float s = __fdiv_rn(amax, 127.0f);
     if (tid == 0) p.out_scale[row] = s;
+    // Codes rne(fl(v/s)): reciprocal path (see rotate_impl.cuh) with an exact fallback.
+    uint32_t words[kIdMaxChunks][2];
+    bool fast = s >= 1e-30f;
+    if (fast) {
+        const float r = __frcp_rn(s);
+        float dmax = 0.0f;
+#pragma unroll
+        for (int c = 0; c < kIdMaxChunks; ++c) {
+            uint32_t mb[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float t = __fmul_rn(v[c][e], r);
+                const float m = __fadd_rn(t, 12582912.0f);
+                dmax = fmaxf(dmax, fabsf(__fsub_rn(t, __fsub_rn(m, 12582912.0f))));
+                mb[e] = __float_as_uint(m);
+            }
+            words[c][0] = __byte_perm(__byte_perm(mb[0], mb[1], 0x0040), __byte_perm(mb[2], mb[3], 0x0040), 0x5410);
+            words[c][1] = __byte_perm(__byte_perm(mb[4], mb[5], 0x0040), __byte_perm(mb[6], mb[7], 0x0040), 0x5410);
+        }
+        fast = dmax <= 0.4999f;
+    }
+    if (!fast) {
+#pragma unroll
+        for (int c = 0; c < kIdMaxChunks; ++c) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t w = 0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    int qq = 0;
+                    if (s != 0.0f) qq = max(-127, min(127, __float2int_rn(__fdiv_rn(v[c][4 * h + e], s))));
+                    w |= (uint32_t)(qq & 0xFF) << (8 * e);
+                }
+                words[c][h] = w;
+            }
+        }
+    }
 #pragma unroll
     for (int c = 0; c < kIdMaxChunks; ++c) {
         const int ch = tid + c * kIdThreads;
         if (ch >= nchunks) continue;
-        int q[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            int qq = 0;
-            if (s != 0.0f) qq = max(-127, min(127, __float2int_rn(__fdiv_rn(v[c][e], s))));
-            q[e] = qq;
-        }
         if constexpr (OUT == OUT_S8) {
-            uint2 w;
-            w.x = (uint32_t)(q[0] & 0xFF) | ((uint32_t)(q[1] & 0xFF) << 8) | ((uint32_t)(q[2] & 0xFF) << 16) |
-                  ((uint32_t)(q[3] & 0xFF) << 24);
-            w.y = (uint32_t)(q[4] & 0xFF) | ((uint32_t)(q[5] & 0xFF) << 8) | ((uint32_t)(q[6] & 0xFF) << 16) |
-                  ((uint32_t)(q[7] & 0xFF) << 24);
-            reinterpret_cast<uint2 *>(reinterpret_cast<int8_t *>(p.out) + row * p.K)[ch] = w;
+            reinterpret_cast<uint2 *>(reinterpret_cast<int8_t *>(p.out) + row * p.K)[ch] =
+                make_uint2(words[c][0], words[c][1]);
         } else {
-            uint32_t w[4];
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                __half2 h2 = __halves2half2(__int2half_rn(q[2 * h]), __int2half_rn(q[2 * h + 1]));
-                w[h] = *reinterpret_cast<uint32_t *>(&h2);
-            }
+            const uint32_t a = words[c][0], b = words[c][1];
             reinterpret_cast<uint4 *>(reinterpret_cast<__half *>(p.out) + row * p.K)[ch] =
-                make_uint4(w[0], w[1], w[2], w[3]);
+                make_uint4(s8pair_to_f16x2(__byte_perm(a, 0, 0x4140)), s8pair_to_f16x2(__byte_perm(a, 0, 0x4342)),
+                           s8pair_to_f16x2(__byte_perm(b, 0, 0x4140)), s8pair_to_f16x2(__byte_perm(b, 0, 0x4342)));
         }
     }
 }
 
 cudaError_t launch_quant_identity(int out_kind, IdArgs a, cudaStream_t st) {
-    if (a.K % 8 != 0 || a.K / 8 > (int64_t)kIdThreads * kIdMaxChunks) return cudaErrorNotSupported;
+    if (a.K % 8 != 0 || a.K / 8 > (int64_t)kIdThreads * kIdChunkCap) return cudaErrorNotSupported;
     if (a.M > 0x7fffffff) return cudaErrorInvalidValue;
     if (out_kind != OUT_S8 && out_kind != OUT_F16Q) return cudaErrorNotSupported;
+    const int64_t chunks = (a.K / 8 + kIdThreads - 1) / kIdThreads;  // per thread
+    const unsigned grid = (unsigned)a.M;
     prof_begin(0, st);
-    if (out_kind == OUT_S8)
-        quant_identity_kernel<OUT_S8><<<(unsigned)a.M, kIdThreads, 0, st>>>(a);
+#define GBQ_ID_LAUNCH(CH)                                                                              \
+    do {                                                                                               \
+        if (out_kind == OUT_S8)                                                                        \
+            quant_identity_kernel<OUT_S8, CH><<<grid, kIdThreads, 0, st>>>(a);                         \
+        else                                                                                           \
+            quant_identity_kernel<OUT_F16Q, CH><<<grid, kIdThreads, 0, st>>>(a);                       \
+    } while (0)
+    if (chunks <= 4)
+        GBQ_ID_LAUNCH(4);
+    else if (chunks <= 8)
+        GBQ_ID_LAUNCH(8);
     else
-        quant_identity_kernel<OUT_F16Q><<<(unsigned)a.M, kIdThreads, 0, st>>>(a);
+        GBQ_ID_LAUNCH(16);
+#undef GBQ_ID_LAUNCH
     prof_end(st);
     return cudaGetLastError();
 }
