@@ -63,12 +63,16 @@ __device__ __forceinline__ int producer_id(int warp) {
 constexpr uint32_t kTokBox = 256 * 128;             // one 256-row x 128-byte token box (64 K)
 constexpr uint32_t kBStageBytes = kSubs * kTokBox;  // 64 KB fp16 tokens
 constexpr uint32_t kWStageBytes = kBM * kBK;        // 16 KB int8 weights (one 128 x 128-byte box)
-constexpr size_t kSmemBytes = (size_t)kStages * (kBStageBytes + kWStageBytes) + 1024 /*barriers*/ + 1024 /*align*/;
+constexpr uint32_t kOutBlock = 32 * 128 * 4;       // one 32-token x 128-column output block (<= 4 B/elem)
+constexpr uint32_t kOutStaging = 2 * 2 * kOutBlock;  // two epilogue warpgroups x double buffer
+constexpr size_t kSmemBytes =
+    (size_t)kStages * (kBStageBytes + kWStageBytes) + kOutStaging + 1024 /*barriers*/ + 1024 /*align*/;
 
 struct Params {
     CUtensorMap tm_b;
     CUtensorMap tm_w0;
     CUtensorMap tm_w1;
+    CUtensorMap tm_out;  // output [M][ld_out], box 128 columns x 32 rows (when use_tma_out)
     int64_t M, N, K;
     int64_t n_split;
     int64_t ld_out;
@@ -80,6 +84,7 @@ struct Params {
     unsigned int *status;
     int w_layout;
     int epi;
+    int use_tma_out;
 };
 
 struct Bars {
@@ -117,7 +122,8 @@ __global__ void __launch_bounds__(kThreads, 1) i8gemm_kernel(const __grid_consta
     uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     uint8_t *bbuf = smem;
     uint8_t *wbuf = smem + kStages * kBStageBytes;
-    Bars *bars = reinterpret_cast<Bars *>(wbuf + kStages * kWStageBytes);
+    uint8_t *obuf = wbuf + kStages * kWStageBytes;  // output staging
+    Bars *bars = reinterpret_cast<Bars *>(obuf + kOutStaging);
     volatile int *abort = &bars->abort;
 
     const int warp = threadIdx.x >> 5;
@@ -146,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1) i8gemm_kernel(const __grid_consta
         tma_prefetch_desc(&p.tm_b);
         tma_prefetch_desc(&p.tm_w0);
         tma_prefetch_desc(&p.tm_w1);
+        if (p.use_tma_out) tma_prefetch_desc(&p.tm_out);
     }
     if (warp == 1) tmem_alloc(&bars->tmem_base, kTmemCols);
     tc_fence_before();
@@ -330,7 +337,47 @@ __global__ void __launch_bounds__(kThreads, 1) i8gemm_kernel(const __grid_consta
                 if (lane == 0) mbar_arrive(&bars->accempty);  // this warp is done with the accumulator
                 ++chunk;
             }
+            // The staged store below synchronises the warpgroup on named barriers, so its
+            // four warps agree on giving up (a timed-out wait in one of them) before it.
+            if (p.use_tma_out) ok = named_bar_and(1 + h, 128, ok);
             if (!ok) break;
+            if (p.use_tma_out) {
+                // Stage 32-token x 128-column blocks in shared memory, one TMA store each
+                // (double-buffered per warpgroup; the store clips rows/columns past the edge).
+                const uint32_t esz = p.epi == EPI_DEQUANT_BF16 ? 2u : 4u;
+                const bool issuer = (q == 0 && lane == 0);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint8_t *buf = obuf + (uint32_t)(h * 2 + (j & 1)) * kOutBlock;
+                    const int64_t mb = m0 + 128 * h + 32 * j;
+                    float xs_l = 0.0f;
+                    if (p.epi != EPI_ACC_I32 && mb + lane < p.M) xs_l = __ldg(p.x_scale + mb + lane);
+                    if (issuer) tma_store_wait_read<1>();  // the store that last read `buf` is done
+                    named_bar_sync(1 + h, 128);
+                    uint8_t *col = buf + (uint32_t)(q * 32 + lane) * esz;
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float xs = __shfl_sync(0xffffffffu, xs_l, i);
+                        const int32_t acc = tot[32 * j + i];
+                        if (p.epi == EPI_ACC_I32) {
+                            *reinterpret_cast<int32_t *>(col + i * 128 * esz) = acc;
+                        } else if (p.epi == EPI_DEQUANT_BF16) {
+                            const float tv = __fmul_rn(__int2float_rn(acc), xs);
+                            *reinterpret_cast<__nv_bfloat16 *>(col + i * 128 * esz) =
+                                __float2bfloat16_rn(__fmaf_rn(tv, ws, bias));
+                        } else {
+                            *reinterpret_cast<float *>(col + i * 128 * esz) = __fmul_rn(__int2float_rn(acc), xs);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    named_bar_sync(1 + h, 128);
+                    if (issuer) {
+                        tma_store_2d(&p.tm_out, buf, (int)n0, (int)mb);
+                        tma_store_commit();
+                    }
+                }
+                continue;
+            }
             // Write token rows m0 + 128h + 32j + i of output column n.
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -357,6 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) i8gemm_kernel(const __grid_consta
         }
     }
 
+    if (wg >= 2 && (warp & 3) == 0 && lane == 0 && p.use_tma_out) tma_store_wait_all<0>();  // smem must outlive the stores
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -386,6 +434,19 @@ int launch_i8gemm(const I8GemmProblem &q, cudaStream_t st) {
             rc = encode_tmap_2d(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, (uint64_t)q.N, (uint64_t)rows,
                                 (uint64_t)q.ld_w, kBM, kBK, CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc) return rc;
+    }
+    // Output through TMA when its row stride allows (16-byte multiple).
+    {
+        const uint32_t esz = q.epi == EPI_DEQUANT_BF16 ? 2u : 4u;
+        const CUtensorMapDataType dt = q.epi == EPI_DEQUANT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                       : q.epi == EPI_ACC_I32    ? CU_TENSOR_MAP_DATA_TYPE_INT32
+                                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+        p.use_tma_out = ((q.ld_out * esz) % 16 == 0 && ((uintptr_t)q.out & 15) == 0) ? 1 : 0;
+        if (p.use_tma_out) {
+            rc = encode_tmap_2d(&p.tm_out, dt, q.out, (uint64_t)q.N, (uint64_t)q.M, (uint64_t)q.ld_out * esz, 128, 32,
+                                CU_TENSOR_MAP_SWIZZLE_NONE);
+            if (rc) return rc;
+        }
     }
     p.M = q.M;
     p.N = q.N;
