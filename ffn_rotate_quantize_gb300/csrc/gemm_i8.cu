@@ -13,20 +13,28 @@
 //     the fp32 accumulator (fp32 -> int32, exact) into int32 running totals
 //     held in their registers; the MMA resumes once the accumulator is read.
 //
-// Tile: 128 weight rows (TMEM lanes, MMA M) x 256 tokens (MMA N).  A tcgen05
-// MMA takes about the same time for N = 128 as for N = 256, so only N = 256
-// reaches the tensor-core peak.  The weight is the A operand and lives in TMEM:
-// a converter warpgroup widens the TMA-staged int8 tile to fp16 in 64-deep
-// sub-steps (byte-permute + one half2 subtract per pair) and tcgen05.st's it
-// into an 8-slot ring, so the widened weight never costs shared-memory
-// bandwidth.  The fp16-coded tokens are the B operand (128-byte swizzle, two
-// 256-row boxes per 128-deep stage).  One persistent CTA per SM.
+// CTA pairs.  Two CTAs of a cluster share one 256 x 256 tile: the pair MMA
+// (tcgen05 cta_group::2, M = 256, N = 256) takes weight rows 128r..128r+127 from
+// CTA r's tensor memory and tokens 128r..128r+127 from CTA r's shared memory,
+// and writes D rows 128r.. into CTA r's tensor memory.  Each SM so stages only
+// half the token tile: 384 bytes of operands per unit of K for 128 x 256
+// products, against 640 for a one-CTA 128 x 256 tile.  The fp16-coded tokens
+// are what fills shared memory and the L2 -> SM path; halving them is what lets
+// four 48 KB stages stay in flight.
 //
-// Warp roles (512 threads): warps 0 and 2 TMA producers (alternate stages),
-// warp 1 TMEM owner + MMA issuer, warps 4-7 converters, warps 8-15 epilogue
-// (warp w owns TMEM lane quadrant w%4 and token half (w/4)%2).  Register
-// budgets per warpgroup (setmaxnreg; launch total 512 x 128 = 65,536):
-// 48 + 88 + 184 + 184 = 504 per lane -> 64,512.  Every mbarrier wait is bounded.
+// The weight is the A operand and lives in TMEM: a converter warpgroup in each
+// CTA widens the TMA-staged int8 tile to fp16 in 64-deep sub-steps
+// (byte-permute + one half2 subtract per pair) and tcgen05.st's it into an
+// 8-slot ring.  CTA 0's warp 1 issues every MMA of the pair once both CTAs'
+// converters have published the sub-step (remote mbarrier arrivals); its
+// commits arrive on the barriers of both CTAs (multicast).
+//
+// Warp roles per CTA (512 threads): warps 0 and 2 TMA producers (alternate
+// stages), warp 1 TMEM owner (+ the MMA issuer in CTA 0), warps 4-7
+// converters, warps 8-15 epilogue (warp w owns TMEM lane quadrant w%4 and
+// token half (w/4)%2).  Register budgets per warpgroup (setmaxnreg; launch
+// total 512 x 128 = 65,536): 48 + 88 + 184 + 184 = 504 per lane -> 64,512.
+// Every mbarrier wait is bounded; a timeout in one CTA aborts its peer too.
 //
 // TMEM columns: [0,256) A ring (8 x 32), [256,512) accumulator.
 #include "common.cuh"
@@ -35,12 +43,14 @@
 namespace gbq {
 namespace {
 
-constexpr int kBM = 128;                 // weight rows per tile
-constexpr int kBN = 256;                 // tokens per tile
+constexpr int kPairM = 256;              // weight rows per CTA pair (pair MMA M)
+constexpr int kBM = 128;                 // weight rows per CTA
+constexpr int kBN = 256;                 // tokens per tile (MMA N)
+constexpr int kBNHalf = kBN / 2;         // tokens staged by each CTA
 constexpr int kBK = 128;                 // K per shared-memory stage
 constexpr int kSub = 64;                 // K per converter / A-ring sub-step
 constexpr int kSubs = kBK / kSub;        // sub-steps per stage
-constexpr int kStages = 2;
+constexpr int kStages = 4;
 constexpr int kAStages = 8;
 constexpr int kChunkSubs = 1024 / kSub;  // sub-steps per exact fp32 chunk
 constexpr uint32_t kTmemCols = 512;
@@ -60,19 +70,20 @@ __device__ __forceinline__ int producer_id(int warp) {
     return -1;
 }
 
-constexpr uint32_t kTokBox = 256 * 128;             // one 256-row x 128-byte token box (64 K)
-constexpr uint32_t kBStageBytes = kSubs * kTokBox;  // 64 KB fp16 tokens
+constexpr uint32_t kTokBox = kBNHalf * 128;         // one 128-row x 128-byte token box (64 K)
+constexpr uint32_t kBStageBytes = kSubs * kTokBox;  // 32 KB fp16 tokens
 constexpr uint32_t kWStageBytes = kBM * kBK;        // 16 KB int8 weights (one 128 x 128-byte box)
-constexpr uint32_t kOutBlock = 32 * 128 * 4;       // one 32-token x 128-column output block (<= 4 B/elem)
+constexpr uint32_t kOutBlock = 8192;                // 128 columns x (32 bf16 | 16 four-byte) token rows
 constexpr uint32_t kOutStaging = 2 * 2 * kOutBlock;  // two epilogue warpgroups x double buffer
 constexpr size_t kSmemBytes =
     (size_t)kStages * (kBStageBytes + kWStageBytes) + kOutStaging + 1024 /*barriers*/ + 1024 /*align*/;
+static_assert(kSmemBytes <= 232448, "shared memory exceeds the per-CTA limit");
 
 struct Params {
     CUtensorMap tm_b;
     CUtensorMap tm_w0;
     CUtensorMap tm_w1;
-    CUtensorMap tm_out;  // output [M][ld_out], box 128 columns x 32 rows (when use_tma_out)
+    CUtensorMap tm_out;  // output [M][ld_out], box 128 columns x (kOutBlock / 128 / esz) rows
     int64_t M, N, K;
     int64_t n_split;
     int64_t ld_out;
@@ -88,19 +99,20 @@ struct Params {
 };
 
 struct Bars {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    uint64_t afull[kAStages];
-    uint64_t aempty[kAStages];
-    uint64_t accfull;
-    uint64_t accempty;
-    uint64_t drain;
+    uint64_t full[kStages];     // local: TMA bytes landed
+    uint64_t empty[kStages];    // local: pair MMA done reading (multicast commit) + local converters
+    uint64_t afull[kAStages];   // CTA 0 only: converter warps of both CTAs published the sub-step
+    uint64_t aempty[kAStages];  // both: pair MMA done reading the A slot (multicast commit)
+    uint64_t accfull;           // both: chunk accumulated (multicast commit)
+    uint64_t accempty;          // CTA 0 only: epilogue warps of both CTAs drained the accumulator
+    uint64_t drain;             // CTA 0 only: every MMA finished
     uint32_t tmem_base;
     int abort;
 };
 
+// Pair tile t: weight rows [n0, n0 + 256), tokens [m0, m0 + 256).
 __device__ __forceinline__ void tile_coords(int64_t t, int64_t m_tiles, int64_t *n0, int64_t *m0) {
-    *n0 = (t / m_tiles) * kBM;
+    *n0 = (t / m_tiles) * kPairM;
     *m0 = (t % m_tiles) * kBN;
 }
 
@@ -116,10 +128,69 @@ __device__ __forceinline__ void s8x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t
     hi = *reinterpret_cast<uint32_t *>(&h1);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) i8gemm_kernel(const __grid_constant__ Params p) {
+// Add 32 exact integer-valued fp32 partial sums to int32 totals.  When every
+// value of the warp is below 2^22 in magnitude, v + 1.5*2^23 lands in
+// [2^23, 2^24) where the fp32 spacing is 1, so its bit pattern minus that of
+// 1.5*2^23 is v exactly: one FADD + one integer add instead of a (quarter-rate)
+// float -> int conversion.  Otherwise convert each value with round-to-nearest.
+__device__ __forceinline__ void add_exact_totals(int32_t *tot, const uint32_t (&rr)[32]) {
+    float mx = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fabsf(__uint_as_float(rr[i])));
+    if (__all_sync(0xffffffffu, mx < 4194304.0f)) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            tot[i] += (int32_t)(__float_as_uint(__fadd_rn(__uint_as_float(rr[i]), 12582912.0f)) - 0x4B400000u);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) tot[i] += __float2int_rn(__uint_as_float(rr[i]));
+    }
+}
+
+// Write this thread's 128 token values of output column n through shared-memory
+// blocks of ROWS tokens x 128 columns, one TMA tensor store per block
+// (double-buffered per warpgroup; the store clips rows and columns past the edge).
+template <int ROWS, int EPI>
+__device__ __forceinline__ void store_tile_tma(const Params &p, const int32_t (&tot)[128], uint8_t *obuf, int h,
+                                               int q, int lane, int64_t n0, int64_t m0, float ws, float bias) {
+    constexpr uint32_t esz = EPI == EPI_DEQUANT_BF16 ? 2u : 4u;
+    static_assert(ROWS * 128 * esz == kOutBlock, "block geometry");
+    const bool issuer = (q == 0 && lane == 0);
+#pragma unroll
+    for (int j = 0; j < 128 / ROWS; ++j) {
+        uint8_t *buf = obuf + (uint32_t)(h * 2 + (j & 1)) * kOutBlock;
+        const int64_t mb = m0 + 128 * h + ROWS * j;
+        float xs_l = 0.0f;
+        if (EPI != EPI_ACC_I32 && lane < ROWS && mb + lane < p.M) xs_l = __ldg(p.x_scale + mb + lane);
+        if (issuer) tma_store_wait_read<1>();  // the store that last read `buf` is done
+        named_bar_sync(1 + h, 128);
+        uint8_t *col = buf + (uint32_t)(q * 32 + lane) * esz;
+#pragma unroll
+        for (int i = 0; i < ROWS; ++i) {
+            const float xs = __shfl_sync(0xffffffffu, xs_l, i);
+            const int32_t acc = tot[ROWS * j + i];
+            if (EPI == EPI_ACC_I32) {
+                *reinterpret_cast<int32_t *>(col + i * 128 * esz) = acc;
+            } else if (EPI == EPI_DEQUANT_BF16) {
+                const float tv = __fmul_rn(__int2float_rn(acc), xs);
+                *reinterpret_cast<__nv_bfloat16 *>(col + i * 128 * esz) = __float2bfloat16_rn(__fmaf_rn(tv, ws, bias));
+            } else {
+                *reinterpret_cast<float *>(col + i * 128 * esz) = __fmul_rn(__int2float_rn(acc), xs);
+            }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1 + h, 128);
+        if (issuer) {
+            tma_store_2d(&p.tm_out, buf, (int)n0, (int)mb);
+            tma_store_commit();
+        }
+    }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) i8gemm_kernel(const __grid_constant__ Params p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
-    uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // same offset in both CTAs
     uint8_t *bbuf = smem;
     uint8_t *wbuf = smem + kStages * kBStageBytes;
     uint8_t *obuf = wbuf + kStages * kWStageBytes;  // output staging
@@ -128,8 +199,12 @@ __global__ void __launch_bounds__(kThreads, 1) i8gemm_kernel(const __grid_consta
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_cta_rank();  // 0 leads the pair
+    const uint32_t peer_abort = cluster_map(smem_u32(&bars->abort), rank ^ 1u);
+    const int64_t pair = blockIdx.x >> 1;
+    const int64_t npairs = gridDim.x >> 1;
     const int64_t m_tiles = (p.M + kBN - 1) / kBN;
-    const int64_t n_tiles = (p.N + kBM - 1) / kBM;
+    const int64_t n_tiles = (p.N + kPairM - 1) / kPairM;
     const int64_t num_tiles = m_tiles * n_tiles;
     const int KT = (int)((p.K + kBK - 1) / kBK);  // stages per tile (the K tail reads zeros)
     const int tile_subs = KT * kSubs;
@@ -138,14 +213,14 @@ __global__ void __launch_bounds__(kThreads, 1) i8gemm_kernel(const __grid_consta
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&bars->full[s], 1);
-            mbar_init(&bars->empty[s], 1 + 4 * kSubs);  // MMA commit + every converter warp per sub-step
+            mbar_init(&bars->empty[s], 1 + 4 * kSubs);  // pair-MMA commit + every local converter warp per sub-step
         }
         for (int a = 0; a < kAStages; ++a) {
-            mbar_init(&bars->afull[a], 4);
+            mbar_init(&bars->afull[a], 8);  // four converter warps in each CTA
             mbar_init(&bars->aempty[a], 1);
         }
         mbar_init(&bars->accfull, 1);
-        mbar_init(&bars->accempty, kEpiWarps);
+        mbar_init(&bars->accempty, 2 * kEpiWarps);
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
         fence_mbar_init();
@@ -154,12 +229,13 @@ __global__ void __launch_bounds__(kThreads, 1) i8gemm_kernel(const __grid_consta
         tma_prefetch_desc(&p.tm_w1);
         if (p.use_tma_out) tma_prefetch_desc(&p.tm_out);
     }
-    if (warp == 1) tmem_alloc(&bars->tmem_base, kTmemCols);
+    if (warp == 1) tmem_alloc_pair(&bars->tmem_base, kTmemCols);
     tc_fence_before();
-    __syncthreads();
+    cluster_sync_all();  // barriers of both CTAs initialised, TMEM allocated
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     const int wg = warp >> 2;
+    const uint32_t lead_accempty = cluster_map(smem_u32(&bars->accempty), 0);
 
     if (wg == 0) {
         setmaxnreg_dec<kRegsWG0>();
@@ -169,17 +245,20 @@ __global__ void __launch_bounds__(kThreads, 1) i8gemm_kernel(const __grid_consta
             if (lane == 0) {
                 uint32_t gs = 0;
                 bool ok = true;
-                for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                for (int64_t t = pair; t < num_tiles && ok; t += npairs) {
                     int64_t n0, m0;
                     tile_coords(t, m_tiles, &n0, &m0);
-                    const bool src1 = n0 >= p.n_split;
+                    const int64_t nr = n0 + kBM * rank;  // this CTA's weight rows
+                    const bool src1 = nr >= p.n_split;
                     const CUtensorMap *tw = src1 ? &p.tm_w1 : &p.tm_w0;
-                    const int wrow = (int)(src1 ? n0 - p.n_split : n0);
+                    const int wrow = (int)(src1 ? nr - p.n_split : nr);
+                    const int trow = (int)(m0 + kBNHalf * rank);  // this CTA's tokens
                     for (int kt = 0; kt < KT; ++kt) {
                         const uint32_t my = gs++;
                         if (my % kProducers != pid) continue;
                         const int stage = (int)(my % kStages);
-                        ok = mbar_wait(&bars->empty[stage], ((my / kStages) & 1u) ^ 1u, p.status, abort);
+                        ok = mbar_wait_cluster(&bars->empty[stage], ((my / kStages) & 1u) ^ 1u, p.status, abort,
+                                               peer_abort);
                         if (!ok) break;
                         uint64_t *fb = &bars->full[stage];
                         mbar_arrive_expect_tx(fb, kBStageBytes + kWStageBytes);
@@ -191,70 +270,71 @@ __global__ void __launch_bounds__(kThreads, 1) i8gemm_kernel(const __grid_consta
                         uint8_t *bdst = bbuf + stage * kBStageBytes;
 #pragma unroll
                         for (int b = 0; b < kSubs; ++b)
-                            tma_load_2d(bdst + b * kTokBox, &p.tm_b, fb, kt * kBK + b * kSub, (int)m0);
+                            tma_load_2d(bdst + b * kTokBox, &p.tm_b, fb, kt * kBK + b * kSub, trow);
                     }
                 }
             }
-        } else if (warp == 1) {
-            // ------------------------------------------------ MMA issuer
+        } else if (warp == 1 && rank == 0) {
+            // ------------------------------------------------ pair-MMA issuer (CTA 0)
             if (lane == 0) {
-                constexpr uint32_t idesc = idesc_f16(kBM, kBN, 0, 0, 0);
+                constexpr uint32_t idesc = idesc_f16(kPairM, kBN, 0, 0, 0);
                 uint32_t gs = 0, gsub = 0, chunk = 0;
                 bool ok = true;
-                for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                for (int64_t t = pair; t < num_tiles && ok; t += npairs) {
                     for (int kt = 0; kt < KT && ok; ++kt) {
                         const uint32_t my = gs++;
                         const int stage = (int)(my % kStages);
-                        ok = mbar_wait(&bars->full[stage], (my / kStages) & 1u, p.status, abort);
-                        if (!ok) break;
+                        // Both CTAs' stage data has landed once their converters publish its sub-steps.
                         const uint32_t b_stage = smem_u32(bbuf + stage * kBStageBytes);
                         for (int sub = 0; sub < kSubs && ok; ++sub) {
                             const uint32_t ms = gsub++;
                             const int tsub = kt * kSubs + sub;  // sub-step within the tile
                             const int cpos = tsub % kChunkSubs;
-                            if (cpos == 0) {  // a new chunk: the accumulator must have been drained
-                                ok = mbar_wait(&bars->accempty, (chunk & 1u) ^ 1u, p.status, abort);
+                            if (cpos == 0) {  // a new chunk: both CTAs' accumulators must have been drained
+                                ok = mbar_wait_cluster(&bars->accempty, (chunk & 1u) ^ 1u, p.status, abort,
+                                                       peer_abort);
                                 if (!ok) break;
                             }
                             const int as = (int)(ms % kAStages);
-                            ok = mbar_wait(&bars->afull[as], (ms / kAStages) & 1u, p.status, abort);
+                            ok = mbar_wait_cluster(&bars->afull[as], (ms / kAStages) & 1u, p.status, abort,
+                                                   peer_abort);
                             if (!ok) break;
                             tc_fence_after();
 #pragma unroll
                             for (int k16 = 0; k16 < kSub / 16; ++k16) {
                                 const uint64_t bdesc =
                                     smem_desc(b_stage + sub * kTokBox + k16 * 32, 16, 1024, kLayoutSw128);
-                                mma_ts_f16(tmem + kColAcc, tmem + kColA + as * 32 + k16 * 8, bdesc, idesc,
-                                           (cpos > 0 || k16 > 0) ? 1u : 0u);
+                                mma_pair_ts_f16(tmem + kColAcc, tmem + kColA + as * 32 + k16 * 8, bdesc, idesc,
+                                                (cpos > 0 || k16 > 0) ? 1u : 0u);
                             }
-                            tc_commit(&bars->aempty[as]);
+                            tc_commit_pair(&bars->aempty[as], 3);
                             if (cpos == kChunkSubs - 1 || tsub == tile_subs - 1) {
-                                tc_commit(&bars->accfull);
+                                tc_commit_pair(&bars->accfull, 3);
                                 ++chunk;
                             }
                         }
-                        tc_commit(&bars->empty[stage]);
+                        tc_commit_pair(&bars->empty[stage], 3);
                     }
                 }
-                // Let every issued MMA finish before the CTA can release TMEM.
-                tc_commit(&bars->drain);
-                mbar_wait(&bars->drain, 0, p.status, abort);
+                // Let every issued MMA finish before either CTA can release TMEM or shared memory.
+                tc_commit_pair(&bars->drain, 1);
+                mbar_wait_cluster(&bars->drain, 0, p.status, abort, peer_abort);
             }
         }
     } else if (wg == 1) {
         setmaxnreg_dec<kRegsConv>();
         // ------------------------------------------------ int8 -> fp16 converters (A operand into TMEM)
         const int q = warp & 3;
-        const int r = q * 32 + lane;  // TMEM lane = A row of the tile
+        const int r = q * 32 + lane;  // TMEM lane = A row of this CTA's half
         const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
         uint32_t gs = 0, gsub = 0;
         bool ok = true;
-        for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        for (int64_t t = pair; t < num_tiles && ok; t += npairs) {
             for (int kt = 0; kt < KT && ok; ++kt) {
                 const uint32_t mstage = gs++;
                 const int stage = (int)(mstage % kStages);
                 const uint8_t *ws = wbuf + stage * kWStageBytes;
-                ok = mbar_wait(&bars->full[stage], (mstage / kStages) & 1u, p.status, abort);
+                ok = mbar_wait_cluster(&bars->full[stage], (mstage / kStages) & 1u, p.status, abort, peer_abort);
                 if (!ok) break;
                 for (int sub = 0; sub < kSubs; ++sub) {
                     const uint32_t my = gsub++;
@@ -277,25 +357,26 @@ __global__ void __launch_bounds__(kThreads, 1) i8gemm_kernel(const __grid_consta
                         }
                     } else {
                         // Box [128 contraction rows][128 output columns], 128-byte swizzle:
-                        // byte (n, r) at n*128 + 16*((r >> 4) ^ (n & 7)) + (r & 15).
+                        // byte (kr, r) at kr*128 + 16*((r >> 4) ^ (kr & 7)) + (r & 15).
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
-                            const int n = sub * kSub + 2 * j;
-                            const uint32_t b0 = ws[n * 128 + 16 * ((r >> 4) ^ (n & 7)) + (r & 15)];
-                            const uint32_t b1 = ws[(n + 1) * 128 + 16 * ((r >> 4) ^ ((n + 1) & 7)) + (r & 15)];
+                            const int kr = sub * kSub + 2 * j;
+                            const uint32_t b0 = ws[kr * 128 + 16 * ((r >> 4) ^ (kr & 7)) + (r & 15)];
+                            const uint32_t b1 = ws[(kr + 1) * 128 + 16 * ((r >> 4) ^ ((kr + 1) & 7)) + (r & 15)];
                             a[j] = s8pair_to_f16x2(b0 | (b1 << 16));
                         }
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bars->empty[stage]);
-                    ok = mbar_wait(&bars->aempty[astage], ((my / kAStages) & 1u) ^ 1u, p.status, abort);
+                    ok = mbar_wait_cluster(&bars->aempty[astage], ((my / kAStages) & 1u) ^ 1u, p.status, abort,
+                                           peer_abort);
                     if (!ok) break;
                     tc_fence_after();
                     tmem_st32(lane_addr + kColA + astage * 32, a);
                     tc_wait_st();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&bars->afull[astage]);
+                    if (lane == 0) mbar_arrive_cluster(cluster_map(smem_u32(&bars->afull[astage]), 0));
                 }
             }
         }
@@ -307,9 +388,10 @@ __global__ void __launch_bounds__(kThreads, 1) i8gemm_kernel(const __grid_consta
         const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16) + kColAcc + h * 128;
         uint32_t chunk = 0;
         bool ok = true;
-        for (int64_t t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        for (int64_t t = pair; t < num_tiles && ok; t += npairs) {
             int64_t n0, m0;
             tile_coords(t, m_tiles, &n0, &m0);
+            n0 += kBM * rank;                      // this CTA's output columns
             const int64_t n = n0 + q * 32 + lane;  // output column owned by this thread
             const bool n_ok = n < p.N;
             float ws = 0.0f, bias = 0.0f;
@@ -321,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) i8gemm_kernel(const __grid_consta
 #pragma unroll
             for (int i = 0; i < 128; ++i) tot[i] = 0;
             for (int c = 0; c < nchunks; ++c) {
-                ok = mbar_wait(&bars->accfull, chunk & 1u, p.status, abort);
+                ok = mbar_wait_cluster(&bars->accfull, chunk & 1u, p.status, abort, peer_abort);
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
@@ -329,12 +411,11 @@ __global__ void __launch_bounds__(kThreads, 1) i8gemm_kernel(const __grid_consta
                     uint32_t rr[32];
                     tmem_ld32(lane_addr + 32 * j, rr);
                     tc_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) tot[32 * j + i] += __float2int_rn(__uint_as_float(rr[i]));
+                    add_exact_totals(tot + 32 * j, rr);
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->accempty);  // this warp is done with the accumulator
+                if (lane == 0) mbar_arrive_cluster(lead_accempty);  // this warp is done with the accumulator
                 ++chunk;
             }
             // The staged store below synchronises the warpgroup on named barriers, so its
@@ -342,40 +423,12 @@ __global__ void __launch_bounds__(kThreads, 1) i8gemm_kernel(const __grid_consta
             if (p.use_tma_out) ok = named_bar_and(1 + h, 128, ok);
             if (!ok) break;
             if (p.use_tma_out) {
-                // Stage 32-token x 128-column blocks in shared memory, one TMA store each
-                // (double-buffered per warpgroup; the store clips rows/columns past the edge).
-                const uint32_t esz = p.epi == EPI_DEQUANT_BF16 ? 2u : 4u;
-                const bool issuer = (q == 0 && lane == 0);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint8_t *buf = obuf + (uint32_t)(h * 2 + (j & 1)) * kOutBlock;
-                    const int64_t mb = m0 + 128 * h + 32 * j;
-                    float xs_l = 0.0f;
-                    if (p.epi != EPI_ACC_I32 && mb + lane < p.M) xs_l = __ldg(p.x_scale + mb + lane);
-                    if (issuer) tma_store_wait_read<1>();  // the store that last read `buf` is done
-                    named_bar_sync(1 + h, 128);
-                    uint8_t *col = buf + (uint32_t)(q * 32 + lane) * esz;
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float xs = __shfl_sync(0xffffffffu, xs_l, i);
-                        const int32_t acc = tot[32 * j + i];
-                        if (p.epi == EPI_ACC_I32) {
-                            *reinterpret_cast<int32_t *>(col + i * 128 * esz) = acc;
-                        } else if (p.epi == EPI_DEQUANT_BF16) {
-                            const float tv = __fmul_rn(__int2float_rn(acc), xs);
-                            *reinterpret_cast<__nv_bfloat16 *>(col + i * 128 * esz) =
-                                __float2bfloat16_rn(__fmaf_rn(tv, ws, bias));
-                        } else {
-                            *reinterpret_cast<float *>(col + i * 128 * esz) = __fmul_rn(__int2float_rn(acc), xs);
-                        }
-                    }
-                    fence_proxy_async_smem();
-                    named_bar_sync(1 + h, 128);
-                    if (issuer) {
-                        tma_store_2d(&p.tm_out, buf, (int)n0, (int)mb);
-                        tma_store_commit();
-                    }
-                }
+                if (p.epi == EPI_ACC_I32)
+                    store_tile_tma<16, EPI_ACC_I32>(p, tot, obuf, h, q, lane, n0, m0, ws, bias);
+                else if (p.epi == EPI_DEQUANT_BF16)
+                    store_tile_tma<32, EPI_DEQUANT_BF16>(p, tot, obuf, h, q, lane, n0, m0, ws, bias);
+                else
+                    store_tile_tma<16, EPI_ROWSCALE_F32>(p, tot, obuf, h, q, lane, n0, m0, ws, bias);
                 continue;
             }
             // Write token rows m0 + 128h + 32j + i of output column n.
@@ -405,12 +458,33 @@ __global__ void __launch_bounds__(kThreads, 1) i8gemm_kernel(const __grid_consta
     }
 
     if (wg >= 2 && (warp & 3) == 0 && lane == 0 && p.use_tma_out) tma_store_wait_all<0>();  // smem must outlive the stores
+    __syncwarp();
     tc_fence_before();
-    __syncthreads();
+    cluster_sync_all();  // no CTA leaves while its peer's MMAs, arrivals or stores may touch it
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc_pair(tmem, kTmemCols);
     }
+}
+
+// Co-resident CTA pairs on the current device (cached).
+int max_pairs_for_device(int num_sms) {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms / 2;
+    if (cached[dev] == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(num_sms & ~1), 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, i8gemm_kernel, &cfg) != cudaSuccess || n <= 0) {
+            (void)cudaGetLastError();
+            n = num_sms / 2;
+        }
+        cached[dev] = n;
+    }
+    return cached[dev];
 }
 
 }  // namespace
@@ -419,9 +493,9 @@ int launch_i8gemm(const I8GemmProblem &q, cudaStream_t st) {
     Params p;  // host staging; copied into the launch's parameter buffer
     memset(&p, 0, sizeof(p));
     int rc;
-    // Activations: fp16 [M][K], box 64 x 128, 128-byte swizzle.
+    // Activations: fp16 [M][K], box 64 x 128, 128-byte swizzle (each CTA stages its 128-token half).
     rc = encode_tmap_2d(&p.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, q.b_f16, (uint64_t)q.K, (uint64_t)q.M,
-                        (uint64_t)q.K * 2, kSub, kBN, CU_TENSOR_MAP_SWIZZLE_128B);
+                        (uint64_t)q.K * 2, kSub, kBNHalf, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
     for (int s = 0; s < 2; ++s) {
         const int8_t *w = s ? q.w1 : q.w0;
@@ -443,8 +517,8 @@ int launch_i8gemm(const I8GemmProblem &q, cudaStream_t st) {
                                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
         p.use_tma_out = ((q.ld_out * esz) % 16 == 0 && ((uintptr_t)q.out & 15) == 0) ? 1 : 0;
         if (p.use_tma_out) {
-            rc = encode_tmap_2d(&p.tm_out, dt, q.out, (uint64_t)q.N, (uint64_t)q.M, (uint64_t)q.ld_out * esz, 128, 32,
-                                CU_TENSOR_MAP_SWIZZLE_NONE);
+            rc = encode_tmap_2d(&p.tm_out, dt, q.out, (uint64_t)q.N, (uint64_t)q.M, (uint64_t)q.ld_out * esz, 128,
+                                kOutBlock / (128 * esz), CU_TENSOR_MAP_SWIZZLE_NONE);
             if (rc) return rc;
         }
     }
@@ -474,8 +548,9 @@ int launch_i8gemm(const I8GemmProblem &q, cudaStream_t st) {
             return gbq_fail(GBQ_ECUDA, "int8 GEMM: register split exceeds the launch allocation");
         attr = true;
     }
-    const int64_t tiles = ((q.M + kBN - 1) / kBN) * ((q.N + kBM - 1) / kBM);
-    const int grid = (int)(tiles < q.num_sms ? tiles : q.num_sms);
+    const int64_t tiles = ((q.M + kBN - 1) / kBN) * ((q.N + kPairM - 1) / kPairM);
+    const int64_t pairs_max = max_pairs_for_device(q.num_sms);
+    const int grid = 2 * (int)(tiles < pairs_max ? tiles : pairs_max);
     prof_begin(1, st);
     i8gemm_kernel<<<grid, kThreads, kSmemBytes, st>>>(p);
     prof_end(st);
