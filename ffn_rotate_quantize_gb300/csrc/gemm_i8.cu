@@ -12,6 +12,11 @@
 //   * K is cut into chunks of 1024.  After each chunk the epilogue warps drain
 //     the fp32 accumulator (fp32 -> int32, exact) into int32 running totals
 //     held in their registers; the MMA resumes once the accumulator is read.
+//   * The accumulator is split into two N = 128 halves, each with its own
+//     epilogue warpgroup and barriers.  The MMA issuer keeps one cursor per
+//     half over the stream of 64-deep sub-steps and issues whichever half can
+//     go (the lagging one first, the leading one at most 7 sub-steps ahead), so
+//     while one half is being drained the other keeps the tensor pipe busy.
 //
 // CTA pairs.  Two CTAs of a cluster share one 256 x 256 tile: the pair MMA
 // (tcgen05 cta_group::2, M = 256, N = 256) takes weight rows 128r..128r+127 from
@@ -73,8 +78,8 @@ __device__ __forceinline__ int producer_id(int warp) {
 constexpr uint32_t kTokBox = kBNHalf * 128;         // one 128-row x 128-byte token box (64 K)
 constexpr uint32_t kBStageBytes = kSubs * kTokBox;  // 32 KB fp16 tokens
 constexpr uint32_t kWStageBytes = kBM * kBK;        // 16 KB int8 weights (one 128 x 128-byte box)
-constexpr uint32_t kOutBlock = 8192;                // 128 columns x (32 bf16 | 16 four-byte) token rows
-constexpr uint32_t kOutStaging = 2 * 2 * kOutBlock;  // two epilogue warpgroups x double buffer
+constexpr uint32_t kOutBlock = 2048;                   // 32 columns x (32 bf16 | 16 four-byte) token rows
+constexpr uint32_t kOutStaging = kEpiWarps * 2 * kOutBlock;  // per epilogue warp, double-buffered
 constexpr size_t kSmemBytes =
     (size_t)kStages * (kBStageBytes + kWStageBytes) + kOutStaging + 1024 /*barriers*/ + 1024 /*align*/;
 static_assert(kSmemBytes <= 232448, "shared memory exceeds the per-CTA limit");
@@ -83,7 +88,7 @@ struct Params {
     CUtensorMap tm_b;
     CUtensorMap tm_w0;
     CUtensorMap tm_w1;
-    CUtensorMap tm_out;  // output [M][ld_out], box 128 columns x (kOutBlock / 128 / esz) rows
+    CUtensorMap tm_out;  // output [M][ld_out], box 32 columns x (kOutBlock / 32 / esz) rows
     int64_t M, N, K;
     int64_t n_split;
     int64_t ld_out;
@@ -147,41 +152,44 @@ __device__ __forceinline__ void add_exact_totals(int32_t *tot, const uint32_t (&
     }
 }
 
-// Write this thread's 128 token values of output column n through shared-memory
-// blocks of ROWS tokens x 128 columns, one TMA tensor store per block
-// (double-buffered per warpgroup; the store clips rows and columns past the edge).
+// Write this thread's 128 token values of output column n: each epilogue warp
+// stages blocks of ROWS tokens x its 32 columns in its own double-buffered
+// shared-memory slots and lane 0 stores each block with one TMA tensor store
+// (which clips rows and columns past the edge).  No warp waits on another.
+// xs4[g] holds x_scale of token row m0 + 128h + 32g + lane (loaded when the tile starts).
 template <int ROWS, int EPI>
-__device__ __forceinline__ void store_tile_tma(const Params &p, const int32_t (&tot)[128], uint8_t *obuf, int h,
-                                               int q, int lane, int64_t n0, int64_t m0, float ws, float bias) {
+__device__ __forceinline__ void store_tile_tma(const Params &p, const int32_t (&tot)[128], const float (&xs4)[4],
+                                               uint8_t *wbuf_out, int h, int q, int lane, int64_t n0, int64_t m0,
+                                               float ws, float bias) {
     constexpr uint32_t esz = EPI == EPI_DEQUANT_BF16 ? 2u : 4u;
-    static_assert(ROWS * 128 * esz == kOutBlock, "block geometry");
-    const bool issuer = (q == 0 && lane == 0);
+    static_assert(ROWS * 32 * esz == kOutBlock, "block geometry");
 #pragma unroll
     for (int j = 0; j < 128 / ROWS; ++j) {
-        uint8_t *buf = obuf + (uint32_t)(h * 2 + (j & 1)) * kOutBlock;
+        uint8_t *buf = wbuf_out + (uint32_t)(j & 1) * kOutBlock;
         const int64_t mb = m0 + 128 * h + ROWS * j;
-        float xs_l = 0.0f;
-        if (EPI != EPI_ACC_I32 && lane < ROWS && mb + lane < p.M) xs_l = __ldg(p.x_scale + mb + lane);
-        if (issuer) tma_store_wait_read<1>();  // the store that last read `buf` is done
-        named_bar_sync(1 + h, 128);
-        uint8_t *col = buf + (uint32_t)(q * 32 + lane) * esz;
+        const float xs_l = xs4[(ROWS * j) / 32];
+        const int xs_lane0 = (ROWS * j) % 32;
+        if (lane == 0) tma_store_wait_read<1>();  // the store that last read `buf` is done
+        __syncwarp();
+        uint8_t *col = buf + (uint32_t)lane * esz;
 #pragma unroll
         for (int i = 0; i < ROWS; ++i) {
-            const float xs = __shfl_sync(0xffffffffu, xs_l, i);
             const int32_t acc = tot[ROWS * j + i];
             if (EPI == EPI_ACC_I32) {
-                *reinterpret_cast<int32_t *>(col + i * 128 * esz) = acc;
+                *reinterpret_cast<int32_t *>(col + i * 32 * esz) = acc;
             } else if (EPI == EPI_DEQUANT_BF16) {
+                const float xs = __shfl_sync(0xffffffffu, xs_l, xs_lane0 + i);
                 const float tv = __fmul_rn(__int2float_rn(acc), xs);
-                *reinterpret_cast<__nv_bfloat16 *>(col + i * 128 * esz) = __float2bfloat16_rn(__fmaf_rn(tv, ws, bias));
+                *reinterpret_cast<__nv_bfloat16 *>(col + i * 32 * esz) = __float2bfloat16_rn(__fmaf_rn(tv, ws, bias));
             } else {
-                *reinterpret_cast<float *>(col + i * 128 * esz) = __fmul_rn(__int2float_rn(acc), xs);
+                const float xs = __shfl_sync(0xffffffffu, xs_l, xs_lane0 + i);
+                *reinterpret_cast<float *>(col + i * 32 * esz) = __fmul_rn(__int2float_rn(acc), xs);
             }
         }
         fence_proxy_async_smem();
-        named_bar_sync(1 + h, 128);
-        if (issuer) {
-            tma_store_2d(&p.tm_out, buf, (int)n0, (int)mb);
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(&p.tm_out, buf, (int)(n0 + 32 * q), (int)mb);
             tma_store_commit();
         }
     }
@@ -399,6 +407,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) i8gemm_
                 ws = n < p.n_split ? __ldg(p.w_scale0 + n) : __ldg(p.w_scale1 + (n - p.n_split));
                 if (p.bias) bias = __bfloat162float(p.bias[n]);
             }
+            float xs4[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // x_scale of rows m0 + 128h + 32g + lane
+            if (p.epi != EPI_ACC_I32) {
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const int64_t m = m0 + 128 * h + 32 * g + lane;
+                    if (m < p.M) xs4[g] = __ldg(p.x_scale + m);
+                }
+            }
             int32_t tot[128];  // exact running sums for this thread's 128 token columns
 #pragma unroll
             for (int i = 0; i < 128; ++i) tot[i] = 0;
@@ -418,25 +434,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) i8gemm_
                 if (lane == 0) mbar_arrive_cluster(lead_accempty);  // this warp is done with the accumulator
                 ++chunk;
             }
-            // The staged store below synchronises the warpgroup on named barriers, so its
-            // four warps agree on giving up (a timed-out wait in one of them) before it.
-            if (p.use_tma_out) ok = named_bar_and(1 + h, 128, ok);
             if (!ok) break;
             if (p.use_tma_out) {
+                uint8_t *mine = obuf + (uint32_t)(warp - 8) * 2 * kOutBlock;
                 if (p.epi == EPI_ACC_I32)
-                    store_tile_tma<16, EPI_ACC_I32>(p, tot, obuf, h, q, lane, n0, m0, ws, bias);
+                    store_tile_tma<16, EPI_ACC_I32>(p, tot, xs4, mine, h, q, lane, n0, m0, ws, bias);
                 else if (p.epi == EPI_DEQUANT_BF16)
-                    store_tile_tma<32, EPI_DEQUANT_BF16>(p, tot, obuf, h, q, lane, n0, m0, ws, bias);
+                    store_tile_tma<32, EPI_DEQUANT_BF16>(p, tot, xs4, mine, h, q, lane, n0, m0, ws, bias);
                 else
-                    store_tile_tma<16, EPI_ROWSCALE_F32>(p, tot, obuf, h, q, lane, n0, m0, ws, bias);
+                    store_tile_tma<16, EPI_ROWSCALE_F32>(p, tot, xs4, mine, h, q, lane, n0, m0, ws, bias);
                 continue;
             }
             // Write token rows m0 + 128h + 32j + i of output column n.
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int64_t mb = m0 + 128 * h + 32 * j;
-                float xs_l = 0.0f;
-                if (p.epi != EPI_ACC_I32 && mb + lane < p.M) xs_l = __ldg(p.x_scale + mb + lane);
+                const float xs_l = xs4[j];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const float xs = __shfl_sync(0xffffffffu, xs_l, i);
@@ -457,7 +470,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) i8gemm_
         }
     }
 
-    if (wg >= 2 && (warp & 3) == 0 && lane == 0 && p.use_tma_out) tma_store_wait_all<0>();  // smem must outlive the stores
+    if (wg >= 2 && lane == 0 && p.use_tma_out) tma_store_wait_all<0>();  // smem must outlive the stores
     __syncwarp();
     tc_fence_before();
     cluster_sync_all();  // no CTA leaves while its peer's MMAs, arrivals or stores may touch it
@@ -517,8 +530,8 @@ int launch_i8gemm(const I8GemmProblem &q, cudaStream_t st) {
                                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
         p.use_tma_out = ((q.ld_out * esz) % 16 == 0 && ((uintptr_t)q.out & 15) == 0) ? 1 : 0;
         if (p.use_tma_out) {
-            rc = encode_tmap_2d(&p.tm_out, dt, q.out, (uint64_t)q.N, (uint64_t)q.M, (uint64_t)q.ld_out * esz, 128,
-                                kOutBlock / (128 * esz), CU_TENSOR_MAP_SWIZZLE_NONE);
+            rc = encode_tmap_2d(&p.tm_out, dt, q.out, (uint64_t)q.N, (uint64_t)q.M, (uint64_t)q.ld_out * esz, 32,
+                                kOutBlock / (32 * esz), CU_TENSOR_MAP_SWIZZLE_NONE);
             if (rc) return rc;
         }
     }

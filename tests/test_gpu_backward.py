@@ -61,3 +61,18 @@ def test_linear_dx_int8_gemm_exact(ops):
     s = np.ones(N, np.float32)
     dx = ops.linear_dx_int8(bf16_dev(dy), d(w8), d(s), (16, 16, 1))
     assert_bf16_parity(bf16_np(dx), O.linear_dx_int8(dy, w8, s, (16, 16, 1)))
+
+
+def test_linear_dx_int8_large_accumulators(ops):
+    """Accumulators past 2^22 (dy rows of ones against +127 weight rows) beside small ones in
+    the same tile: the fp32 row-scale epilogue converts both ranges exactly."""
+    rng = np.random.default_rng(23)
+    M, N, K = 130, 1024, 256
+    dy = rng.standard_normal((M, N)).astype(np.float32)
+    dy[::3] = 1.0
+    dy = I.bf16_bits(dy)
+    w8 = rng.integers(-127, 128, (N, K)).astype(np.int8)
+    w8[:, :40] = 127
+    s = np.ones(N, np.float32)
+    dx = ops.linear_dx_int8(bf16_dev(dy), d(w8), d(s), (16, 16, 1))
+    assert_bf16_parity(bf16_np(dx), O.linear_dx_int8(dy, w8, s, (16, 16, 1)))

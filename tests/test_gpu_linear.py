@@ -153,3 +153,22 @@ def test_decode_gemv(ops, M, K, N, rot, with_bias):
     assert_int8_parity(qg.cpu().numpy(), qr)
     same = np.all(qg.cpu().numpy() == qr, axis=1)
     assert_rows_explained(bf16_np(y), O.dequant(O.gemm_s8(qr, w8), sr, ws, bias_np), same)
+
+
+def test_linear_large_accumulators_exact(ops):
+    """One-hot x and W rows rotate to +-127 code patterns, so matching rows accumulate 127^2*K
+    (far past 2^22) next to zeros: the bf16 epilogue must convert both exactly."""
+    rot, M, K, N = (64, 64, 1), 8, 4096, 256
+    x = np.zeros((M, K), np.float32)
+    w = np.zeros((N, K), np.float32)
+    for r in range(M):
+        x[r, 37 * r] = 1.0 + r
+    for n in range(N):
+        w[n, (37 * n) % K] = 0.5
+    xb, wb = I.bf16_bits(x), I.bf16_bits(w)
+    bias = I.bf16_bits(np.linspace(-1, 1, N).astype(np.float32))
+    w8, ws = O.prepare_weight(wb, rot)
+    y = ops.linear(bf16_dev(xb), d(w8), d(ws), bf16_dev(bias), rot)
+    y_r = O.linear(xb, w8, ws, bias, rot)
+    assert np.array_equal(bf16_np(y), y_r)
+    assert np.abs(O.linear_acc(xb, w8, rot)[0]).max() == 127 * 127 * K
