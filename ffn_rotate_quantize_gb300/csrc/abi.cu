@@ -126,6 +126,11 @@ int check_rot(gbq_rot r, int64_t K, int *logn) {
 // Rotate(+quantize) rows of an input through the right kernel.
 int run_rotq(const char *what, gbq_rot rot, int logn, int in_kind, int out_kind, RotArgs a, cudaStream_t st) {
     cudaError_t e;
+    DevState *d = nullptr;
+    int rc = init_current(&d);
+    if (rc != GBQ_OK) return rc;
+    a.status = d->status;
+    a.num_sms = d->sms;
     if (logn == 0) {
         if (in_kind != IN_BF16 || out_kind == OUT_BF16)
             return fail(GBQ_ENOTSUP, "%s: identity rotation is supported for bf16 quantization only", what);

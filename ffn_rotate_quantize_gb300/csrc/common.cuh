@@ -133,6 +133,21 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *map, uin
         : "memory");
 }
 
+// Untiled bulk copies (both addresses 16-byte aligned, size a multiple of 16).
+// Global -> shared, completing `bytes` of transaction count on `bar`.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+// Shared -> global, tracked by the issuing thread's bulk groups (commit + wait below).
+__device__ __forceinline__ void bulk_s2g(void *dst, const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+
 // Shared -> global tensor store (bulk-group completion) and its waits.
 __device__ __forceinline__ void tma_store_2d(const void *map, const void *smem_src, int x, int y) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(x),

@@ -6,18 +6,25 @@
 //     V = (H_n X H_n) / n        (= (H_n (x) H_n) x / sqrt(n*n), H_n symmetric)
 // in fp32; then, per row, amax = max|v|, s = amax/127, q = clamp(rne(v/s), +-127).
 //
-// GB300 design.  One group is owned by TPG threads; every value is carried in a
-// float2 pair so that each Hadamard level runs on the packed fp32x2 pipe:
+// GB300 design.  The kernel is persistent and HBM-streaming: each CTA holds a
+// few "teams" (one warp, or the threads of one row when a row needs more), and
+// each team loops over rows.  Its leader thread bulk-copies (cp.async.bulk) the
+// input rows into a double-buffered shared-memory stage two rows ahead, so the
+// HBM stream never waits for arithmetic, and the team writes each finished row
+// back with one bulk store from shared memory.  The rotation itself: one group
+// is owned by TPG threads and every value is carried in a float2 pair so that
+// each Hadamard level runs on the packed fp32x2 pipe:
 //   n <= 64  pass 1: thread t holds columns 2t, 2t+1 (pair = the two columns);
 //            pass 2: thread t holds rows t, t+n/2     (pair = the two rows);
 //   n == 128 pass 1: thread t holds column t, pair = (row i, row i+64);
 //            pass 2: thread t holds row t,    pair = (col j, col j+64).
-// Pass 1 applies H_n down the columns, a padded shared tile of float2 pairs
-// turns columns into rows (16-byte accesses, conflict-free), pass 2 applies H_n
-// along the rows.  Levels run in a fixed order (H4/2 on base-4 digits from the
-// low bit up, then the unnormalised H2 on the top bit when log2 n is odd, whose
-// two sqrt(2) factors are removed by one final exact halving), so every kernel
-// that uses this core produces bit-identical rotated values.
+// Pass 1 applies H_n down the columns (reading the staged input), a padded
+// shared tile of float2 pairs turns columns into rows (16-byte accesses,
+// conflict-free), pass 2 applies H_n along the rows; the tile then holds the
+// row's output for the bulk store.  Levels run in a fixed order (H4/2 on base-4
+// digits from the low bit up, then the unnormalised H2 on the top bit when
+// log2 n is odd, whose two sqrt(2) factors are removed by one final exact
+// halving), so every kernel that uses this core produces bit-identical values.
 // Quantize: r = 1/s once per row; t = v*r; the code is rint(t) (read out of the
 // low byte of t + 1.5*2^23), which equals rne(fl(v/s)) unless t lies within
 // 1e-4 of a half-integer (|t - v/s| <= 128*2^-23 and |fl(v/s) - v/s| <= 2^-18
@@ -43,7 +50,16 @@ struct RotArgs {
     float *out_scale;         // per-row scale (quantizing outputs)
     int64_t M, K;
     int G;                    // groups per row
-    int rows_per_cta;
+    unsigned int *status;     // device status word (bounded-wait timeouts)
+    int num_sms;
+    // Set by the launcher (launch_rotq_t):
+    int team_threads;         // threads of one team (a multiple of 32)
+    int rows_per_team;        // rows a team rotates at once (several only when a row needs < 32 threads)
+    int stages;               // input stages per team (1 or 2)
+    uint32_t row_in_bytes;    // bytes of one input row (one of the two GLU inputs)
+    uint32_t stage_bytes;     // one stage: rows_per_team x inputs x row_in_bytes (rounded to 128)
+    uint32_t tiles_bytes;     // the transpose tiles of one team (rounded to 128)
+    uint32_t team_bytes;      // stages + tiles + barriers / scratch
 };
 
 // Shapes of the packed two-pass rotation of one n x n group.
@@ -124,16 +140,49 @@ __device__ __forceinline__ void hadamard_pairs(float2 (&v)[1 << LOG]) {
     }
 }
 
-// H_n for the pass layout of RotGeom<LOGN>: for n = 128 the pair holds the top
-// index bit, so the H4 digits run packed and the H2 combines the two halves.
-template <int LOGN>
-__device__ __forceinline__ void hadamard_pass(float2 (&v)[RotGeom<LOGN>::NP]) {
-    if constexpr (RotGeom<LOGN>::PAIR_TOP) {
-        hadamard_pairs<LOGN - 1>(v);
+// Unnormalised H2 across the two halves of every pair: (x, y) -> (x + y, x - y).
+template <int NP>
+__device__ __forceinline__ void h2_pairs(float2 (&v)[NP]) {
 #pragma unroll
-        for (int i = 0; i < RotGeom<LOGN>::NP; ++i) {
-            const float a = v[i].x, b = v[i].y;
-            v[i] = f2(__fadd_rn(a, b), __fsub_rn(a, b));
+    for (int i = 0; i < NP; ++i) {
+        const float a = v[i].x, b = v[i].y;
+        v[i] = f2(__fadd_rn(a, b), __fsub_rn(a, b));
+    }
+}
+
+// H_n for the pass layout of RotGeom<LOGN>, in the fixed level order every
+// rotation kernel of the library shares (so their rotated values agree bit for
+// bit).  COLS selects the first pass (H_n down the columns, index i) or the
+// second (along the rows, index j):
+//   n = 16, 32 : digits (0,1), (2,3), then H2 on bit 4 for n = 32, both passes;
+//   n = 64     : columns (0,1), (2,3), (4,5); rows (4,5), (0,1), (2,3);
+//   n = 128    : columns H2 on bit 6, then (0,1), (2,3), (4,5);
+//                rows (4,5), H2 on bit 6, (0,1), (2,3).
+// (For n = 128 the pair holds bit 6, so its H2 combines the two halves.)
+template <int LOGN, bool COLS>
+__device__ __forceinline__ void hadamard_pass(float2 (&v)[RotGeom<LOGN>::NP]) {
+    constexpr int NP = RotGeom<LOGN>::NP;
+    if constexpr (LOGN == 7) {
+        if constexpr (COLS) {
+            h2_pairs<NP>(v);
+            h4_level<NP, 0>(v);
+            h4_level<NP, 2>(v);
+            h4_level<NP, 4>(v);
+        } else {
+            h4_level<NP, 4>(v);
+            h2_pairs<NP>(v);
+            h4_level<NP, 0>(v);
+            h4_level<NP, 2>(v);
+        }
+    } else if constexpr (LOGN == 6) {
+        if constexpr (COLS) {
+            h4_level<NP, 0>(v);
+            h4_level<NP, 2>(v);
+            h4_level<NP, 4>(v);
+        } else {
+            h4_level<NP, 4>(v);
+            h4_level<NP, 0>(v);
+            h4_level<NP, 2>(v);
         }
     } else {
         hadamard_pairs<LOGN>(v);
@@ -184,18 +233,62 @@ __device__ __forceinline__ float2 load_in2(const RotArgs &p, int64_t row, int64_
     }
 }
 
-// The rotation of one group (pass 1, transpose through T, pass 2) for the
-// thread (row, g, t); leaves this thread's pass-2 pairs in v.  Every thread of
-// the CTA must call it (it contains one __syncthreads()).  Inactive threads
-// touch neither global memory nor the tile and return zeros.
+// Pass-1 tile write: after H_n down the columns (c), write the column pairs of
+// this thread into the transpose tile T of its group.
+template <int LOGN>
+__device__ __forceinline__ void pass1_store_tile(const float2 (&c)[RotGeom<LOGN>::NP], int t, float2 *T) {
+    using Geo = RotGeom<LOGN>;
+    constexpr int N = Geo::N, NP = Geo::NP, PP = Geo::PP;
+    if constexpr (Geo::PAIR_TOP) {
+        // tile row i, float2 column (t mod N/2), half (t div N/2) <- X[i][t]
+        float *Tf = reinterpret_cast<float *>(T);
+        const int cc = t & (N / 2 - 1), hh = t >> (LOGN - 1);
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+            Tf[(i * PP + cc) * 2 + hh] = c[i].x;
+            Tf[((i + N / 2) * PP + cc) * 2 + hh] = c[i].y;
+        }
+    } else {
+        // tile row i' holds pairs (X[i'][j], X[i' + N/2][j])
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i)
+            *reinterpret_cast<float4 *>(&T[i * PP + 2 * t]) = make_float4(c[i].x, c[i + N / 2].x, c[i].y, c[i + N / 2].y);
+    }
+}
+
+// Pass 2: read this thread's row pairs from the tile and apply H_n along the rows
+// (then the exact halving that normalises the two H2 levels of an odd log2 n).
+template <int LOGN>
+__device__ __forceinline__ void pass2_from_tile(bool active, int t, const float2 *T, float2 (&v)[RotGeom<LOGN>::NP]) {
+    using Geo = RotGeom<LOGN>;
+    constexpr int NP = Geo::NP, PP = Geo::PP;
+#pragma unroll
+    for (int j2 = 0; j2 < NP / 2; ++j2) {
+        const float4 f =
+            active ? *reinterpret_cast<const float4 *>(&T[t * PP + 2 * j2]) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[2 * j2] = f2(f.x, f.y);
+        v[2 * j2 + 1] = f2(f.z, f.w);
+    }
+    hadamard_pass<LOGN, false>(v);
+    if (LOGN & 1) {
+        const float2 half2 = f2(0.5f, 0.5f);
+#pragma unroll
+        for (int j = 0; j < NP; ++j) v[j] = __fmul2_rn(v[j], half2);  // the two H2 levels: (1/sqrt2)^2
+    }
+}
+
+// The rotation of one group reading its input straight from global memory (the
+// decode kernel's x): pass 1, transpose through T, pass 2; leaves this thread's
+// pass-2 pairs in v.  Every thread of the CTA must call it (it contains one
+// __syncthreads()).  Inactive threads touch neither global memory nor the tile
+// and return zeros.
 template <int LOGN, int IN>
 __device__ __forceinline__ void rot_group_core(const RotArgs &p, int64_t row, bool active, int g, int t, float2 *T,
                                                float2 (&v)[RotGeom<LOGN>::NP]) {
     using Geo = RotGeom<LOGN>;
-    constexpr int N = Geo::N, NP = Geo::NP, PP = Geo::PP;
+    constexpr int N = Geo::N, NP = Geo::NP;
     float2 c[NP];
     const int64_t goff = (int64_t)g * N * N;
-    // ---------------- pass 1: load columns, H_n down each column ----------------
     if (active) {
         const int64_t rbase = row * p.ld_in + goff;
 #pragma unroll
@@ -212,40 +305,10 @@ __device__ __forceinline__ void rot_group_core(const RotArgs &p, int64_t row, bo
 #pragma unroll
         for (int i = 0; i < NP; ++i) c[i] = f2(0.f, 0.f);
     }
-    hadamard_pass<LOGN>(c);
-    if (active) {
-        if constexpr (Geo::PAIR_TOP) {
-            // tile row i, float2 column (t mod N/2), half (t div N/2) <- X[i][t]
-            float *Tf = reinterpret_cast<float *>(T);
-            const int cc = t & (N / 2 - 1), hh = t >> (LOGN - 1);
-#pragma unroll
-            for (int i = 0; i < NP; ++i) {
-                Tf[(i * PP + cc) * 2 + hh] = c[i].x;
-                Tf[((i + N / 2) * PP + cc) * 2 + hh] = c[i].y;
-            }
-        } else {
-            // tile row i' holds pairs (X[i'][j], X[i' + N/2][j])
-#pragma unroll
-            for (int i = 0; i < N / 2; ++i)
-                *reinterpret_cast<float4 *>(&T[i * PP + 2 * t]) =
-                    make_float4(c[i].x, c[i + N / 2].x, c[i].y, c[i + N / 2].y);
-        }
-    }
+    hadamard_pass<LOGN, true>(c);
+    if (active) pass1_store_tile<LOGN>(c, t, T);
     __syncthreads();
-    // ---------------- pass 2: read row pairs, H_n along each row ----------------
-#pragma unroll
-    for (int j2 = 0; j2 < NP / 2; ++j2) {
-        const float4 f =
-            active ? *reinterpret_cast<const float4 *>(&T[t * PP + 2 * j2]) : make_float4(0.f, 0.f, 0.f, 0.f);
-        v[2 * j2] = f2(f.x, f.y);
-        v[2 * j2 + 1] = f2(f.z, f.w);
-    }
-    hadamard_pass<LOGN>(v);
-    if (LOGN & 1) {
-        const float2 half2 = f2(0.5f, 0.5f);
-#pragma unroll
-        for (int j = 0; j < NP; ++j) v[j] = __fmul2_rn(v[j], half2);  // the two H2 levels: (1/sqrt2)^2
-    }
+    pass2_from_tile<LOGN>(active, t, T, v);
 }
 
 // Element offset, within the row, of output half h of thread t in group g:
@@ -340,75 +403,279 @@ __device__ __forceinline__ void store_codes(void *out, int64_t off, const uint32
     }
 }
 
-template <int LOGN, int IN, int OUT>
-__global__ void __launch_bounds__(RotqMaxThreads<LOGN>::value) rotq_kernel(RotArgs p) {
-    using Geo = RotGeom<LOGN>;
-    constexpr int NP = Geo::NP, TPG = Geo::TPG;
-    extern __shared__ __align__(16) float2 smem2[];
-    const int G = p.G;
-    const int row_threads = G * TPG;
-    const int tid = threadIdx.x;
-    const int rloc = tid / row_threads;
-    const int rem = tid - rloc * row_threads;
-    const int g = rem / TPG;
-    const int t = rem - g * TPG;
-    const int64_t row = (int64_t)blockIdx.x * p.rows_per_cta + rloc;
-    const bool active = row < p.M;
-    float2 *T = smem2 + (size_t)(rloc * G + g) * Geo::TILE;
-    unsigned *s_amax = reinterpret_cast<unsigned *>(smem2 + (size_t)p.rows_per_cta * G * Geo::TILE);
-    if (tid < p.rows_per_cta) s_amax[tid] = 0u;
+// ---------------------------------------------------------------- staged input
+// Number of input tensors and bytes per input element of an input kind.
+__host__ __device__ constexpr int in_count(int in_kind) { return (in_kind == IN_GLU_BF16 || in_kind == IN_ACC_GLU) ? 2 : 1; }
+__host__ __device__ constexpr int in_elem_bytes(int in_kind) {
+    return in_kind == IN_S8_ROWSCALE ? 1 : (in_kind == IN_F32 || in_kind == IN_ACC_GLU) ? 4 : 2;
+}
+__host__ __device__ constexpr int out_elem_bytes(int out_kind) { return out_kind == OUT_S8 ? 1 : 2; }
 
-    float2 v[NP];
-    rot_group_core<LOGN, IN>(p, row, active, g, t, T, v);
-
-    if constexpr (OUT == OUT_BF16) {
-        if (!active) return;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + row * p.K +
-                                                   out_offset<LOGN>(g, t, h));
-#pragma unroll
-            for (int j8 = 0; j8 < NP / 8; ++j8) {
-                uint32_t w[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float a = h ? v[8 * j8 + 2 * k].y : v[8 * j8 + 2 * k].x;
-                    const float b = h ? v[8 * j8 + 2 * k + 1].y : v[8 * j8 + 2 * k + 1].x;
-                    __nv_bfloat162 b2 = __floats2bfloat162_rn(a, b);
-                    w[k] = *reinterpret_cast<uint32_t *>(&b2);
-                }
-                dst[j8] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-        }
-        return;
-    } else {
-        // ---------------- row amax ----------------
-        float m = 0.0f;
-#pragma unroll
-        for (int j = 0; j < NP; ++j) m = fmaxf(m, pair_max_abs(v[j]));
-        constexpr int W = TPG < 32 ? TPG : 32;  // lanes of one group inside a warp
-#pragma unroll
-        for (int o = W / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if ((t & (W - 1)) == 0) atomicMax(&s_amax[rloc], __float_as_uint(m));
-        __syncthreads();
-        if (!active) return;
-        const float amax = __uint_as_float(s_amax[rloc]);
-        const float s = __fdiv_rn(amax, 127.0f);
-        if (rem == 0) p.out_scale[row] = s;
-        uint32_t words[2][NP / 4];
-        quant_codes<NP>(v, s, words);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) store_codes<OUT, NP / 4>(p.out, row * p.K + out_offset<LOGN>(g, t, h), words[h]);
+// Elements idx, idx + 1 (idx even, index within the row) of a staged row as an
+// fp32 pair, with the same arithmetic as load_in2.  s0 / s1: the row's staged
+// input(s); rs: the row's scale (IN_S8_ROWSCALE: s[row]; IN_ACC_GLU: x_scale[row]).
+template <int IN>
+__device__ __forceinline__ float2 staged_pair(const RotArgs &p, const uint8_t *s0, const uint8_t *s1, float rs,
+                                              int idx) {
+    if constexpr (IN == IN_BF16) {
+        const uint32_t w = *reinterpret_cast<const uint32_t *>(s0 + 2 * idx);
+        return f2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    } else if constexpr (IN == IN_F32) {
+        return *reinterpret_cast<const float2 *>(s0 + 4 * idx);
+    } else if constexpr (IN == IN_GLU_BF16) {
+        const uint32_t wg = *reinterpret_cast<const uint32_t *>(s0 + 2 * idx);
+        const uint32_t wu = *reinterpret_cast<const uint32_t *>(s1 + 2 * idx);
+        return f2(silu_mul(__uint_as_float(wg << 16), __uint_as_float(wu << 16)),
+                  silu_mul(__uint_as_float(wg & 0xFFFF0000u), __uint_as_float(wu & 0xFFFF0000u)));
+    } else if constexpr (IN == IN_S8_ROWSCALE) {
+        const char2 q = *reinterpret_cast<const char2 *>(s0 + idx);
+        return __fmul2_rn(f2((float)q.x, (float)q.y), f2(rs, rs));
+    } else {  // IN_ACC_GLU
+        const int2 ag = *reinterpret_cast<const int2 *>(s0 + 4 * idx);
+        const int2 au = *reinterpret_cast<const int2 *>(s1 + 4 * idx);
+        const float2 sg = __ldg(reinterpret_cast<const float2 *>(p.col_scale0 + idx));
+        const float2 su = __ldg(reinterpret_cast<const float2 *>(p.col_scale1 + idx));
+        return f2(silu_mul(dequant_bf16_value(ag.x, rs, sg.x), dequant_bf16_value(au.x, rs, su.x)),
+                  silu_mul(dequant_bf16_value(ag.y, rs, sg.y), dequant_bf16_value(au.y, rs, su.y)));
     }
 }
 
-// Shared memory bytes for one launch of rotq_kernel.
-__host__ __device__ inline size_t rotq_smem_bytes(int logn, int G, int rows_per_cta) {
-    const int n = 1 << logn;
-    const bool pt = logn >= 7;
-    const int rows = pt ? n : n / 2, cols = pt ? n / 2 : n;
-    const size_t tile = (size_t)rows * (cols + 2) + 8;
-    return (size_t)rows_per_cta * G * tile * sizeof(float2) + (size_t)rows_per_cta * sizeof(unsigned) + 16;
+// One element of a staged row (the same arithmetic as load_in).
+template <int IN>
+__device__ __forceinline__ float staged_one(const RotArgs &p, const uint8_t *s0, const uint8_t *s1, float rs, int idx) {
+    if constexpr (IN == IN_BF16) {
+        return bf16_to_float(*reinterpret_cast<const uint16_t *>(s0 + 2 * idx));
+    } else if constexpr (IN == IN_F32) {
+        return *reinterpret_cast<const float *>(s0 + 4 * idx);
+    } else if constexpr (IN == IN_GLU_BF16) {
+        return silu_mul(bf16_to_float(*reinterpret_cast<const uint16_t *>(s0 + 2 * idx)),
+                        bf16_to_float(*reinterpret_cast<const uint16_t *>(s1 + 2 * idx)));
+    } else if constexpr (IN == IN_S8_ROWSCALE) {
+        return __fmul_rn((float)*reinterpret_cast<const int8_t *>(s0 + idx), rs);
+    } else {
+        const int32_t ag = *reinterpret_cast<const int32_t *>(s0 + 4 * idx);
+        const int32_t au = *reinterpret_cast<const int32_t *>(s1 + 4 * idx);
+        return silu_mul(dequant_bf16_value(ag, rs, __ldg(p.col_scale0 + idx)),
+                        dequant_bf16_value(au, rs, __ldg(p.col_scale1 + idx)));
+    }
+}
+
+// Pass-1 values of thread t of group g from a staged row.
+template <int LOGN, int IN>
+__device__ __forceinline__ void staged_columns(const RotArgs &p, const uint8_t *s0, const uint8_t *s1, float rs, int g,
+                                               int t, float2 (&c)[RotGeom<LOGN>::NP]) {
+    using Geo = RotGeom<LOGN>;
+    constexpr int N = Geo::N, NP = Geo::NP;
+    const int goff = g * N * N;
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+        if constexpr (Geo::PAIR_TOP)  // column t, rows i and i + N/2
+            c[i] = f2(staged_one<IN>(p, s0, s1, rs, goff + i * N + t),
+                      staged_one<IN>(p, s0, s1, rs, goff + (i + N / 2) * N + t));
+        else  // columns 2t, 2t+1 of row i
+            c[i] = staged_pair<IN>(p, s0, s1, rs, goff + i * N + 2 * t);
+    }
+}
+
+// ---------------------------------------------------------------- the kernel
+// Team-wide barrier: one warp, or a named barrier (id 1 + team) over the team.
+__device__ __forceinline__ void team_sync(int team, int team_threads) {
+    if (team_threads == 32)
+        __syncwarp();
+    else
+        named_bar_sync(1 + team, team_threads);
+}
+__device__ __forceinline__ bool team_all(int team, int team_threads, bool pred) {
+    if (team_threads == 32) return __all_sync(0xffffffffu, pred);
+    return named_bar_and(1 + team, team_threads, pred);
+}
+
+// Shared memory of one team: [stages][tiles][misc].  misc: full barriers (one
+// per stage), an abort flag, and one amax slot per warp of the team.
+constexpr uint32_t kRotMiscBytes = 256;
+
+template <int LOGN, int IN, int OUT>
+__global__ void __launch_bounds__(RotqMaxThreads<LOGN>::value) rotq_kernel(const __grid_constant__ RotArgs p) {
+    using Geo = RotGeom<LOGN>;
+    constexpr int NP = Geo::NP, TPG = Geo::TPG;
+    constexpr int NIN = in_count(IN);
+    constexpr uint32_t OESZ = out_elem_bytes(OUT);
+    extern __shared__ __align__(128) uint8_t smem[];
+
+    const int team = threadIdx.x / p.team_threads;
+    const int tt = threadIdx.x - team * p.team_threads;  // thread within the team
+    const int rt = p.G * TPG;                            // threads of one row
+    const int slot = tt / rt;                            // row slot within the team
+    const int rem = tt - slot * rt;
+    const int g = rem / TPG;
+    const int t = rem - g * TPG;
+    const bool used = slot < p.rows_per_team;
+    const bool leader = tt == 0;
+    const int rpt = p.rows_per_team;
+
+    uint8_t *tb = smem + (size_t)team * p.team_bytes;
+    uint8_t *stage0 = tb;
+    float2 *tiles = reinterpret_cast<float2 *>(tb + (size_t)p.stages * p.stage_bytes);
+    uint8_t *misc = tb + (size_t)p.stages * p.stage_bytes + p.tiles_bytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(misc);
+    volatile int *abort = reinterpret_cast<volatile int *>(misc + 16);
+    float *wmax = reinterpret_cast<float *>(misc + 32);  // one per warp of the team (<= 32)
+
+    float2 *T = tiles + (size_t)((used ? slot : 0) * p.G + g) * Geo::TILE;
+    uint8_t *ostage = reinterpret_cast<uint8_t *>(tiles + (size_t)(used ? slot : 0) * p.G * Geo::TILE);
+
+    const int64_t nunits = (p.M + rpt - 1) / rpt;
+    const int64_t u0 = (int64_t)blockIdx.x * (blockDim.x / p.team_threads) + team;
+    const int64_t ustride = (int64_t)gridDim.x * (blockDim.x / p.team_threads);
+    const uint32_t in_row_bytes = p.row_in_bytes;
+
+    // Leader: copy the inputs of row unit u into stage st.
+    auto issue = [&](int64_t u, int st) {
+        const int64_t r0 = u * rpt;
+        const int nr = (int)min((int64_t)rpt, p.M - r0);
+        uint8_t *dst = stage0 + (size_t)st * p.stage_bytes;
+        mbar_arrive_expect_tx(&full[st], (uint32_t)nr * NIN * in_row_bytes);
+        for (int r = 0; r < nr; ++r) {
+            const int64_t off = (r0 + r) * p.ld_in * in_elem_bytes(IN);
+            bulk_g2s(dst + (size_t)(r * NIN) * in_row_bytes, reinterpret_cast<const uint8_t *>(p.in0) + off,
+                     in_row_bytes, &full[st]);
+            if (NIN == 2)
+                bulk_g2s(dst + (size_t)(r * NIN + 1) * in_row_bytes, reinterpret_cast<const uint8_t *>(p.in1) + off,
+                         in_row_bytes, &full[st]);
+        }
+    };
+
+    if (leader) {
+        for (int s2 = 0; s2 < p.stages; ++s2) mbar_init(&full[s2], 1);
+        *abort = 0;
+        fence_mbar_init();
+    }
+    team_sync(team, p.team_threads);
+    // Iteration whose input was last issued into stage 0 / 1 (-1: none); team-uniform.
+    int64_t issued0 = -1, issued1 = -1;
+    for (int s2 = 0; s2 < p.stages; ++s2)
+        if (u0 + s2 * ustride < nunits) {
+            if (leader) issue(u0 + s2 * ustride, s2);
+            if (s2 == 0) issued0 = 0; else issued1 = 1;
+        }
+
+    int64_t it = 0;
+    bool failed = false;
+    for (int64_t u = u0; u < nunits; u += ustride, ++it) {
+        const int st = (int)(it % p.stages);
+        uint8_t *sbuf = stage0 + (size_t)st * p.stage_bytes;
+        {
+            bool ok = mbar_wait(&full[st], (uint32_t)((it / p.stages) & 1), p.status, abort);
+            if (!team_all(team, p.team_threads, ok)) {
+                failed = true;
+                break;
+            }
+        }
+        const int64_t row = u * rpt + slot;
+        const bool active = used && row < p.M;
+
+        // ---- pass 1 from the stage ----
+        float2 c[NP];
+        if (active) {
+            const uint8_t *s0 = sbuf + (size_t)(slot * NIN) * in_row_bytes;
+            float rs = 0.0f;
+            if (IN == IN_S8_ROWSCALE || IN == IN_ACC_GLU) rs = __ldg(p.in_scale + row);
+            staged_columns<LOGN, IN>(p, s0, s0 + in_row_bytes, rs, g, t, c);
+        } else {
+#pragma unroll
+            for (int i = 0; i < NP; ++i) c[i] = f2(0.f, 0.f);
+        }
+        hadamard_pass<LOGN, true>(c);
+        // The tile doubles as the previous row's output staging: its bulk store must have read it.
+        if (leader && it > 0) tma_store_wait_read<0>();
+        team_sync(team, p.team_threads);
+        if (active) pass1_store_tile<LOGN>(c, t, T);
+        team_sync(team, p.team_threads);
+        // Every thread has read the stage: refill it with the unit `stages` iterations ahead.
+        if (u + p.stages * ustride < nunits) {
+            if (leader) issue(u + p.stages * ustride, st);
+            if (st == 0) issued0 = it + p.stages; else issued1 = it + p.stages;
+        }
+
+        // ---- pass 2 ----
+        float2 v[NP];
+        pass2_from_tile<LOGN>(active, t, T, v);
+
+        if constexpr (OUT == OUT_BF16) {
+            team_sync(team, p.team_threads);  // every pass-2 read of the tiles is done
+            if (active) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(ostage + out_offset<LOGN>(g, t, h) * 2);
+#pragma unroll
+                    for (int j8 = 0; j8 < NP / 8; ++j8) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float a0 = h ? v[8 * j8 + 2 * k].y : v[8 * j8 + 2 * k].x;
+                            const float a1 = h ? v[8 * j8 + 2 * k + 1].y : v[8 * j8 + 2 * k + 1].x;
+                            __nv_bfloat162 b2 = __floats2bfloat162_rn(a0, a1);
+                            w[k] = *reinterpret_cast<uint32_t *>(&b2);
+                        }
+                        dst[j8] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+        } else {
+            // ---- row amax -> scale -> codes ----
+            float m = 0.0f;
+#pragma unroll
+            for (int j = 0; j < NP; ++j) m = fmaxf(m, pair_max_abs(v[j]));
+            float amax;
+            if (32 % rt == 0) {  // a row is rt consecutive lanes of one warp
+                for (int o = rt / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                amax = m;
+                team_sync(team, p.team_threads);  // every pass-2 read of the tiles is done
+            } else {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                if ((tt & 31) == 0) wmax[tt >> 5] = m;
+                team_sync(team, p.team_threads);  // also: every pass-2 read of the tiles is done
+                amax = wmax[0];
+                for (int w = 1; w < p.team_threads / 32; ++w) amax = fmaxf(amax, wmax[w]);
+            }
+            const float s = __fdiv_rn(amax, 127.0f);
+            if (active && rem == 0) p.out_scale[row] = s;
+            if (active) {
+                uint32_t words[2][NP / 4];
+                quant_codes<NP>(v, s, words);
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    store_codes<OUT, NP / 4>(ostage, out_offset<LOGN>(g, t, h), words[h]);
+            }
+        }
+        fence_proxy_async_smem();
+        team_sync(team, p.team_threads);
+        if (leader) {
+            const int64_t r0 = u * rpt;
+            const int nr = (int)min((int64_t)rpt, p.M - r0);
+            const uint32_t ob = (uint32_t)(p.K * OESZ);
+            for (int r = 0; r < nr; ++r)
+                bulk_s2g(reinterpret_cast<uint8_t *>(p.out) + (r0 + r) * (int64_t)ob,
+                         reinterpret_cast<const uint8_t *>(tiles) + (size_t)r * p.G * Geo::TILE * sizeof(float2), ob);
+            tma_store_commit();
+        }
+        // The amax slots are rewritten next row only after two more team barriers.
+    }
+    if (leader) {
+        tma_store_wait_all<0>();  // stores complete before the team's shared memory goes away
+        if (failed) {
+            // A wait gave up at iteration `it`: let every copy still in flight land (bounded) before leaving.
+            for (int s2 = 0; s2 < p.stages; ++s2) {
+                const int64_t is = s2 == 0 ? issued0 : issued1;
+                if (is < it) continue;
+                const uint32_t par = (uint32_t)((is / p.stages) & 1);
+                const uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(&full[s2], par) && globaltimer() - t0 < kWaitLimitNs) {
+                }
+            }
+        }
+    }
 }
 
 }  // namespace gbq

@@ -139,3 +139,39 @@ def test_dequant_act_quantize_matches_chain(ops, rot):
     v = O.rotate(O.silu_glu(gr, ur), rot)
     qr, sr = O.quantize(v)
     assert_int8_parity(q.cpu().numpy(), qr, (v / sr[:, None]).astype(np.float32))
+
+
+@pytest.mark.parametrize("rot,M", [((64, 64, 1), 3001), ((16, 16, 1), 2999), ((32, 32, 1), 2001),
+                                   ((16, 16, 5), 1999), ((64, 64, 2), 1201)])
+def test_quantize_act_many_rows(ops, rot, M):
+    """Many rows per persistent team: every input stage is refilled several times and the
+    last row unit is ragged."""
+    K = rot[0] * rot[1] * rot[2]
+    xb = _x(M, K, seed=M + K, outliers=max(1, K // 100))
+    q, s = ops.quantize_act(bf16_dev(xb), rot)
+    torch.cuda.synchronize()
+    qr, sr, vs = _oracle_q(xb, rot)
+    assert_scale_parity(s.cpu().numpy(), sr)
+    assert_int8_parity(q.cpu().numpy(), qr, vs)
+
+
+def test_quantize_act_glu_many_rows(ops):
+    rot, M = (128, 128, 1), 1500
+    H = rot[0] * rot[1]
+    rng = np.random.default_rng(15)
+    g = I.bf16_bits(rng.standard_normal((M, H), dtype=np.float32) * np.float32(3))
+    u = I.bf16_bits(rng.standard_normal((M, H), dtype=np.float32))
+    q, s = ops.quantize_act_glu(bf16_dev(g), bf16_dev(u), rot)
+    v = O.rotate(O.silu_glu(g, u), rot)
+    qr, sr = O.quantize(v)
+    assert_scale_parity(s.cpu().numpy(), sr)
+    assert_int8_parity(q.cpu().numpy(), qr, (v / sr[:, None]).astype(np.float32))
+
+
+@pytest.mark.parametrize("rot,N", [((64, 64, 1), 2500), ((32, 32, 1), 1999)])
+def test_dequant_weight_many_rows(ops, rot, N):
+    K = rot[0] * rot[1] * rot[2]
+    wb = I.bf16_bits(np.random.default_rng(14).standard_normal((N, K), dtype=np.float32) * np.float32(0.02))
+    w8, s = O.prepare_weight(wb, rot)
+    w = ops.dequant_weight(torch.from_numpy(w8).cuda(), torch.from_numpy(s).cuda(), rot)
+    assert_bf16_parity(bf16_np(w), O.dequant_weight(w8, s, rot))
