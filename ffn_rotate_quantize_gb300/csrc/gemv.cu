@@ -14,7 +14,7 @@
 // products against the quantized x, reduce across lanes and apply the dequant
 // epilogue (fp32(acc) * x_scale, fmaf with the row scale and bias, bf16).
 #include "gemm.h"
-#include "rotate_impl.cuh"
+#include "rotate_fast.cuh"
 
 namespace gbq {
 namespace {
@@ -36,37 +36,17 @@ struct GemvArgs {
     int rows_per_stage;
     uint32_t stage_bytes;   // rows_per_stage * K, multiple of 128
     uint32_t x_off, t_off, misc_off;
+    uint32_t xb_off;        // bf16 staging of the M token rows (three-pass n = 64 path), else 0
     unsigned int *status;
 };
 
-template <int LOGN>
-__global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(GemvArgs p) {
-    using Geo = RotGeom<LOGN>;
-    constexpr int NP = Geo::NP, TPG = Geo::TPG;
-
-    extern __shared__ __align__(128) uint8_t smem[];
-    uint8_t *stages = smem;
-    int8_t *xq = reinterpret_cast<int8_t *>(smem + p.x_off);
-    float2 *T = reinterpret_cast<float2 *>(smem + p.t_off);
-    float *xs_s = reinterpret_cast<float *>(smem + p.misc_off);
-    unsigned *amax_s = reinterpret_cast<unsigned *>(xs_s + kGvMaxM);
-    uint64_t *full = reinterpret_cast<uint64_t *>(amax_s + kGvMaxM);
-    int *abort_flag = reinterpret_cast<int *>(full + kGvStages);
-
+// Dot products of the staged weight slice against the quantized tokens xq (row
+// stride K) and the dequant epilogue; every thread of the CTA takes part.
+__device__ __forceinline__ void gemv_dot_phase(const GemvArgs &p, uint8_t *stages, const int8_t *xq,
+                                               const float *xs_s, uint64_t *full, int *abort_flag, int64_t r0,
+                                               int nrows, int nchunks) {
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int64_t r0 = (int64_t)blockIdx.x * p.rows_per_cta;
-    const int64_t r1 = min(p.N, r0 + p.rows_per_cta);
-    const int nrows = (int)(r1 - r0);
-    const int nchunks = (nrows + p.rows_per_stage - 1) / p.rows_per_stage;
-
-    if (tid == 0) {
-        for (int s = 0; s < kGvStages; ++s) mbar_init(&full[s], 1);
-        *abort_flag = 0;
-        fence_mbar_init();
-    }
-    if (tid < kGvMaxM) amax_s[tid] = 0u;
-    __syncthreads();
     auto issue = [&](int c) {
         const int rows = min(p.rows_per_stage, nrows - c * p.rows_per_stage);
         const uint32_t bytes = (uint32_t)rows * (uint32_t)p.K;
@@ -75,44 +55,11 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(GemvArgs p) {
         bulk_g2s(stages + (size_t)(c % kGvStages) * p.stage_bytes, p.w8 + (r0 + (int64_t)c * p.rows_per_stage) * p.K,
                  bytes, bar);
     };
-    if (tid == 0)
-        for (int c = 0; c < nchunks && c < kGvStages; ++c) issue(c);
-
-    // ---- rotate + quantize x (the same core and operation order as rotq_kernel) ----
-    const int row_threads = p.G * TPG;
-    const bool in_row = tid < row_threads;
-    const int g = in_row ? tid / TPG : 0;
-    const int t = in_row ? tid - g * TPG : 0;
-    RotArgs ra{};
-    ra.in0 = p.x;
-    ra.ld_in = p.K;
-    for (int m = 0; m < p.M; ++m) {
-        float2 v[NP];
-        rot_group_core<LOGN, IN_BF16>(ra, m, in_row, g, t, T + (size_t)g * Geo::TILE, v);
-        float mx = 0.0f;
-#pragma unroll
-        for (int j = 0; j < NP; ++j) mx = fmaxf(mx, pair_max_abs(v[j]));
-        constexpr int W = TPG < 32 ? TPG : 32;
-#pragma unroll
-        for (int o = W / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        if (in_row && (t & (W - 1)) == 0) atomicMax(&amax_s[m], __float_as_uint(mx));
-        __syncthreads();
-        const float s = __fdiv_rn(__uint_as_float(amax_s[m]), 127.0f);
-        if (tid == 0) xs_s[m] = s;
-        if (in_row) {
-            uint32_t words[2][NP / 4];
-            quant_codes<NP>(v, s, words);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) store_codes<OUT_S8, NP / 4>(xq, (int64_t)m * p.K + out_offset<LOGN>(g, t, h),
-                                                                   words[h]);
-        }
-        __syncthreads();
-    }
-
     // ---- stream the weight slice: dp4a dot products ----
     const int kq = (int)(p.K / 16);
     for (int c = 0; c < nchunks; ++c) {
-        if (!mbar_wait(&full[c % kGvStages], (uint32_t)((c / kGvStages) & 1), p.status, abort_flag)) break;
+        const bool ok = mbar_wait(&full[c % kGvStages], (uint32_t)((c / kGvStages) & 1), p.status, abort_flag);
+        if (!__syncthreads_and(ok)) break;  // every thread leaves together
         const int rows = min(p.rows_per_stage, nrows - c * p.rows_per_stage);
         const uint8_t *st = stages + (size_t)(c % kGvStages) * p.stage_bytes;
         for (int j = warp; j < rows; j += kGvThreads / 32) {
@@ -152,26 +99,175 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(GemvArgs p) {
 }
 
 template <int LOGN>
+__global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(GemvArgs p) {
+    using Geo = RotGeom<LOGN>;
+    constexpr int NP = Geo::NP, TPG = Geo::TPG;
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t *stages = smem;
+    int8_t *xq = reinterpret_cast<int8_t *>(smem + p.x_off);
+    float2 *T = reinterpret_cast<float2 *>(smem + p.t_off);
+    float *xs_s = reinterpret_cast<float *>(smem + p.misc_off);
+    unsigned *amax_s = reinterpret_cast<unsigned *>(xs_s + kGvMaxM);
+    uint64_t *full = reinterpret_cast<uint64_t *>(amax_s + kGvMaxM);
+    int *abort_flag = reinterpret_cast<int *>(full + kGvStages);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int64_t r0 = (int64_t)blockIdx.x * p.rows_per_cta;
+    const int64_t r1 = min(p.N, r0 + p.rows_per_cta);
+    const int nrows = (int)(r1 - r0);
+    const int nchunks = (nrows + p.rows_per_stage - 1) / p.rows_per_stage;
+
+    if (tid == 0) {
+        for (int s = 0; s < kGvStages; ++s) mbar_init(&full[s], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (tid < kGvMaxM) amax_s[tid] = 0u;
+    __syncthreads();
+    auto issue = [&](int c) {
+        const int rows = min(p.rows_per_stage, nrows - c * p.rows_per_stage);
+        const uint32_t bytes = (uint32_t)rows * (uint32_t)p.K;
+        uint64_t *bar = &full[c % kGvStages];
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_g2s(stages + (size_t)(c % kGvStages) * p.stage_bytes, p.w8 + (r0 + (int64_t)c * p.rows_per_stage) * p.K,
+                 bytes, bar);
+    };
+    const bool fast_x = (LOGN == 6 && p.G == 1);
+    uint64_t *xfull = full + kGvStages + 1;  // after the abort flag's slot
+    if (fast_x) {
+        // The tokens first (the rotation waits on them), then the weight slice, its copies spread
+        // over the eight warps (one row each, round robin) so that many are in flight at once.
+        if (tid == 0) {
+            mbar_init(xfull, 1);
+            fence_mbar_init();
+            mbar_arrive_expect_tx(xfull, (uint32_t)(p.M * p.K * 2));
+            bulk_g2s(smem + p.xb_off, p.x, (uint32_t)(p.M * p.K * 2), xfull);
+            for (int c = 0; c < nchunks && c < kGvStages; ++c) {
+                const int rows = min(p.rows_per_stage, nrows - c * p.rows_per_stage);
+                mbar_arrive_expect_tx(&full[c], (uint32_t)rows * (uint32_t)p.K);
+            }
+        }
+        __syncthreads();
+        if (lane == 0)
+            for (int c = 0; c < nchunks && c < kGvStages; ++c) {
+                const int rows = min(p.rows_per_stage, nrows - c * p.rows_per_stage);
+                for (int j = warp; j < rows; j += kGvThreads / 32)
+                    bulk_g2s(stages + (size_t)c * p.stage_bytes + (size_t)j * p.K,
+                             p.w8 + (r0 + (int64_t)c * p.rows_per_stage + j) * p.K, (uint32_t)p.K, &full[c]);
+            }
+    } else if (tid == 0) {
+        for (int c = 0; c < nchunks && c < kGvStages; ++c) issue(c);
+    }
+
+    if constexpr (LOGN == 6) {
+        if (p.G == 1) {
+            // ---- rotate + quantize x: the three-pass n = 64 row transform on threads 0..127
+            // (the same operations as the standalone kernel), one token row at a time ----
+            if (tid < 128) {
+                float *wmax = reinterpret_cast<float *>(amax_s);  // 4 slots (one per warp of the 128)
+                auto bar = [] { named_bar_sync(1, 128); };
+                RotArgs ra{};
+                const bool ok = named_bar_and(1, 128, mbar_wait(xfull, 0, p.status, abort_flag));
+                for (int m = 0; m < p.M && ok; ++m) {
+                    const uint8_t *xb = smem + p.xb_off + (size_t)m * p.K * 2;
+                    float2 v[16];
+                    rot64_row<IN_BF16>(ra, xb, xb, 0.0f, T, tid, bar, [] {}, v);
+                    float mx = pairs_amax(v);
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                    if (lane == 0) wmax[warp] = mx;
+                    bar();
+                    const float amax = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+                    const float s = __fdiv_rn(amax, 127.0f);
+                    if (tid == 0) xs_s[m] = s;
+                    uint32_t words[2][4];
+                    quant_codes<16>(v, s, words);
+                    const int r = tid >> 2, jq = tid & 3;
+                    store_codes<OUT_S8, 4>(xq, (int64_t)m * p.K + 128 * r + 16 * jq, words[0]);
+                    store_codes<OUT_S8, 4>(xq, (int64_t)m * p.K + 128 * r + 64 + 16 * jq, words[1]);
+                    bar();  // the tile, the staging row and the amax slots are free for the next token
+                }
+            }
+            __syncthreads();
+            gemv_dot_phase(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks);
+            if (tid == 0 && *(volatile int *)abort_flag) {
+                // A wait gave up: let the copies issued at entry land (bounded) before the CTA leaves.
+                for (int c = 0; c <= min(nchunks, kGvStages); ++c) {
+                    uint64_t *b = c < min(nchunks, kGvStages) ? &full[c] : xfull;
+                    const uint64_t t0 = globaltimer();
+                    while (!mbar_try_wait(b, 0) && globaltimer() - t0 < kWaitLimitNs) {
+                    }
+                }
+            }
+            return;
+        }
+    }
+    // ---- rotate + quantize x (the same core and operation order as rotq_kernel) ----
+    const int row_threads = p.G * TPG;
+    const bool in_row = tid < row_threads;
+    const int g = in_row ? tid / TPG : 0;
+    const int t = in_row ? tid - g * TPG : 0;
+    RotArgs ra{};
+    ra.in0 = p.x;
+    ra.ld_in = p.K;
+    for (int m = 0; m < p.M; ++m) {
+        float2 v[NP];
+        rot_group_core<LOGN, IN_BF16>(ra, m, in_row, g, t, T + (size_t)g * Geo::TILE, v);
+        float mx = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NP; ++j) mx = fmaxf(mx, pair_max_abs(v[j]));
+        constexpr int W = TPG < 32 ? TPG : 32;
+#pragma unroll
+        for (int o = W / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (in_row && (t & (W - 1)) == 0) atomicMax(&amax_s[m], __float_as_uint(mx));
+        __syncthreads();
+        const float s = __fdiv_rn(__uint_as_float(amax_s[m]), 127.0f);
+        if (tid == 0) xs_s[m] = s;
+        if (in_row) {
+            uint32_t words[2][NP / 4];
+            quant_codes<NP>(v, s, words);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) store_codes<OUT_S8, NP / 4>(xq, (int64_t)m * p.K + out_offset<LOGN>(g, t, h),
+                                                                   words[h]);
+        }
+        __syncthreads();
+    }
+
+    gemv_dot_phase(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks);
+}
+
+template <int LOGN>
 int launch_gemv_t(const GemvArgs &base, int num_sms, cudaStream_t st) {
     constexpr int TPG = RotGeom<LOGN>::TPG;
     GemvArgs a = base;
     if (a.G * TPG > kGvThreads) return GBQ_ENOTSUP;
     const size_t x_bytes = (size_t)a.M * a.K;
     const size_t t_bytes = (size_t)a.G * RotGeom<LOGN>::TILE * sizeof(float2);
-    const size_t misc = 2 * kGvMaxM * 4 + kGvStages * 8 + 16;
-    const size_t fixed = ((x_bytes + 127) & ~(size_t)127) + ((t_bytes + 127) & ~(size_t)127) + 128;
+    const size_t misc = 2 * kGvMaxM * 4 + (kGvStages + 2) * 8 + 16;  // scales, amax, barriers, abort, x barrier
+    const size_t xb_bytes = (LOGN == 6 && a.G == 1) ? (size_t)a.M * a.K * 2 + 128 : 0;  // bf16 token staging
+    const size_t fixed = ((x_bytes + 127) & ~(size_t)127) + ((t_bytes + 127) & ~(size_t)127) + 128 + xb_bytes;
     if (fixed + (size_t)kGvStages * a.K > kGvSmem) return GBQ_ENOTSUP;
     int64_t rpc = (a.N + num_sms - 1) / num_sms;
     const int64_t grid = (a.N + rpc - 1) / rpc;
     const int64_t rps_cap = (int64_t)((kGvSmem - fixed) / kGvStages) / a.K;
-    const int64_t rps = rps_cap < rpc ? rps_cap : rpc;
+    // Rows per stage: the whole slice over the ring when it fits (no more shared memory than needed),
+    // else as many as fit.
+    const int64_t rps_fit = (rpc + kGvStages - 1) / kGvStages;
+    const int64_t rps = rps_fit <= rps_cap ? rps_fit : rps_cap;
     a.rows_per_cta = (int)rpc;
     a.rows_per_stage = (int)rps;
     a.stage_bytes = (uint32_t)(((size_t)rps * a.K + 127) & ~(size_t)127);
     a.x_off = (uint32_t)((size_t)kGvStages * a.stage_bytes);
     a.t_off = a.x_off + (uint32_t)((x_bytes + 127) & ~(size_t)127);
     a.misc_off = a.t_off + (uint32_t)((t_bytes + 127) & ~(size_t)127);
-    const size_t smem = a.misc_off + misc;
+    a.xb_off = 0;
+    size_t smem = a.misc_off + misc;
+    if (LOGN == 6 && a.G == 1) {
+        a.xb_off = (uint32_t)((smem + 127) & ~(size_t)127);
+        smem = a.xb_off + (size_t)a.M * a.K * 2;
+    }
     static bool attr = false;
     if (!attr) {
         if (cudaFuncSetAttribute(gemv_kernel<LOGN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGvSmem) !=

@@ -98,10 +98,59 @@ __device__ __forceinline__ void fast_issue(const RotArgs &p, int64_t row, uint8_
 }
 
 // ============================================================== n = 64
+// One row through the three passes: s0 / s1 the row's staged input(s), rs its
+// row scale, T the 64 x kP64 tile.  Threads tau = 0..127 take part and meet at
+// bar() (a CTA barrier or a named barrier over those 128 threads); after_a() runs
+// (on every thread) right after the barrier that ends the reads of the stage.
+// Leaves this thread's pass-C pairs: v[c] = (X[2r][16 jq + c], X[2r + 1][16 jq + c])
+// with r = tau / 4, jq = tau % 4.
+template <int IN, class Bar, class Hook>
+__device__ __forceinline__ void rot64_row(const RotArgs &p, const uint8_t *s0, const uint8_t *s1, float rs,
+                                          float2 *T, int tau, Bar bar, Hook after_a, float2 (&v)[16]) {
+    // ---- pass A: regs i0..i3, pair j0; thread = (j1..j5, i4 i5) ----
+    {
+        const int jh = tau & 31, ih = tau >> 5;
+#pragma unroll
+        for (int a = 0; a < 16; ++a) v[a] = staged_pair<IN>(p, s0, s1, rs, 64 * (a + 16 * ih) + 2 * jh);
+        h4_level<16, 0>(v);
+        h4_level<16, 2>(v);
+#pragma unroll
+        for (int a = 0; a < 16; ++a) T[(a + 16 * ih) * kP64 + jh] = v[a];
+    }
+    bar();
+    after_a();
+    // ---- pass B: regs (i4 i5 | j4 j5), pair j0; thread = (i0..i3, j1 j2 j3); in place ----
+    {
+        const int il = tau & 15, jm = tau >> 4;
+#pragma unroll
+        for (int b = 0; b < 16; ++b) v[b] = T[(il + 16 * (b & 3)) * kP64 + jm + 8 * (b >> 2)];
+        h4_level<16, 0>(v);
+        h4_level<16, 2>(v);
+#pragma unroll
+        for (int b = 0; b < 16; ++b) T[(il + 16 * (b & 3)) * kP64 + jm + 8 * (b >> 2)] = v[b];
+    }
+    bar();
+    // ---- pass C: regs j0..j3, pair i0 (rows 2r, 2r+1); thread = (j4 j5, i1..i5) ----
+    const int r = tau >> 2, jq = tau & 3;
+    // Row 2r starts on a 16-byte boundary (66 r float2); row 2r + 1 (odd pitch) only on 8.
+    const float4 *t0 = reinterpret_cast<const float4 *>(T + (2 * r) * kP64 + 8 * jq);
+    const float2 *t1 = T + (2 * r + 1) * kP64 + 8 * jq;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float4 a0 = t0[k];
+        const float2 b0 = t1[2 * k], b1 = t1[2 * k + 1];
+        v[4 * k + 0] = f2(a0.x, b0.x);
+        v[4 * k + 1] = f2(a0.y, b0.y);
+        v[4 * k + 2] = f2(a0.z, b1.x);
+        v[4 * k + 3] = f2(a0.w, b1.y);
+    }
+    h4_level<16, 0>(v);
+    h4_level<16, 2>(v);
+}
+
 template <int IN, int OUT>
 __global__ void __launch_bounds__(128) rot64_kernel(const __grid_constant__ FastArgs f) {
     const RotArgs &p = f.a;
-    constexpr int NIN = in_count(IN);
     extern __shared__ __align__(128) uint8_t smem[];
     float2 *T = reinterpret_cast<float2 *>(smem + f.tile_off);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + f.misc_off);
@@ -140,54 +189,20 @@ __global__ void __launch_bounds__(128) rot64_kernel(const __grid_constant__ Fast
         float rs = 0.0f;
         if (IN == IN_S8_ROWSCALE || IN == IN_ACC_GLU) rs = __ldg(p.in_scale + row);
 
-        // ---- pass A: regs i0..i3, pair j0; thread = (j1..j5, i4 i5) ----
         float2 v[16];
-        {
-            const int jh = tau & 31, ih = tau >> 5;
-#pragma unroll
-            for (int a = 0; a < 16; ++a) v[a] = staged_pair<IN>(p, s0, s0 + rb, rs, 64 * (a + 16 * ih) + 2 * jh);
-            h4_level<16, 0>(v);
-            h4_level<16, 2>(v);
-#pragma unroll
-            for (int a = 0; a < 16; ++a) T[(a + 16 * ih) * kP64 + jh] = v[a];
-        }
-        __syncthreads();
-        if (tau == 0) {  // every thread has read the stage: stream the row `stages` iterations ahead into it
-            const int64_t r2 = row + (int64_t)f.stages * gridDim.x;
-            if (r2 < p.M) {
-                fast_issue<IN>(p, r2, smem + (size_t)st * f.stage_bytes, &full[st]);
-                pending = it + f.stages;
-            }
-        }
-        // ---- pass B: regs (i4 i5 | j4 j5), pair j0; thread = (i0..i3, j1 j2 j3); in place ----
-        {
-            const int il = tau & 15, jm = tau >> 4;
-#pragma unroll
-            for (int b = 0; b < 16; ++b) v[b] = T[(il + 16 * (b & 3)) * kP64 + jm + 8 * (b >> 2)];
-            h4_level<16, 0>(v);
-            h4_level<16, 2>(v);
-#pragma unroll
-            for (int b = 0; b < 16; ++b) T[(il + 16 * (b & 3)) * kP64 + jm + 8 * (b >> 2)] = v[b];
-        }
-        __syncthreads();
-        // ---- pass C: regs j0..j3, pair i0 (rows 2r, 2r+1); thread = (j4 j5, i1..i5) ----
+        rot64_row<IN>(
+            p, s0, s0 + rb, rs, T, tau, [] { __syncthreads(); },
+            [&] {
+                if (tau == 0) {  // every thread has read the stage: stream the row `stages` iterations ahead into it
+                    const int64_t r2 = row + (int64_t)f.stages * gridDim.x;
+                    if (r2 < p.M) {
+                        fast_issue<IN>(p, r2, smem + (size_t)st * f.stage_bytes, &full[st]);
+                        pending = it + f.stages;
+                    }
+                }
+            },
+            v);
         const int r = tau >> 2, jq = tau & 3;
-        {
-            // Row 2r starts on a 16-byte boundary (66 r float2); row 2r + 1 (odd pitch) only on 8.
-            const float4 *t0 = reinterpret_cast<const float4 *>(T + (2 * r) * kP64 + 8 * jq);
-            const float2 *t1 = T + (2 * r + 1) * kP64 + 8 * jq;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float4 a0 = t0[k];
-                const float2 b0 = t1[2 * k], b1 = t1[2 * k + 1];
-                v[4 * k + 0] = f2(a0.x, b0.x);
-                v[4 * k + 1] = f2(a0.y, b0.y);
-                v[4 * k + 2] = f2(a0.z, b1.x);
-                v[4 * k + 3] = f2(a0.w, b1.y);
-            }
-            h4_level<16, 0>(v);
-            h4_level<16, 2>(v);
-        }
         const int64_t o0 = row * 4096 + (2 * r) * 64 + 16 * jq;  // element offset of row 2r's chunk
         if constexpr (OUT == OUT_BF16) {
             float x0[16], x1[16];

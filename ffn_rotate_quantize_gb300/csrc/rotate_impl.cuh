@@ -327,18 +327,20 @@ __device__ __forceinline__ int64_t out_offset(int g, int t, int h) {
 __device__ __forceinline__ float pair_max_abs(const float2 a) { return fmaxf(fabsf(a.x), fabsf(a.y)); }
 
 // Codes rint(v * r) of a pair array, four int8 per word per half: words[h][w]
-// holds elements 4w..4w+3 of half h.  Returns false if some t = v*r lies within
-// 1e-4 of a half-integer, where the code might differ from rne(fl(v/s)).
+// holds elements 4w..4w+3 of half h.  Returns a bit mask of the words in which
+// some t = v*r lies within 1e-4 of a half-integer, where the code might differ
+// from rne(fl(v/s)).
 template <int NP>
-__device__ __forceinline__ bool quant_codes_fast(const float2 (&v)[NP], float r, uint32_t (&words)[2][NP / 4]) {
+__device__ __forceinline__ uint32_t quant_codes_fast(const float2 (&v)[NP], float r, uint32_t (&words)[2][NP / 4]) {
     const float2 r2 = f2(r, r);
     const float2 magic = f2(12582912.0f, 12582912.0f);  // 1.5 * 2^23: t + magic rounds t to an integer (RNE)
     const float2 nmagic = f2(-12582912.0f, -12582912.0f);
     const float2 mone2 = f2(-1.0f, -1.0f);
-    float dmax = 0.0f;
+    uint32_t bad = 0;
 #pragma unroll
     for (int w = 0; w < NP / 4; ++w) {
         uint32_t mx[4], my[4];
+        float dmax = 0.0f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const float2 tt = __fmul2_rn(v[4 * w + k], r2);
@@ -349,40 +351,42 @@ __device__ __forceinline__ bool quant_codes_fast(const float2 (&v)[NP], float r,
             mx[k] = __float_as_uint(m.x);
             my[k] = __float_as_uint(m.y);
         }
+        if (dmax > 0.4999f) bad |= 1u << w;
         words[0][w] = __byte_perm(__byte_perm(mx[0], mx[1], 0x0040), __byte_perm(mx[2], mx[3], 0x0040), 0x5410);
         words[1][w] = __byte_perm(__byte_perm(my[0], my[1], 0x0040), __byte_perm(my[2], my[3], 0x0040), 0x5410);
     }
-    return dmax <= 0.4999f;
+    return bad;
 }
 
-// The codes clamp(rne(fl(v/s)), +-127) through IEEE division.
+// The codes of word w (elements 4w..4w+3 of both halves): clamp(rne(fl(v/s)), +-127) through IEEE division.
 template <int NP>
-__device__ __forceinline__ void quant_codes_exact(const float2 (&v)[NP], float s, uint32_t (&words)[2][NP / 4]) {
+__device__ __forceinline__ void quant_word_exact(const float2 (&v)[NP], int w, float s, uint32_t &wx, uint32_t &wy) {
+    wx = 0;
+    wy = 0;
 #pragma unroll
-    for (int w = 0; w < NP / 4; ++w) {
-        uint32_t wx = 0, wy = 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            int qx = 0, qy = 0;
-            if (s != 0.0f) {
-                qx = max(-127, min(127, __float2int_rn(__fdiv_rn(v[4 * w + k].x, s))));
-                qy = max(-127, min(127, __float2int_rn(__fdiv_rn(v[4 * w + k].y, s))));
-            }
-            wx |= (uint32_t)(qx & 0xFF) << (8 * k);
-            wy |= (uint32_t)(qy & 0xFF) << (8 * k);
+    for (int k = 0; k < 4; ++k) {
+        int qx = 0, qy = 0;
+        if (s != 0.0f) {
+            qx = max(-127, min(127, __float2int_rn(__fdiv_rn(v[4 * w + k].x, s))));
+            qy = max(-127, min(127, __float2int_rn(__fdiv_rn(v[4 * w + k].y, s))));
         }
-        words[0][w] = wx;
-        words[1][w] = wy;
+        wx |= (uint32_t)(qx & 0xFF) << (8 * k);
+        wy |= (uint32_t)(qy & 0xFF) << (8 * k);
     }
 }
 
-// Quantize a thread's pairs with the row scale s (|v| <= 127 s): reciprocal
-// path unless a tie is near or 1/s is not a safe finite number.
+// Quantize a thread's pairs with the row scale s (|v| <= 127 s): the reciprocal
+// path, then IEEE division for the words it flagged (or for all of them when
+// 1/s is not a safe finite number).
 template <int NP>
 __device__ __forceinline__ void quant_codes(const float2 (&v)[NP], float s, uint32_t (&words)[2][NP / 4]) {
-    bool ok = false;
-    if (s >= 1e-30f) ok = quant_codes_fast<NP>(v, __frcp_rn(s), words);
-    if (!ok) quant_codes_exact<NP>(v, s, words);
+    uint32_t bad = (NP / 4 >= 32) ? 0xFFFFFFFFu : ((1u << (NP / 4)) - 1u);
+    if (s >= 1e-30f) bad = quant_codes_fast<NP>(v, __frcp_rn(s), words);
+    if (bad) {
+#pragma unroll
+        for (int w = 0; w < NP / 4; ++w)
+            if (bad & (1u << w)) quant_word_exact<NP>(v, w, s, words[0][w], words[1][w]);
+    }
 }
 
 // Store the codes of one output half (NW words = 4*NW values) with 16-byte stores.

@@ -120,21 +120,6 @@ cudaError_t launch_rot_fast(RotArgs a, cudaStream_t st) {
     a.row_in_bytes = (uint32_t)row_in;
     f.stage_bytes = (uint32_t)((nin * row_in + 127) / 128 * 128);
     int threads;
-    if constexpr (LOGN == 6) {
-        threads = 128;
-        f.stages = 2;
-        f.tile_off = 2 * f.stage_bytes;
-        f.misc_off = f.tile_off + (fast_tile_bytes(6) + 127) / 128 * 128;
-    } else {
-        threads = 512;
-        f.stages = 1;
-        f.tile_off = 0;  // the tile reuses the stage's memory
-        const uint32_t tb = fast_tile_bytes(7);
-        f.misc_off = (f.stage_bytes > tb ? f.stage_bytes : (tb + 127) / 128 * 128);
-    }
-    f.a = a;
-    const size_t smem = f.misc_off + kFastMisc;
-    if (smem > (size_t)kMaxSmem) return cudaErrorNotSupported;
     auto kern = LOGN == 6 ? rot64_kernel<IN, OUT> : rot128_kernel<IN, OUT>;
     static int regs = -1;  // one per instantiation
     if (regs < 0) {
@@ -145,6 +130,25 @@ cudaError_t launch_rot_fast(RotArgs a, cudaStream_t st) {
         if (e != cudaSuccess) return e;
         regs = fa.numRegs;
     }
+    if constexpr (LOGN == 6) {
+        threads = 128;
+        // Two input stages stream the next row while this one is rotated; when every row fits in
+        // the resident CTAs at once with one stage, one stage (more CTAs per SM) is the faster choice.
+        const uint32_t tile = (fast_tile_bytes(6) + 127) / 128 * 128;
+        const int per_sm1 = resident_ctas(regs, threads, f.stage_bytes + tile + kFastMisc);
+        f.stages = (a.M <= (int64_t)per_sm1 * (a.num_sms > 0 ? a.num_sms : 1)) ? 1 : 2;
+        f.tile_off = f.stages * f.stage_bytes;
+        f.misc_off = f.tile_off + tile;
+    } else {
+        threads = 512;
+        f.stages = 1;
+        f.tile_off = 0;  // the tile reuses the stage's memory
+        const uint32_t tb = fast_tile_bytes(7);
+        f.misc_off = (f.stage_bytes > tb ? f.stage_bytes : (tb + 127) / 128 * 128);
+    }
+    f.a = a;
+    const size_t smem = f.misc_off + kFastMisc;
+    if (smem > (size_t)kMaxSmem) return cudaErrorNotSupported;
     const int per_sm = resident_ctas(regs, threads, smem);
     if (per_sm < 1) return cudaErrorNotSupported;
     const int64_t resident = (int64_t)per_sm * (a.num_sms > 0 ? a.num_sms : 1);
