@@ -43,8 +43,11 @@ __global__ void __launch_bounds__(kIdThreads) quant_identity_kernel(IdArgs p) {
                 v[c][2 * h + 1] = __uint_as_float(ws[h] & 0xFFFF0000u);
             }
             if (p.col_scale) {
+                const float4 c0 = __ldg(reinterpret_cast<const float4 *>(p.col_scale + 8 * ch));
+                const float4 c1 = __ldg(reinterpret_cast<const float4 *>(p.col_scale + 8 * ch + 4));
+                const float cs[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[c][e] = __fmul_rn(v[c][e], __ldg(p.col_scale + 8 * ch + e));
+                for (int e = 0; e < 8; ++e) v[c][e] = __fmul_rn(v[c][e], cs[e]);
             }
 #pragma unroll
             for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(v[c][e]));
@@ -62,15 +65,17 @@ __global__ void __launch_bounds__(kIdThreads) quant_identity_kernel(IdArgs p) {
     for (int w = 0; w < kIdThreads / 32; ++w) amax = fmaxf(amax, s_warp[w]);
     const float s = __fdiv_rn(amax, 127.0f);
     if (tid == 0) p.out_scale[row] = s;
-    // Codes rne(fl(v/s)): reciprocal path (see rotate_impl.cuh) with an exact fallback.
+    // Codes rne(fl(v/s)): the reciprocal path (see rotate_impl.cuh), then IEEE division for
+    // the chunks whose products lie within 1e-4 of a half-integer (or all, for a tiny scale).
     uint32_t words[kIdMaxChunks][2];
-    bool fast = s >= 1e-30f;
-    if (fast) {
+    uint32_t bad = 0xFFFFFFFFu;
+    if (s >= 1e-30f) {
+        bad = 0;
         const float r = __frcp_rn(s);
-        float dmax = 0.0f;
 #pragma unroll
         for (int c = 0; c < kIdMaxChunks; ++c) {
             uint32_t mb[8];
+            float dmax = 0.0f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const float t = __fmul_rn(v[c][e], r);
@@ -78,14 +83,15 @@ __global__ void __launch_bounds__(kIdThreads) quant_identity_kernel(IdArgs p) {
                 dmax = fmaxf(dmax, fabsf(__fsub_rn(t, __fsub_rn(m, 12582912.0f))));
                 mb[e] = __float_as_uint(m);
             }
+            if (dmax > 0.4999f) bad |= 1u << c;
             words[c][0] = __byte_perm(__byte_perm(mb[0], mb[1], 0x0040), __byte_perm(mb[2], mb[3], 0x0040), 0x5410);
             words[c][1] = __byte_perm(__byte_perm(mb[4], mb[5], 0x0040), __byte_perm(mb[6], mb[7], 0x0040), 0x5410);
         }
-        fast = dmax <= 0.4999f;
     }
-    if (!fast) {
+    if (bad) {
 #pragma unroll
         for (int c = 0; c < kIdMaxChunks; ++c) {
+            if (!(bad & (1u << c))) continue;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t w = 0;
