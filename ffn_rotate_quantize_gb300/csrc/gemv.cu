@@ -244,7 +244,8 @@ int launch_gemv_t(const GemvArgs &base, int num_sms, cudaStream_t st) {
     GemvArgs a = base;
     if (a.G * TPG > kGvThreads) return GBQ_ENOTSUP;
     const size_t x_bytes = (size_t)a.M * a.K;
-    const size_t t_bytes = (size_t)a.G * RotGeom<LOGN>::TILE * sizeof(float2);
+    size_t t_bytes = (size_t)a.G * RotGeom<LOGN>::TILE * sizeof(float2);
+    if (LOGN == 6 && a.G == 1 && t_bytes < fast_tile_bytes(6)) t_bytes = fast_tile_bytes(6);  // three-pass tile
     const size_t misc = 2 * kGvMaxM * 4 + (kGvStages + 2) * 8 + 16;  // scales, amax, barriers, abort, x barrier
     const size_t xb_bytes = (LOGN == 6 && a.G == 1) ? (size_t)a.M * a.K * 2 + 128 : 0;  // bf16 token staging
     const size_t fixed = ((x_bytes + 127) & ~(size_t)127) + ((t_bytes + 127) & ~(size_t)127) + 128 + xb_bytes;

@@ -16,13 +16,14 @@ cudaError_t launch_rotb(int logn, int in_kind, RotArgs a, cudaStream_t st) {
 // Per-row quantizer with R = I (the dy side of linear_dx_int8, and identity
 // rotation descriptors).  One CTA of 256 threads per row; each thread keeps its
 // (up to 16) chunks of 8 values in registers across load -> amax -> quantize.
+// Long rows (>= 16384 values) take 512 threads, so each thread holds at most 32
+// values and four CTAs fit an SM: enough loads in flight to stream from HBM.
 // Optional fp32 column scale: v = bf16(dy[m,n]) * s[n] in fp32 (the weight scale
 // moved onto the contraction index, "The backward: dL/dx, weight-only").
 // ---------------------------------------------------------------------------
-constexpr int kIdThreads = 256;
-constexpr int kIdChunkCap = 16;  // K <= 256 * 16 * 8 = 32768
+constexpr int kIdChunkCap = 8;  // K <= 512 * 8 * 8 = 32768
 
-template <int OUT, int kIdMaxChunks>
+template <int OUT, int kIdMaxChunks, int kIdThreads>
 __global__ void __launch_bounds__(kIdThreads) quant_identity_kernel(IdArgs p) {
     __shared__ float s_warp[kIdThreads / 32];
     const int64_t row = blockIdx.x;
@@ -122,25 +123,31 @@ __global__ void __launch_bounds__(kIdThreads) quant_identity_kernel(IdArgs p) {
 }
 
 cudaError_t launch_quant_identity(int out_kind, IdArgs a, cudaStream_t st) {
-    if (a.K % 8 != 0 || a.K / 8 > (int64_t)kIdThreads * kIdChunkCap) return cudaErrorNotSupported;
+    const int threads = (a.K / 8 >= 2048) ? 512 : 256;
+    if (a.K % 8 != 0 || a.K / 8 > (int64_t)threads * kIdChunkCap) return cudaErrorNotSupported;
     if (a.M > 0x7fffffff) return cudaErrorInvalidValue;
     if (out_kind != OUT_S8 && out_kind != OUT_F16Q) return cudaErrorNotSupported;
-    const int64_t chunks = (a.K / 8 + kIdThreads - 1) / kIdThreads;  // per thread
+    const int64_t chunks = (a.K / 8 + threads - 1) / threads;  // per thread
     const unsigned grid = (unsigned)a.M;
     prof_begin(0, st);
-#define GBQ_ID_LAUNCH(CH)                                                                              \
+#define GBQ_ID_LAUNCH(CH, TH)                                                                          \
     do {                                                                                               \
         if (out_kind == OUT_S8)                                                                        \
-            quant_identity_kernel<OUT_S8, CH><<<grid, kIdThreads, 0, st>>>(a);                         \
+            quant_identity_kernel<OUT_S8, CH, TH><<<grid, TH, 0, st>>>(a);                             \
         else                                                                                           \
-            quant_identity_kernel<OUT_F16Q, CH><<<grid, kIdThreads, 0, st>>>(a);                       \
+            quant_identity_kernel<OUT_F16Q, CH, TH><<<grid, TH, 0, st>>>(a);                           \
     } while (0)
-    if (chunks <= 4)
-        GBQ_ID_LAUNCH(4);
-    else if (chunks <= 8)
-        GBQ_ID_LAUNCH(8);
-    else
-        GBQ_ID_LAUNCH(16);
+    if (threads == 512) {
+        if (chunks <= 4)
+            GBQ_ID_LAUNCH(4, 512);
+        else
+            GBQ_ID_LAUNCH(8, 512);
+    } else {
+        if (chunks <= 4)
+            GBQ_ID_LAUNCH(4, 256);
+        else
+            GBQ_ID_LAUNCH(8, 256);
+    }
 #undef GBQ_ID_LAUNCH
     prof_end(st);
     return cudaGetLastError();

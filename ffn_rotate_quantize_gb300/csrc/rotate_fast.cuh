@@ -41,7 +41,10 @@ struct FastArgs {
     int stages;
 };
 
-constexpr int kP64 = 33;    // n = 64 tile row pitch (float2): odd, so 16 rows of 8-byte accesses hit distinct banks
+// n = 64 tile: row pitch 35 float2, and one pad float2 after the first 16 of a row (column jh is stored
+// at jh + jh / 16), which makes every 8-byte access of the three passes free of bank conflicts.
+constexpr int kP64 = 35;
+__device__ __forceinline__ int t64(int i, int jh) { return i * kP64 + jh + (jh >> 4); }
 constexpr int kP128A = 129;  // n = 128 tile pitch for passes A/B (float2, pairs over i6)
 constexpr int kP128C = 66;   // n = 128 tile pitch for pass C (float2, pairs over j6)
 constexpr uint32_t kFastMisc = 256;
@@ -115,7 +118,7 @@ __device__ __forceinline__ void rot64_row(const RotArgs &p, const uint8_t *s0, c
         h4_level<16, 0>(v);
         h4_level<16, 2>(v);
 #pragma unroll
-        for (int a = 0; a < 16; ++a) T[(a + 16 * ih) * kP64 + jh] = v[a];
+        for (int a = 0; a < 16; ++a) T[t64(a + 16 * ih, jh)] = v[a];
     }
     bar();
     after_a();
@@ -123,26 +126,23 @@ __device__ __forceinline__ void rot64_row(const RotArgs &p, const uint8_t *s0, c
     {
         const int il = tau & 15, jm = tau >> 4;
 #pragma unroll
-        for (int b = 0; b < 16; ++b) v[b] = T[(il + 16 * (b & 3)) * kP64 + jm + 8 * (b >> 2)];
+        for (int b = 0; b < 16; ++b) v[b] = T[t64(il + 16 * (b & 3), jm + 8 * (b >> 2))];
         h4_level<16, 0>(v);
         h4_level<16, 2>(v);
 #pragma unroll
-        for (int b = 0; b < 16; ++b) T[(il + 16 * (b & 3)) * kP64 + jm + 8 * (b >> 2)] = v[b];
+        for (int b = 0; b < 16; ++b) T[t64(il + 16 * (b & 3), jm + 8 * (b >> 2))] = v[b];
     }
     bar();
     // ---- pass C: regs j0..j3, pair i0 (rows 2r, 2r+1); thread = (j4 j5, i1..i5) ----
     const int r = tau >> 2, jq = tau & 3;
-    // Row 2r starts on a 16-byte boundary (66 r float2); row 2r + 1 (odd pitch) only on 8.
-    const float4 *t0 = reinterpret_cast<const float4 *>(T + (2 * r) * kP64 + 8 * jq);
-    const float2 *t1 = T + (2 * r + 1) * kP64 + 8 * jq;
+    // Slots 8 jq .. 8 jq + 7 of rows 2r and 2r + 1 (all on one side of the pad: 8 jq / 16 = jq / 2).
+    const float2 *t0 = T + t64(2 * r, 8 * jq);
+    const float2 *t1 = T + t64(2 * r + 1, 8 * jq);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const float4 a0 = t0[k];
-        const float2 b0 = t1[2 * k], b1 = t1[2 * k + 1];
-        v[4 * k + 0] = f2(a0.x, b0.x);
-        v[4 * k + 1] = f2(a0.y, b0.y);
-        v[4 * k + 2] = f2(a0.z, b1.x);
-        v[4 * k + 3] = f2(a0.w, b1.y);
+    for (int m = 0; m < 8; ++m) {
+        const float2 a0 = t0[m], b0 = t1[m];
+        v[2 * m] = f2(a0.x, b0.x);
+        v[2 * m + 1] = f2(a0.y, b0.y);
     }
     h4_level<16, 0>(v);
     h4_level<16, 2>(v);
