@@ -322,7 +322,16 @@ def run_ours(args):
                              "exactly on the f16 pipe"}
         e2e = measure_e2e(G, torch, dev, x3, w83, s3, b3, ws_lin, args)
     if "decode_gemv" in opfn:
-        gv_ms = kernel_ms(G, torch, flush, G.K_GEMV, opfn["decode_gemv"], reps=32)  # 16 weight copies, 268 MB
+        # gbq_linear at M = 1 is one gemv_kernel launch: time 32 back-to-back launches (16 weight copies,
+        # 268 MB) with one event pair, after checking that each call is exactly one GEMV launch.
+        G.prof_enable(True)
+        opfn["decode_gemv"](0)
+        torch.cuda.synchronize()
+        n_gv, _ = G.prof_read(G.K_GEMV)
+        n_other = sum(G.prof_read(k)[0] for k in (G.K_ROTATE, G.K_I8GEMM, G.K_BF16GEMM, G.K_ELEMWISE))
+        G.prof_enable(False)
+        assert n_gv == 1 and n_other == 0, "the decode call is not a single GEMV launch"
+        gv_ms = batch_ms(torch, flush, opfn["decode_gemv"], reps=32)
         ach = DECODE_BYTES / (gv_ms * 1e-3) * 1e-9
         dec = {"bound": "hbm", "kernel": "gemv_kernel (decode 1x4096x4096)", "achieved": round(ach, 1),
                "peak": peaks["hbm"], "unit": "GB/s", "frac": round(ach / peaks["hbm"], 4), "ms": round(gv_ms, 4),
@@ -348,6 +357,24 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def batch_ms(torch, flush, fn, reps=32):
+    """Average duration of fn(i) launched reps times back to back on the current stream, one CUDA
+    event pair around the batch (for single-kernel ops, whose per-launch events would add gaps).
+    fn(i) must cycle through inputs whose total exceeds the L2 cache."""
+    fn(0)
+    torch.cuda.synchronize()
+    flush.zero_()
+    st = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for i in range(reps):
+        fn(i)
+    e1.record(st)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
 
 
 def kernel_ms(G, torch, flush, kind, fn, reps=10):

@@ -238,6 +238,150 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(GemvArgs p) {
     gemv_dot_phase(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks);
 }
 
+// ---------------------------------------------------------------------------
+// Register-streaming variant for K = 4096, n = 64, one group, and at most 32
+// weight rows per CTA (4 per warp): every thread issues the loads of its share
+// of the CTA's weight slice at entry, straight into registers (streaming loads,
+// no shared-memory ring), so the whole slice is in flight while threads 0..127
+// rotate and quantize x; the dot products then read the weight from registers.
+constexpr int kDxK = 4096;
+constexpr int kDxChunks = kDxK / 16 / 32;  // 16-byte chunks per lane per row
+
+template <int RPW>
+__global__ void __launch_bounds__(kGvThreads, 1) gemv_direct_kernel(GemvArgs p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    int8_t *xq = reinterpret_cast<int8_t *>(smem + p.x_off);
+    float2 *T = reinterpret_cast<float2 *>(smem + p.t_off);
+    float *xs_s = reinterpret_cast<float *>(smem + p.misc_off);
+    float *wmax = xs_s + kGvMaxM;
+    uint64_t *xfull = reinterpret_cast<uint64_t *>(wmax + kGvMaxM);
+    int *abort_flag = reinterpret_cast<int *>(xfull + 1);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int64_t r0 = (int64_t)blockIdx.x * p.rows_per_cta;
+    const int nrows = (int)(min(p.N, r0 + p.rows_per_cta) - r0);
+
+    if (tid == 0) {
+        mbar_init(xfull, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        mbar_arrive_expect_tx(xfull, (uint32_t)(p.M * kDxK * 2));
+        bulk_g2s(smem + p.xb_off, p.x, (uint32_t)(p.M * kDxK * 2), xfull);
+    }
+    // This warp's rows j = warp + 8 q of the slice: issue every load now (they land while x is rotated).
+    uint4 wv[RPW][kDxChunks];
+#pragma unroll
+    for (int q = 0; q < RPW; ++q) {
+        const int j = warp + 8 * q;
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.w8 + (r0 + (j < nrows ? j : 0)) * kDxK);
+#pragma unroll
+        for (int k = 0; k < kDxChunks; ++k) wv[q][k] = j < nrows ? __ldcs(src + lane + 32 * k) : make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();  // the x barrier is initialised
+
+    // ---- rotate + quantize x: the three-pass n = 64 row transform on threads 0..127 ----
+    if (tid < 128) {
+        auto bar = [] { named_bar_sync(1, 128); };
+        RotArgs ra{};
+        const bool ok = named_bar_and(1, 128, mbar_wait(xfull, 0, p.status, abort_flag));
+        for (int m = 0; m < p.M && ok; ++m) {
+            const uint8_t *xb = smem + p.xb_off + (size_t)m * kDxK * 2;
+            float2 v[16];
+            rot64_row<IN_BF16>(ra, xb, xb, 0.0f, T, tid, bar, [] {}, v);
+            float mx = pairs_amax(v);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            if (lane == 0) wmax[warp] = mx;
+            bar();
+            const float amax = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
+            const float s = __fdiv_rn(amax, 127.0f);
+            if (tid == 0) xs_s[m] = s;
+            uint32_t words[2][4];
+            quant_codes<16>(v, s, words);
+            const int r = tid >> 2, jq = tid & 3;
+            store_codes<OUT_S8, 4>(xq, (int64_t)m * kDxK + 128 * r + 16 * jq, words[0]);
+            store_codes<OUT_S8, 4>(xq, (int64_t)m * kDxK + 128 * r + 64 + 16 * jq, words[1]);
+            bar();  // the tile and the amax slots are free for the next token
+        }
+        if (!ok && tid == 0) {  // the x copy never landed: let it finish (bounded) before leaving
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(xfull, 0) && globaltimer() - t0 < kWaitLimitNs) {
+            }
+        }
+    }
+    __syncthreads();
+    if (*(volatile int *)abort_flag) return;
+
+    // ---- dot products from registers, dequant epilogue ----
+#pragma unroll
+    for (int q = 0; q < RPW; ++q) {
+        const int j = warp + 8 * q;
+        if (j >= nrows) break;
+        int acc[kGvMaxM] = {0, 0, 0, 0};
+#pragma unroll
+        for (int k = 0; k < kDxChunks; ++k) {
+            const uint4 w = wv[q][k];
+#pragma unroll
+            for (int m = 0; m < kGvMaxM; ++m) {
+                if (m < p.M) {
+                    const uint4 xv = reinterpret_cast<const uint4 *>(xq + (int64_t)m * kDxK)[lane + 32 * k];
+                    acc[m] = __dp4a((int)w.x, (int)xv.x, acc[m]);
+                    acc[m] = __dp4a((int)w.y, (int)xv.y, acc[m]);
+                    acc[m] = __dp4a((int)w.z, (int)xv.z, acc[m]);
+                    acc[m] = __dp4a((int)w.w, (int)xv.w, acc[m]);
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < kGvMaxM; ++m) {
+            if (m < p.M) {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], o);
+            }
+        }
+        const int64_t n = r0 + j;
+        if (lane < p.M) {
+            int a = acc[0];
+#pragma unroll
+            for (int m = 1; m < kGvMaxM; ++m)
+                if (lane == m) a = acc[m];
+            const float b = p.bias ? __bfloat162float(p.bias[n]) : 0.0f;
+            const float tv = __fmul_rn(__int2float_rn(a), xs_s[lane]);
+            p.y[(int64_t)lane * p.N + n] = __float2bfloat16_rn(__fmaf_rn(tv, __ldg(p.ws + n), b));
+        }
+    }
+}
+
+// Launch the register-streaming kernel when the shape fits it; GBQ_ENOTSUP otherwise.
+int launch_gemv_direct(const GemvArgs &base, int num_sms, cudaStream_t st) {
+    GemvArgs a = base;
+    if (a.K != kDxK || a.G != 1) return GBQ_ENOTSUP;
+    const int64_t rpc = (a.N + num_sms - 1) / num_sms;
+    if (rpc > 32) return GBQ_ENOTSUP;
+    const int rpw = (int)((rpc + 7) / 8);
+    a.rows_per_cta = (int)rpc;
+    const int64_t grid = (a.N + rpc - 1) / rpc;
+    a.x_off = 0;
+    a.t_off = (uint32_t)(((size_t)a.M * kDxK + 127) & ~(size_t)127);
+    a.misc_off = a.t_off + ((fast_tile_bytes(6) + 127) & ~127u);
+    a.xb_off = a.misc_off + 128;
+    const size_t smem = a.xb_off + (size_t)a.M * kDxK * 2;
+    static bool attr[5] = {false, false, false, false, false};
+    auto kern = rpw == 1 ? gemv_direct_kernel<1> : rpw == 2 ? gemv_direct_kernel<2>
+              : rpw == 3 ? gemv_direct_kernel<3> : gemv_direct_kernel<4>;
+    if (!attr[rpw]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGvSmem) != cudaSuccess)
+            return gbq_fail(GBQ_ECUDA, "gemv: cannot set shared memory size");
+        attr[rpw] = true;
+    }
+    prof_begin(3, st);
+    kern<<<(unsigned)grid, kGvThreads, smem, st>>>(a);
+    prof_end(st);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? GBQ_OK : gbq_fail(GBQ_ECUDA, cudaGetErrorString(e));
+}
+
 template <int LOGN>
 int launch_gemv_t(const GemvArgs &base, int num_sms, cudaStream_t st) {
     constexpr int TPG = RotGeom<LOGN>::TPG;
@@ -302,7 +446,10 @@ int launch_gemv(const void *x, const int8_t *w8, const float *w_scale, const voi
     switch (logn) {
         case 4: return launch_gemv_t<4>(a, num_sms, st);
         case 5: return launch_gemv_t<5>(a, num_sms, st);
-        case 6: return launch_gemv_t<6>(a, num_sms, st);
+        case 6: {
+            const int rc = launch_gemv_direct(a, num_sms, st);
+            return rc == GBQ_ENOTSUP ? launch_gemv_t<6>(a, num_sms, st) : rc;
+        }
         default: return GBQ_ENOTSUP;
     }
 }
