@@ -270,7 +270,7 @@ int gbq_prof_read(int kind, int *launches, double *total_ms) {
 }
 
 size_t gbq_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t H) {
-    return gemm_workspace_size(op, M, N, K, H);
+    return gemm_workspace_size_pref(op, M, N, K, H);
 }
 
 int gbq_quantize_act(const void *x, int8_t *q, float *x_scale, int64_t M, int64_t K, gbq_rot rot, void *stream) {
@@ -441,12 +441,13 @@ int check_ws(const char *what, int op, void *workspace, size_t ws_bytes, int64_t
 
 // Quantize x into the f16-coded GEMM operand.
 int quantize_f16q(const char *what, const void *x, int64_t ld, void *qf16, float *xs, int64_t M, int64_t K,
-                  gbq_rot rot, int logn, cudaStream_t st) {
+                  gbq_rot rot, int logn, cudaStream_t st, int32_t *l1 = nullptr) {
     RotArgs a{};
     a.in0 = x;
     a.ld_in = ld;
     a.out = qf16;
     a.out_scale = xs;
+    a.out_l1 = l1;
     a.M = M;
     a.K = K;
     return run_rotq(what, rot, logn, IN_BF16, OUT_F16Q, a, st);
@@ -518,9 +519,13 @@ int gbq_linear_acc(const void *x, const int8_t *w8, int32_t *acc, int64_t ld_acc
     cudaStream_t st = (cudaStream_t)stream;
     Ws w{(uint8_t *)workspace, ws_bytes};
     void *qf = w.take((size_t)M * K * 2);
-    rc = quantize_f16q("gbq_linear_acc", x, K, qf, x_scale, M, K, rot, logn, st);
+    (void)w.take((size_t)M * 4);                      // (gbq_linear's x_scale slot)
+    int32_t *l1 = (int32_t *)w.take((size_t)M * 4 * ((K + 1023) / 1024));  // block L1 norms: preferred size only
+    if (!rotq_writes_l1(logn, rot.groups)) l1 = nullptr;
+    rc = quantize_f16q("gbq_linear_acc", x, K, qf, x_scale, M, K, rot, logn, st, l1);
     if (rc) return rc;
     I8GemmProblem g = gemm_problem(d, qf, w8, M, N, K, EPI_ACC_I32, acc, ld_acc, nullptr, nullptr, nullptr);
+    g.row_l1 = l1;
     return launch_i8gemm(g, st);
 }
 
@@ -558,9 +563,12 @@ int gbq_linear(const void *x, const int8_t *w8, const float *w_scale, const void
     Ws w{(uint8_t *)workspace, ws_bytes};
     void *qf = w.take((size_t)M * K * 2);
     float *xs = (float *)w.take((size_t)M * 4);
-    rc = quantize_f16q("gbq_linear", x, K, qf, xs, M, K, rot, logn, st);
+    int32_t *l1 = (int32_t *)w.take((size_t)M * 4 * ((K + 1023) / 1024));  // block L1 norms: preferred size only
+    if (!rotq_writes_l1(logn, rot.groups)) l1 = nullptr;
+    rc = quantize_f16q("gbq_linear", x, K, qf, xs, M, K, rot, logn, st, l1);
     if (rc) return rc;
     I8GemmProblem g = gemm_problem(d, qf, w8, M, N, K, EPI_DEQUANT_BF16, y, N, xs, w_scale, bias);
+    g.row_l1 = l1;
     return launch_i8gemm(g, st);
 }
 
@@ -591,8 +599,12 @@ int gbq_ffn_fused(const void *x, const int8_t *wg8, const float *s_gate, const i
     void *gu = w.take((size_t)M * 2 * H * 2);
     void *qh = w.take((size_t)M * H * 2);
     float *hs = (float *)w.take((size_t)M * 4);
+    int32_t *l1x = (int32_t *)w.take((size_t)M * 4 * ((d + 1023) / 1024));  // block L1 norms: preferred size only
+    int32_t *l1h = (int32_t *)w.take((size_t)M * 4 * ((H + 1023) / 1024));
+    if (!rotq_writes_l1(logd, rot_d.groups)) l1x = nullptr;
+    if (!rotq_writes_l1(logh, rot_h.groups)) l1h = nullptr;
     // 1) rotate + quantize x over d
-    rc = quantize_f16q("gbq_ffn_fused (x)", x, d, qx, xs, M, d, rot_d, logd, st);
+    rc = quantize_f16q("gbq_ffn_fused (x)", x, d, qx, xs, M, d, rot_d, logd, st, l1x);
     if (rc) return rc;
     // 2) gate and up GEMMs in one launch over the virtual weight [W_gate; W_up],
     //    dequantized to bf16 g | u (row stride 2H)
@@ -602,6 +614,7 @@ int gbq_ffn_fused(const void *x, const int8_t *wg8, const float *s_gate, const i
     g.w_rows_total1 = H;
     g.n_split = H;
     g.w_scale1 = s_up;
+    g.row_l1 = l1x;
     rc = launch_i8gemm(g, st);
     if (rc) return rc;
     // 3) h = silu(g) * u, rotate over H, quantize
@@ -611,12 +624,14 @@ int gbq_ffn_fused(const void *x, const int8_t *wg8, const float *s_gate, const i
     a.ld_in = 2 * H;
     a.out = qh;
     a.out_scale = hs;
+    a.out_l1 = l1h;
     a.M = M;
     a.K = H;
     rc = run_rotq("gbq_ffn_fused (h)", rot_h, logh, IN_GLU_BF16, OUT_F16Q, a, st);
     if (rc) return rc;
     // 4) down GEMM + dequant
     I8GemmProblem gd = gemm_problem(dv, qh, wd8, M, d, H, EPI_DEQUANT_BF16, y, d, hs, s_down, nullptr);
+    gd.row_l1 = l1h;
     return launch_i8gemm(gd, st);
 }
 

@@ -40,6 +40,7 @@ struct I8GemmProblem {
     const void *bias;         // bf16 [N] or nullptr (EPI_DEQUANT_BF16)
     unsigned int *status;
     int num_sms;
+    const int32_t *row_l1;    // optional [M][K/1024]: sum of |q| over each 1024-long block of a token row
 };
 
 // Enqueue the exact int8 GEMM (tcgen05, fp16-coded operands, chunked fp32 -> int32).
@@ -60,7 +61,8 @@ cudaError_t launch_dequant(const int32_t *acc, int64_t ld_acc, const float *xs, 
 cudaError_t launch_s8_to_f16(const int8_t *q, void *out, int64_t n, cudaStream_t st);
 cudaError_t launch_scale_rows_s8(const int8_t *w8, const float *s, void *w, int64_t N, int64_t K, cudaStream_t st);
 
-size_t gemm_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t H);
+size_t gemm_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t H);       // minimum
+size_t gemm_workspace_size_pref(int op, int64_t M, int64_t N, int64_t K, int64_t H);  // what gbq_workspace_size reports
 
 // Launch timing hooks (abi.cu): bracket one kernel launch on stream st.
 void prof_begin(int kind, cudaStream_t st);

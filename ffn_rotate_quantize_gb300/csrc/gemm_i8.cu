@@ -63,6 +63,8 @@ constexpr uint32_t kColA = 0, kColAcc = 256;
 constexpr int kProducers = 2;  // warps 0 and 2
 constexpr int kThreads = 512;
 constexpr int kEpiWarps = 8;
+constexpr int kPlanTiles = 64;      // token tiles with a chunk plan (M <= 16384); beyond, 1024-long chunks
+constexpr int kPlanMaxBlocks = 16;  // 1024-long K blocks per row the plan looks at (K <= 16384)
 constexpr int kRegsWG0 = 48, kRegsConv = 88, kRegsEpi = 184;
 static_assert(128 * (kRegsWG0 + kRegsConv + 2 * kRegsEpi) <= 65536, "register split exceeds the launch total");
 static_assert(kStages % kProducers == 0, "each producer owns whole stages");
@@ -97,6 +99,7 @@ struct Params {
     const float *w_scale0;
     const float *w_scale1;
     const __nv_bfloat16 *bias;
+    const int32_t *row_l1;  // optional [M][K/1024]: sum of |q| over each 1024-long block of a token row
     unsigned int *status;
     int w_layout;
     int epi;
@@ -111,9 +114,13 @@ struct Bars {
     uint64_t accfull;           // both: chunk accumulated (multicast commit)
     uint64_t accempty;          // CTA 0 only: epilogue warps of both CTAs drained the accumulator
     uint64_t drain;             // CTA 0 only: every MMA finished
+    uint64_t plan_ready;        // CTA 0 only: the epilogue warps published the chunk plan
+    uint32_t plan[kPlanTiles];  // per token tile: bit j set = chunks of 2^j K blocks are exact for every token
     uint32_t tmem_base;
     int abort;
 };
+
+static_assert(sizeof(Bars) <= 1024, "barriers exceed their shared-memory slot");
 
 // Pair tile t: weight rows [n0, n0 + 256), tokens [m0, m0 + 256).
 __device__ __forceinline__ void tile_coords(int64_t t, int64_t m_tiles, int64_t *n0, int64_t *m0) {
@@ -131,6 +138,16 @@ __device__ __forceinline__ void s8x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t
     __half2 h1 = __hsub2(*reinterpret_cast<const __half2 *>(&p1), off);
     lo = *reinterpret_cast<uint32_t *>(&h0);
     hi = *reinterpret_cast<uint32_t *>(&h1);
+}
+
+// Sub-steps per exact chunk of token tile mt from its plan bits (longest level j whose bit is set;
+// bits are only ever set for a prefix of levels).  Without a plan: 1024-long chunks.
+__device__ __forceinline__ int tile_chunk_subs(const uint32_t *plan, const Params &p, int64_t mt, int tile_subs) {
+    if (!p.row_l1 || p.K % 1024 != 0 || p.K / 1024 > kPlanMaxBlocks || mt >= kPlanTiles) return kChunkSubs;
+    const uint32_t bits = plan[mt];
+    const int j = 31 - __clz(bits);  // bit 0 is always set
+    const int c = kChunkSubs << j;
+    return c < tile_subs ? c : tile_subs;
 }
 
 // Add 32 exact integer-valued fp32 partial sums to int32 totals.  When every
@@ -216,7 +233,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) i8gemm_
     const int64_t num_tiles = m_tiles * n_tiles;
     const int KT = (int)((p.K + kBK - 1) / kBK);  // stages per tile (the K tail reads zeros)
     const int tile_subs = KT * kSubs;
-    const int nchunks = (tile_subs + kChunkSubs - 1) / kChunkSubs;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -230,6 +246,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) i8gemm_
         mbar_init(&bars->accfull, 1);
         mbar_init(&bars->accempty, 2 * kEpiWarps);
         mbar_init(&bars->drain, 1);
+        mbar_init(&bars->plan_ready, 1);
+        for (int i = 0; i < kPlanTiles; ++i) bars->plan[i] = ~0u;
         bars->abort = 0;
         fence_mbar_init();
         tma_prefetch_desc(&p.tm_b);
@@ -287,8 +305,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) i8gemm_
             if (lane == 0) {
                 constexpr uint32_t idesc = idesc_f16(kPairM, kBN, 0, 0, 0);
                 uint32_t gs = 0, gsub = 0, chunk = 0;
-                bool ok = true;
+                bool ok = mbar_wait_cluster(&bars->plan_ready, 0, p.status, abort, peer_abort);
                 for (int64_t t = pair; t < num_tiles && ok; t += npairs) {
+                    const int csubs = tile_chunk_subs(bars->plan, p, t % m_tiles, tile_subs);
+                    int cpos = 0;  // sub-step within the current chunk (kept incrementally: no division here)
                     for (int kt = 0; kt < KT && ok; ++kt) {
                         const uint32_t my = gs++;
                         const int stage = (int)(my % kStages);
@@ -297,7 +317,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) i8gemm_
                         for (int sub = 0; sub < kSubs && ok; ++sub) {
                             const uint32_t ms = gsub++;
                             const int tsub = kt * kSubs + sub;  // sub-step within the tile
-                            const int cpos = tsub % kChunkSubs;
                             if (cpos == 0) {  // a new chunk: both CTAs' accumulators must have been drained
                                 ok = mbar_wait_cluster(&bars->accempty, (chunk & 1u) ^ 1u, p.status, abort,
                                                        peer_abort);
@@ -316,9 +335,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) i8gemm_
                                                 (cpos > 0 || k16 > 0) ? 1u : 0u);
                             }
                             tc_commit_pair(&bars->aempty[as], 3);
-                            if (cpos == kChunkSubs - 1 || tsub == tile_subs - 1) {
+                            if (cpos == csubs - 1 || tsub == tile_subs - 1) {
                                 tc_commit_pair(&bars->accfull, 3);
                                 ++chunk;
+                                cpos = 0;
+                            } else {
+                                ++cpos;
                             }
                         }
                         tc_commit_pair(&bars->empty[stage], 3);
@@ -390,6 +412,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) i8gemm_
         }
     } else {
         setmaxnreg_inc<kRegsEpi>();
+        // ------------------------------------------------ chunk plan (epilogue warps, once)
+        // Every partial sum of token m's products with int8 weights (|w| <= 128) over a set of K
+        // indices is bounded by 128 * sum |q[m][k]| over that set.  A chunk of 2^j aligned 1024-long
+        // blocks is therefore exact in fp32 when that bound stays within 2^24 -- block sums of at most
+        // 2^17 -- for every token of the tile.  Level 0 (one block) holds for any int8 data; a tile
+        // takes its longest level that holds.  Each epilogue thread checks whole token rows and ANDs
+        // its verdict into the tile's bits.
+        const int nb = (int)(p.K / 1024);
+        const bool have_plan = p.row_l1 && p.K % 1024 == 0 && nb <= kPlanMaxBlocks;
+        int plan_levels = 0;  // largest j with 2^j <= nb
+        while ((2 << plan_levels) <= nb) ++plan_levels;
+        if (have_plan) {
+            const int et = (warp - 8) * 32 + lane;  // 0 .. 255
+            const int64_t mmax = min(p.M, (int64_t)kPlanTiles * kBN);
+            for (int64_t m = et; m < mmax; m += 32 * kEpiWarps) {
+                int s16[kPlanMaxBlocks];
+#pragma unroll
+                for (int b2 = 0; b2 < kPlanMaxBlocks; ++b2) s16[b2] = b2 < nb ? __ldg(p.row_l1 + m * nb + b2) : 0;
+                uint32_t okb = 1u;  // level 0 always holds
+#pragma unroll
+                for (int j = 1, w = kPlanMaxBlocks / 2; w >= 1; ++j, w >>= 1) {
+                    int mx = 0;
+#pragma unroll
+                    for (int i = 0; i < w; ++i) {
+                        s16[i] = s16[2 * i] + s16[2 * i + 1];  // sums of aligned groups of 2^j blocks
+                        mx = max(mx, s16[i]);
+                    }
+                    if (mx <= (1 << 17)) okb |= 1u << j;
+                }
+                // bit j for j <= plan_levels only if every level below also holds (longer chunks are unions)
+                uint32_t pref = 0;
+                for (int j = 0; j <= plan_levels && ((okb >> j) & 1u); ++j) pref |= 1u << j;
+                atomicAnd(&bars->plan[m / kBN], pref);
+            }
+        }
+        named_bar_sync(1, 32 * kEpiWarps);  // every epilogue thread's verdicts are in
+        if (warp == 8 && lane == 0) mbar_arrive(&bars->plan_ready);  // publish the plan to the MMA issuer
         // ------------------------------------------------ epilogue: drain chunks, write outputs
         const int q = warp & 3;
         const int h = (warp >> 2) & 1;  // token half of the tile
@@ -418,6 +477,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) i8gemm_
             int32_t tot[128];  // exact running sums for this thread's 128 token columns
 #pragma unroll
             for (int i = 0; i < 128; ++i) tot[i] = 0;
+            const int csubs = tile_chunk_subs(bars->plan, p, t % m_tiles, tile_subs);
+            const int nchunks = (tile_subs + csubs - 1) / csubs;
             for (int c = 0; c < nchunks; ++c) {
                 ok = mbar_wait_cluster(&bars->accfull, chunk & 1u, p.status, abort, peer_abort);
                 if (!ok) break;
@@ -545,6 +606,7 @@ int launch_i8gemm(const I8GemmProblem &q, cudaStream_t st) {
     p.w_scale0 = q.w_scale0;
     p.w_scale1 = q.w_scale1;
     p.bias = reinterpret_cast<const __nv_bfloat16 *>(q.bias);
+    p.row_l1 = q.row_l1;
     p.status = q.status;
     p.w_layout = q.w_layout;
     p.epi = q.epi;

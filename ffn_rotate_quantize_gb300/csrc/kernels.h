@@ -27,6 +27,10 @@ cudaError_t launch_rotq(int logn, int in_kind, int out_kind, RotArgs a, cudaStre
 cudaError_t launch_rotb(int logn, int in_kind, RotArgs a, cudaStream_t st);                 // OUT_BF16
 cudaError_t launch_quant_identity(int out_kind, IdArgs a, cudaStream_t st);
 
+// Whether the rotate+quantize launch for this rotation fills RotArgs::out_l1 (the three-pass
+// kernels: n = 64 or 128, one group per row); elsewhere out_l1 is left untouched.
+inline bool rotq_writes_l1(int logn, int groups) { return (logn == 6 || logn == 7) && groups == 1; }
+
 // Threads of one rotq launch row (G groups of n/CPT threads).
 inline int rotq_row_threads(int logn, int G) {
     const int n = 1 << logn;

@@ -130,6 +130,23 @@ cudaError_t launch_scale_rows_s8(const int8_t *w8, const float *s, void *w, int6
 //   LINEAR / INT8_GEMM : q f16 [M][K], x_scale f32 [M]
 //   FFN                : qx f16 [M][d], x_scale [M], g|u bf16 [M][2H], qh f16 [M][H], h_scale [M]
 //   LINEAR_DX_INT8     : qd f16 [M][N], t f32 [M], dx_rot f32 [M][K]
+// Preferred size: the minimum plus, for each quantized GEMM operand, the sums of |code| over each
+// 1024-long block of every token row (int32 [M][ceil(K/1024)]), which let the int8 GEMM accumulate
+// longer exact chunks when they are small.
+size_t gemm_workspace_size_pref(int op, int64_t M, int64_t N, int64_t K, int64_t H) {
+    const size_t base = gemm_workspace_size(op, M, N, K, H);
+    if (M < 0 || base == 0) return base;
+    const auto blocks = [](int64_t k) { return (size_t)((k + 1023) / 1024); };
+    switch (op) {
+        case GBQ_OP_LINEAR:
+            return base + align256((size_t)M * 4 * blocks(K));
+        case GBQ_OP_FFN:
+            return base + align256((size_t)M * 4 * blocks(K)) + align256((size_t)M * 4 * blocks(H));
+        default:
+            return base;
+    }
+}
+
 size_t gemm_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t H) {
     if (M < 0 || N < 0 || K < 0 || H < 0) return 0;
     switch (op) {

@@ -71,6 +71,25 @@ __device__ __forceinline__ void store_chunk_bf16(void *out, int64_t off, const f
     dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
+// Sum of |code| over a thread's 32 int8 codes (8 words of four).
+__device__ __forceinline__ int codes_l1(const uint32_t (&w)[2][4]) {
+    unsigned acc = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc = __dp4a(__vabsss4(w[h][k]), 0x01010101u, acc);
+    return (int)acc;
+}
+
+// Per-warp totals of a per-thread value, stored by lane 0 of each warp at dst[warp].  In pass C
+// of both three-pass kernels warp w holds exactly elements [1024 w, 1024 w + 1024) of the row,
+// so these are the row's per-1024-block sums.
+__device__ __forceinline__ void warp_sums_store(int v, int32_t *dst) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((threadIdx.x & 31) == 0) dst[threadIdx.x >> 5] = v;
+}
+
 // Row scale from the per-warp maxima (NW warps) after a CTA barrier.
 __device__ __forceinline__ float block_amax(float m, float *wmax, int nwarps) {
 #pragma unroll
@@ -221,6 +240,7 @@ __global__ void __launch_bounds__(128) rot64_kernel(const __grid_constant__ Fast
             quant_codes<16>(v, s, words);
             store_chunk_codes<OUT>(p.out, o0, words[0]);
             store_chunk_codes<OUT>(p.out, o0 + 64, words[1]);
+            if (p.out_l1) warp_sums_store(codes_l1(words), p.out_l1 + row * 4);  // K = 4096: 4 blocks
         }
     }
     if (tau == 0 && failed) {
@@ -341,6 +361,7 @@ __global__ void __launch_bounds__(512, 2) rot128_kernel(const __grid_constant__ 
             quant_codes<16>(v, s, words);
             store_chunk_codes<OUT>(p.out, o0, words[0]);
             store_chunk_codes<OUT>(p.out, o0 + 64, words[1]);
+            if (p.out_l1) warp_sums_store(codes_l1(words), p.out_l1 + row * 16);  // K = 16384: 16 blocks
         }
     }
     if (tau == 0 && failed) {

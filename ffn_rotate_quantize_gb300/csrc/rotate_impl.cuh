@@ -48,6 +48,8 @@ struct RotArgs {
     int64_t ld_in;            // elements between consecutive input rows
     void *out;                // int8 / f16-coded int / bf16, row stride K
     float *out_scale;         // per-row scale (quantizing outputs)
+    int32_t *out_l1;          // optional [M][K/1024]: sum of |code| over each 1024-long block of a row
+                              // (quantizing outputs of the three-pass kernels)
     int64_t M, K;
     int G;                    // groups per row
     unsigned int *status;     // device status word (bounded-wait timeouts)

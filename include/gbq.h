@@ -52,7 +52,7 @@ typedef struct gbq_rot {
 
 #define GBQ_OK 0
 #define GBQ_EINVAL (-22)      /* bad argument: null/misaligned pointer, bad size, bad rotation */
-#define GBQ_ENOSPC (-28)      /* workspace smaller than gbq_workspace_size() */
+#define GBQ_ENOSPC (-28)      /* workspace below the minimum (see gbq_workspace_size) */
 #define GBQ_ENODEV (-19)      /* no usable sm_103 device */
 #define GBQ_ECUDA (-5)        /* a CUDA runtime call or launch failed */
 #define GBQ_ENOTSUP (-95)     /* valid but unsupported combination (e.g. rotation shape) */
@@ -84,7 +84,13 @@ enum gbq_op {
     GBQ_OP_FFN = 3,         /* gbq_ffn_fused (M, d=K, H)                 */
     GBQ_OP_LINEAR_DX_INT8 = 4 /* gbq_linear_dx_int8 (M,N,K)             */
 };
-/* Bytes of device workspace the entry point for `op` needs at these sizes. */
+/* Bytes of device workspace to pass to the entry point for `op` at these sizes.
+ * The calls accept less, down to a minimum (linear / linear_acc: M*K*2 + M*4;
+ * ffn: those of x and of the hidden h plus g|u; each term rounded up to 256
+ * bytes) and reject a smaller workspace with GBQ_ENOSPC.  The reported size adds
+ * one int32 per quantized token row (the sum of its |codes|), which lets the
+ * int8 GEMM accumulate a token tile's whole K in one exact fp32 chunk when that
+ * sum is at most 2^17; below it the GEMM uses 1024-long chunks throughout. */
 size_t gbq_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t H);
 
 /* ---- rotate + quantize (activation side) ------------------------------ */

@@ -58,10 +58,15 @@ def test_bad_sizes_and_pointers_rejected(lib):
 
 
 def test_workspace_too_small_rejected(lib):
+    """gbq_workspace_size reports the preferred size (with the per-row code L1 norms that let the
+    GEMM run whole tiles as one exact chunk); calls accept anything down to the minimum, codes and
+    scales: M*K*2 + M*4, each rounded up to 256 bytes, and reject less."""
     p = ctypes.c_void_p(256)
     need = lib.gbq_workspace_size(1, 300, 512, 1024, 0)
-    assert need >= 300 * 1024 * 2
-    rc = lib.gbq_linear(p, p, p, None, p, 300, 512, 1024, R(32, 32, 1), p, need - 1, None)
+    a256 = lambda v: (v + 255) // 256 * 256
+    minimum = a256(300 * 1024 * 2) + a256(300 * 4)
+    assert need == minimum + a256(300 * 4)
+    rc = lib.gbq_linear(p, p, p, None, p, 300, 512, 1024, R(32, 32, 1), p, minimum - 1, None)
     assert rc == -28 and "workspace" in _err(lib)
 
 

@@ -173,3 +173,35 @@ def test_linear_large_accumulators_exact(ops):
     y_r = O.linear(xb, w8, ws, bias, rot)
     assert np.array_equal(bf16_np(y), y_r)
     assert np.abs(O.linear_acc(xb, w8, rot)[0]).max() == 127 * 127 * K
+
+
+def test_linear_acc_chunk_plans_exact(ops):
+    """Token tiles whose codes have small sums of |q| over their 1024-long K blocks accumulate
+    longer exact fp32 chunks, tiles with large ones (one-hot rows rotate to all-|127| codes) take
+    1024-long chunks: both must give
+    the exact int32 accumulator of the GPU's own codes, here against weights that include all-|127|
+    rows (the largest partial sums the bound allows)."""
+    rot, M, K, N = (64, 64, 1), 600, 4096, 300
+    rng = np.random.default_rng(41)
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    x[256:512] = 0.0
+    for r in range(256, 512):
+        x[r, (13 * r) % K] = 1.0 + (r % 7)  # one-hot: codes +-127 everywhere, sum |q| = 127 K
+    xb = I.bf16_bits(x)
+    w8 = rng.integers(-127, 128, (N, K)).astype(np.int8)
+    w8[:8] = 127
+    w8[8:16] = np.where(rng.random((8, K)) < 0.5, 127, -127)
+    acc, _ = ops.linear_acc(bf16_dev(xb), d(w8), rot)
+    qg, _ = ops.quantize_act(bf16_dev(xb), rot)
+    q = qg.cpu().numpy()
+    blk = np.abs(q.astype(np.int64)).reshape(M, 4, 1024).sum(axis=2)  # |q| sums of the 1024-long blocks
+    pairs = blk[:, 0::2] + blk[:, 1::2]
+    assert pairs[:256].max() <= 2 ** 17 and pairs[256:512].min() > 2 ** 17  # longer and default chunks
+    assert np.array_equal(acc.cpu().numpy().astype(np.int64), O.gemm_s8(q, w8))
+    # and through the FFN-sized contraction (K = 16384, rot128): large L1 -> default chunks
+    rot2, K2 = (128, 128, 1), 16384
+    x2 = I.bf16_bits(rng.standard_normal((130, K2)).astype(np.float32))
+    w2 = rng.integers(-127, 128, (64, K2)).astype(np.int8)
+    acc2, _ = ops.linear_acc(bf16_dev(x2), d(w2), rot2)
+    q2, _ = ops.quantize_act(bf16_dev(x2), rot2)
+    assert np.array_equal(acc2.cpu().numpy().astype(np.int64), O.gemm_s8(q2.cpu().numpy(), w2))
