@@ -526,6 +526,7 @@ int gbq_linear_acc(const void *x, const int8_t *w8, int32_t *acc, int64_t ld_acc
     if (rc) return rc;
     I8GemmProblem g = gemm_problem(d, qf, w8, M, N, K, EPI_ACC_I32, acc, ld_acc, nullptr, nullptr, nullptr);
     g.row_l1 = l1;
+    g.pdl = 1;  // directly after the quantizer launch
     return launch_i8gemm(g, st);
 }
 
@@ -569,6 +570,7 @@ int gbq_linear(const void *x, const int8_t *w8, const float *w_scale, const void
     if (rc) return rc;
     I8GemmProblem g = gemm_problem(d, qf, w8, M, N, K, EPI_DEQUANT_BF16, y, N, xs, w_scale, bias);
     g.row_l1 = l1;
+    g.pdl = 1;  // directly after the quantizer launch
     return launch_i8gemm(g, st);
 }
 
@@ -615,6 +617,7 @@ int gbq_ffn_fused(const void *x, const int8_t *wg8, const float *s_gate, const i
     g.n_split = H;
     g.w_scale1 = s_up;
     g.row_l1 = l1x;
+    g.pdl = 1;
     rc = launch_i8gemm(g, st);
     if (rc) return rc;
     // 3) h = silu(g) * u, rotate over H, quantize
@@ -632,6 +635,7 @@ int gbq_ffn_fused(const void *x, const int8_t *wg8, const float *s_gate, const i
     // 4) down GEMM + dequant
     I8GemmProblem gd = gemm_problem(dv, qh, wd8, M, d, H, EPI_DEQUANT_BF16, y, d, hs, s_down, nullptr);
     gd.row_l1 = l1h;
+    gd.pdl = 1;
     return launch_i8gemm(gd, st);
 }
 

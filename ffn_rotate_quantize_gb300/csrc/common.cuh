@@ -60,6 +60,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Programmatic dependent launch.  pdl_wait: block until the grids this one depends on have
+// completed and their memory is visible (a no-op when the launch did not allow overlap);
+// pdl_allow_dependents: let a dependent grid launched with overlap allowed start its prologue.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Bounded wait for the phase with the given parity.  `abort` is a CTA-shared
 // flag: once any thread of the CTA has given up, every other wait returns at
 // once.  Returns false on timeout/abort (after recording the status).

@@ -41,6 +41,8 @@ struct I8GemmProblem {
     unsigned int *status;
     int num_sms;
     const int32_t *row_l1;    // optional [M][K/1024]: sum of |q| over each 1024-long block of a token row
+    int pdl;                  // launch so the kernel may start while the preceding (quantizer) kernel runs:
+                              // it reads the tokens, scales and L1 sums only after that kernel completes
 };
 
 // Enqueue the exact int8 GEMM (tcgen05, fp16-coded operands, chunked fp32 -> int32).

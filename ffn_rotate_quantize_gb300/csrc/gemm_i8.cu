@@ -270,7 +270,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) i8gemm_
             const uint32_t pid = (uint32_t)producer_id(warp);
             if (lane == 0) {
                 uint32_t gs = 0;
-                bool ok = true;
+                bool ok = true, dep_done = false;
                 for (int64_t t = pair; t < num_tiles && ok; t += npairs) {
                     int64_t n0, m0;
                     tile_coords(t, m_tiles, &n0, &m0);
@@ -294,6 +294,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) i8gemm_
                         else
                             tma_load_2d(wdst, tw, fb, wrow, kt * kBK);  // 128 contraction rows x 128 columns
                         uint8_t *bdst = bbuf + stage * kBStageBytes;
+                        if (!dep_done) {  // the tokens come from the preceding kernel: wait for it once
+                            pdl_wait();
+                            dep_done = true;
+                        }
 #pragma unroll
                         for (int b = 0; b < kSubs; ++b)
                             tma_load_2d(bdst + b * kTokBox, &p.tm_b, fb, kt * kBK + b * kSub, trow);
@@ -412,6 +416,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) i8gemm_
         }
     } else {
         setmaxnreg_inc<kRegsEpi>();
+        pdl_wait();  // scales, L1 sums and the output: only after the preceding kernel completed
         // ------------------------------------------------ chunk plan (epilogue warps, once)
         // Every partial sum of token m's products with int8 weights (|w| <= 128) over a set of K
         // indices is bounded by 128 * sum |q[m][k]| over that set.  A chunk of 2^j aligned 1024-long
@@ -627,7 +632,21 @@ int launch_i8gemm(const I8GemmProblem &q, cudaStream_t st) {
     const int64_t pairs_max = max_pairs_for_device(q.num_sms);
     const int grid = 2 * (int)(tiles < pairs_max ? tiles : pairs_max);
     prof_begin(1, st);
-    i8gemm_kernel<<<grid, kThreads, kSmemBytes, st>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute lattr[1];
+    lattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    lattr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = lattr;
+    cfg.numAttrs = q.pdl ? 1 : 0;
+    const cudaError_t le = cudaLaunchKernelEx(&cfg, i8gemm_kernel, p);
+    if (le != cudaSuccess) {
+        prof_end(st);
+        return gbq_fail(GBQ_ECUDA, cudaGetErrorString(le));
+    }
     prof_end(st);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return gbq_fail(GBQ_ECUDA, cudaGetErrorString(e));

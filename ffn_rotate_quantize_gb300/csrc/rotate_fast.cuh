@@ -177,6 +177,7 @@ __global__ void __launch_bounds__(128) rot64_kernel(const __grid_constant__ Fast
     float *wmax = reinterpret_cast<float *>(smem + f.misc_off + 32);
     const int tau = threadIdx.x;
     const uint32_t rb = p.row_in_bytes;
+    pdl_allow_dependents();  // a GEMM launched after this kernel may set itself up meanwhile
 
     if (tau == 0) {
         for (int s = 0; s < f.stages; ++s) mbar_init(&full[s], 1);
@@ -265,6 +266,7 @@ __global__ void __launch_bounds__(512, 2) rot128_kernel(const __grid_constant__ 
     float *wmax = reinterpret_cast<float *>(smem + f.misc_off + 32);
     const int tau = threadIdx.x;
     const uint32_t rb = p.row_in_bytes;
+    pdl_allow_dependents();  // a GEMM launched after this kernel may set itself up meanwhile
 
     if (tau == 0) {
         mbar_init(&full[0], 1);
