@@ -679,6 +679,7 @@ int gbq_linear_dx_int8(const void *dy, const int8_t *w8, const float *w_scale, v
     g.ld_w = K;
     g.w_rows_total0 = N;
     g.w_rows_total1 = N;
+    g.pdl = 1;  // directly after the quantizer launch
     rc = launch_i8gemm(g, st);
     if (rc) return rc;
     // 3) dx = bf16(dx_rot R)

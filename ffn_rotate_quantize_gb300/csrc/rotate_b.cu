@@ -28,6 +28,7 @@ __global__ void __launch_bounds__(kIdThreads) quant_identity_kernel(IdArgs p) {
     __shared__ float s_warp[kIdThreads / 32];
     const int64_t row = blockIdx.x;
     const int tid = threadIdx.x;
+    pdl_allow_dependents();  // a GEMM launched after this kernel may set itself up meanwhile
     const int nchunks = (int)(p.K / 8);
     const uint4 *src = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(p.in) + row * p.ld_in);
     float v[kIdMaxChunks][8];
