@@ -339,9 +339,14 @@ def run_ours(args):
         assert n_gv == 1 and n_other == 0, "the decode call is not a single GEMV launch"
         gv_ms = batch_ms(torch, flush, opfn["decode_gemv"], reps=32)
         ach = DECODE_BYTES / (gv_ms * 1e-3) * 1e-9
-        dec = {"bound": "hbm", "kernel": "gemv_kernel (decode 1x4096x4096)", "achieved": round(ach, 1),
+        graph_ms = graph_batch_ms(torch, flush, opfn["decode_gemv"], reps=32)
+        ach_g = DECODE_BYTES / (graph_ms * 1e-3) * 1e-9
+        dec = {"bound": "hbm", "kernel": "gemv_direct_kernel (decode 1x4096x4096)", "achieved": round(ach, 1),
                "peak": peaks["hbm"], "unit": "GB/s", "frac": round(ach / peaks["hbm"], 4), "ms": round(gv_ms, 4),
-               "traffic": profiled_traffic("gemv_kernel")}
+               "traffic": profiled_traffic("gemv_direct_kernel"),
+               "graph": {"ms": round(graph_ms, 4), "achieved": round(ach_g, 1),
+                         "frac": round(ach_g / peaks["hbm"], 4),
+                         "note": "the same 32 calls captured in one CUDA graph, replayed under one event pair"}}
 
     out = {
         "metric": METRIC, "value": None if value is None else round(value, 2), "unit": "TOPS", "n_gpus": world, "steps": args.steps,
@@ -380,6 +385,29 @@ def batch_ms(torch, flush, fn, reps=32):
         fn(i)
     e1.record(st)
     torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def graph_batch_ms(torch, flush, fn, reps=32):
+    """batch_ms with the reps calls captured once in a CUDA graph (after an eager warm-up call) and the
+    replay timed: host launch overhead leaves the timed region, device-side launch gaps stay."""
+    fn(0)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(reps):
+            fn(i)
+    g.replay()  # first replay uploads the graph
+    torch.cuda.synchronize()
+    flush.zero_()
+    st = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    g.replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    del g
     return e0.elapsed_time(e1) / reps
 
 

@@ -1,0 +1,97 @@
+"""The hot-path calls captured in a CUDA graph and replayed give the eager results bit for bit
+(decode GEMV, prefill linear with its quantizer-to-GEMM overlap, the fused FFN, dx_int8)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from ffn_rotate_quantize_gb300 import inputs as I
+from parity import bf16_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ops():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from ffn_rotate_quantize_gb300 import ops as G
+    G.init()
+    return G
+
+
+@pytest.fixture(autouse=True)
+def _device_status_clean(ops):
+    yield
+    assert ops.device_status() == 0
+
+
+def d(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _capture_and_compare(ops, calls):
+    """calls: list of (fn(out), out tensor).  Eager run, then the same calls captured in one graph
+    (first-launch set-up happened in the eager run) and replayed twice into fresh outputs."""
+    eager = []
+    for fn, out in calls:
+        fn(out)
+        eager.append(out.clone())
+    torch.cuda.synchronize()
+    for _, out in calls:
+        out.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for fn, out in calls:
+            fn(out)
+    for _ in range(2):
+        for _, out in calls:
+            out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for (_, out), ref in zip(calls, eager):
+            assert torch.equal(out.view(torch.int16) if out.dtype == torch.bfloat16 else out,
+                               ref.view(torch.int16) if ref.dtype == torch.bfloat16 else ref)
+
+
+def test_graph_decode_and_prefill(ops):
+    rot = (64, 64, 1)
+    rng = np.random.default_rng(77)
+    w = I.bf16_bits(rng.standard_normal((1500, 4096)).astype(np.float32) * np.float32(0.02))
+    w8, ws = O.prepare_weight(w, rot)
+    w8d, wsd = d(w8), d(ws)
+    bias = bf16_dev(I.bf16_bits(rng.standard_normal(1500).astype(np.float32) * np.float32(0.01)))
+    x1 = bf16_dev(I.bf16_bits(rng.standard_normal((1, 4096)).astype(np.float32)))
+    x2 = bf16_dev(I.bf16_bits(rng.standard_normal((300, 4096)).astype(np.float32)))
+    ws1 = torch.empty(ops.workspace_size(ops.OP_LINEAR, 1, 1500, 4096), dtype=torch.uint8, device="cuda")
+    ws2 = torch.empty(ops.workspace_size(ops.OP_LINEAR, 300, 1500, 4096), dtype=torch.uint8, device="cuda")
+    y1 = torch.empty((1, 1500), dtype=torch.bfloat16, device="cuda")
+    y2 = torch.empty((300, 1500), dtype=torch.bfloat16, device="cuda")
+    _capture_and_compare(ops, [
+        (lambda out: ops.linear(x1, w8d, wsd, None, rot, ws1, out=out), y1),
+        (lambda out: ops.linear(x2, w8d, wsd, bias, rot, ws2, out=out), y2),
+    ])
+
+
+@pytest.mark.parametrize("M", [1, 64])
+def test_graph_ffn_and_dx_int8(ops, M):
+    """The fused FFN (decode and prefill token counts) and dx_int8 against the down projection."""
+    rd, rh = (32, 32, 1), (64, 64, 1)
+    c = I.ffn_case(M, 1024, 4096, seed=78 + M)
+    wg8, sg = O.prepare_weight(c["wg"], rd)
+    wu8, su = O.prepare_weight(c["wu"], rd)
+    wd8, sd = O.prepare_weight(c["wd"], rh)
+    x = bf16_dev(c["x"])
+    t = [d(a) for a in (wg8, sg, wu8, su, wd8, sd)]
+    wsf = torch.empty(ops.workspace_size(ops.OP_FFN, M, 0, 1024, 4096), dtype=torch.uint8, device="cuda")
+    yf = torch.empty((M, 1024), dtype=torch.bfloat16, device="cuda")
+    # dy [130, d] against W_down [d, H] (rotated over H): dx [130, H]
+    dy = bf16_dev(I.bf16_bits(np.random.default_rng(79).standard_normal((130, 1024)).astype(np.float32)
+                              * np.float32(1e-3)))
+    wsx = torch.empty(ops.workspace_size(ops.OP_LINEAR_DX_INT8, 130, 1024, 4096), dtype=torch.uint8,
+                      device="cuda")
+    dx = torch.empty((130, 4096), dtype=torch.bfloat16, device="cuda")
+    _capture_and_compare(ops, [
+        (lambda out: ops.ffn_fused(x, *t, rd, rh, wsf, out=out), yf),
+        (lambda out: ops.linear_dx_int8(dy, t[4], t[5], rh, wsx, out=out), dx),
+    ])
