@@ -357,3 +357,27 @@ void orc_matmul_bf16_nn(const uint16_t *dy, const uint16_t *w, uint16_t *dx,
         free(row);
     }
 }
+
+/*
+ * y[m][n] = bf16( sum_k x[m][k] * w[n][k] + bias[n] ) with bf16 inputs, the
+ * sum and the bias add in fp64, rounded to fp32 and then to bf16: the linear
+ * layer of the rotate-only BF16 path ("Use from C": the activation rotated by
+ * the rotate-only kernel, then a bf16 linear against the pre-rotated weight).
+ * bias may be NULL.
+ */
+void orc_linear_bf16(const uint16_t *x, const uint16_t *w, const uint16_t *bias,
+                     uint16_t *y, int64_t M, int64_t N, int64_t K)
+{
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t m = 0; m < M; ++m) {
+        const uint16_t *xr = x + m * K;
+        for (int64_t n = 0; n < N; ++n) {
+            const uint16_t *wr = w + n * K;
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += (double)bf16_bits_to_f32(xr[k]) * (double)bf16_bits_to_f32(wr[k]);
+            if (bias) acc += (double)bf16_bits_to_f32(bias[n]);
+            y[m * N + n] = f32_to_bf16_bits((float)acc);
+        }
+    }
+}

@@ -251,3 +251,20 @@ def linear_dx_int8(dy_bf16, w8, s, rot, keep=False):
 def rotate_bf16(x_bf16, rot) -> np.ndarray:
     """Rotate-only bf16 path ("Use from C": the BF16 path needs only the rotation)."""
     return f32_to_bf16(rotate(bf16_to_f32(x_bf16), rot))
+
+
+def linear_bf16(x_bf16, w_bf16, bias_bf16=None) -> np.ndarray:
+    """y = bf16(x @ W^T + bias) with bf16 inputs, fp64 sums, one rounding to fp32 then bf16.
+
+    The linear layer of the rotate-only BF16 path ("Use from C"): with x and W both rotated by the
+    same R (R R^T = I) it computes the unrotated layer up to bf16 rounding."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    w = np.ascontiguousarray(w_bf16, dtype=np.uint16)
+    M, K = x.shape
+    N, K2 = w.shape
+    assert K == K2
+    b = None if bias_bf16 is None else np.ascontiguousarray(bias_bf16, dtype=np.uint16)
+    assert b is None or b.shape == (N,)
+    y = np.empty((M, N), np.uint16)
+    _load().orc_linear_bf16(_p(x), _p(w), None if b is None else _p(b), _p(y), _i64(M), _i64(N), _i64(K))
+    return y

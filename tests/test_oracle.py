@@ -340,3 +340,40 @@ def test_linear_dx_int8_exact_when_dy_is_on_the_grid():
     exact = (qd @ w8.astype(np.int64)).astype(np.float64) * float(step)
     want = O.bf16_to_f32(O.f32_to_bf16(exact.astype(np.float32)))
     assert np.array_equal(dx, want)
+
+
+# ------------------------------------------------------------------ rotate-only bf16 path
+def test_linear_bf16_integer_brute_force():
+    """Small-integer operands: the exact sum (Python integers, loop over k) rounded once to bf16.
+    Non-square shapes, so a transposed operand or a dropped bias fails."""
+    rng = np.random.default_rng(31)
+    M, N, K = 3, 5, 64
+    xi = rng.integers(-8, 9, (M, K))
+    wi = rng.integers(-8, 9, (N, K))
+    bi = rng.integers(-50, 51, N)
+    xb = I.bf16_bits(xi.astype(np.float32))
+    wb = I.bf16_bits(wi.astype(np.float32))
+    bb = I.bf16_bits(bi.astype(np.float32))
+    for bias in (None, bb):
+        y = O.linear_bf16(xb, wb, bias)
+        for m in range(M):
+            for n in range(N):
+                exact = sum(int(xi[m, k]) * int(wi[n, k]) for k in range(K)) + (0 if bias is None else int(bi[n]))
+                assert y[m, n] == I.bf16_bits(np.array([exact], np.float32))[0], (m, n)
+
+
+def test_linear_bf16_rotated_pair_is_the_unrotated_layer():
+    """"Use from C": the BF16 path rotates the activation and multiplies by the pre-rotated weight;
+    R orthogonal makes that the original layer up to the bf16 roundings of the rotated operands."""
+    rng = np.random.default_rng(32)
+    M, K, N, rot = 16, 256, 48, (16, 16, 1)
+    x = I.bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    w = I.bf16_bits(rng.standard_normal((N, K)).astype(np.float32) * np.float32(0.02))
+    b = I.bf16_bits(rng.standard_normal(N).astype(np.float32) * np.float32(0.01))
+    y = O.bf16_to_f32(O.linear_bf16(O.rotate_bf16(x, rot), O.rotate_bf16(w, rot), b)).astype(np.float64)
+    ref = (I.bf16_to_float(x).astype(np.float64) @ I.bf16_to_float(w).astype(np.float64).T
+           + I.bf16_to_float(b).astype(np.float64))
+    rel = np.linalg.norm(y - ref) / np.linalg.norm(ref)
+    assert rel < 6e-3, rel
+    # and the rotation is not the identity on this data: the rotated operands differ from the inputs
+    assert not np.array_equal(O.rotate_bf16(x, rot), x)
