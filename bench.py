@@ -11,6 +11,9 @@ synthetic workload (shapes and distributions of the method's configurations):
                    R_d = H64 (x) H64, R_h = H128 (x) H128
   backward dx      dy [4096,16384], W8 [16384,4096]: dequant_weight, linear_dx (bf16),
                    linear_dx_int8
+  rotated bf16     the page's fair comparator on the prefill shape: rotate-only kernel on x,
+                   then a bf16 linear against the pre-rotated bf16 weight (+ bias); the
+                   line reports the int8 layer's speedup over it
 Inputs are resident in HBM; L2 is flushed (a 512 MB write) before every timed
 operation, outside its CUDA-event window.  `value` is the prefill linear's
 throughput 2*M*N*K / t.  The int8 contraction runs exactly on the f16 tensor
@@ -44,7 +47,7 @@ DECODE_BYTES = 4096 * 4096 + 4096 * 4 + 4096 * 2 + 4096 * 2  # W8 + s + x + y
 DEQW_BYTES = 16384 * 4096 * 3 + 16384 * 4  # int8 read + bf16 write + scales
 WORKLOAD = ("prefill INT8 linear x[1024,4096] @ W8[14336,4096]^T + bias, R=H64(x)H64/64; "
             "step also runs decode GEMV [1x4096x4096], SwiGLU FFN [1024,4096,16384], "
-            "backward dx [4096,16384,4096]")
+            "backward dx [4096,16384,4096], rotated-bf16 comparator [1024,4096,14336]")
 
 
 def load_peaks():
@@ -177,11 +180,14 @@ def run_ours(args):
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     ops = []
-    if want("linear", "linear_acc", "dequant") or not args.only:
+    if want("linear", "linear_acc", "dequant", "linear_bf16_rotated") or not args.only:
         c3 = I.linear_case(M3, K3, N3, n_outliers=I.outlier_count(K3), outlier_scale=30.0, bias_std=0.01, seed=0)
         x3, b3 = bf(c3["x"]), bf(c3["bias"])
-        w83, s3 = G.prepare_weight(bf(c3["w"]), PREFILL["rot"])
-        del c3
+        w3 = bf(c3["w"])
+        w83, s3 = G.prepare_weight(w3, PREFILL["rot"])
+        # the rotate-only BF16 path stores the weight pre-rotated in bf16 (one-time, untimed)
+        wr3 = G.rotate_bf16(w3, PREFILL["rot"]) if want("linear_bf16_rotated") else None
+        del c3, w3
         ws_lin = torch.empty(G.workspace_size(G.OP_LINEAR, M3, N3, K3), dtype=torch.uint8, device=dev)
         y3 = torch.empty((M3, N3), dtype=torch.bfloat16, device=dev)
         acc3 = torch.empty((M3, N3), dtype=torch.int32, device=dev)
@@ -195,6 +201,11 @@ def run_ours(args):
                 G._ptr(ws_lin), ws_lin.numel(), G._stream())))
         if want("dequant"):
             ops.append(("dequant", lambda i: G.dequant(acc3, xs3, s3, b3, out=y3b)))
+        if want("linear_bf16_rotated"):
+            # the page's fair comparator: rotate-only kernel on x, then a bf16 linear against bf16(W R)
+            xr3 = torch.empty_like(x3)
+            ops.append(("linear_bf16_rotated", lambda i: (G.rotate_bf16(x3, PREFILL["rot"], out=xr3),
+                                                          G.linear_bf16(xr3, wr3, b3, out=y3b))))
     if want("decode_gemv"):
         c2 = I.linear_case(DECODE["M"], DECODE["K"], DECODE["N"], n_outliers=I.outlier_count(DECODE["K"]),
                            outlier_scale=30.0, bias_std=None, seed=0)
@@ -246,6 +257,7 @@ def run_ours(args):
         "dequant_weight": (float(DEQW_BYTES), "GB/s"),
         "linear_dx": (2.0 * BWD["M"] * BWD["N"] * BWD["K"], "TFLOP/s"),
         "linear_dx_int8": (2.0 * BWD["M"] * BWD["N"] * BWD["K"], "TOPS"),
+        "linear_bf16_rotated": (2.0 * M3 * N3 * K3, "TFLOP/s"),
     }
     evs = {name: [] for name, _ in ops}
 
@@ -357,6 +369,8 @@ def run_ours(args):
                          "launches cycling inputs larger than L2 (4 prefill / 16 decode weight copies)",
                    "parallelism": f"replicas x{world}"},
         "roofline": roof, "decode_roofline": dec, "rows": rows, "gpu_launches": launches,
+        "int8_speedup_vs_rotated_bf16": (round(rows["linear_bf16_rotated"]["ms"] / rows["linear"]["ms"], 3)
+                                         if "linear_bf16_rotated" in rows and "linear" in rows else None),
         "kernel_ms_census_step": {k: round(v[1], 3) for k, v in zip(("rotate", "i8gemm", "bf16gemm", "gemv",
                                                                      "elemwise"), prof.values())},
         "e2e": e2e, "clocks": clk,

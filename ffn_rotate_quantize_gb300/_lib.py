@@ -44,6 +44,7 @@ SIGNATURES = {
                       c_vp],
     "gbq_dequant_weight": [c_vp, c_vp, c_vp, c_i64, c_i64, Rot, c_vp],
     "gbq_linear_dx": [c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp],
+    "gbq_linear_bf16": [c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, c_vp],
     "gbq_linear_dx_int8": [c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, Rot, c_vp, c_sz, c_vp],
     "gbq_rotate_bf16": [c_vp, c_vp, c_i64, c_i64, Rot, c_vp],
     "gbq_linear_noalloc": [c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_i64, Rot, c_vp],

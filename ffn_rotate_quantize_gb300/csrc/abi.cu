@@ -649,6 +649,20 @@ int gbq_linear_dx(const void *dy, const void *w, void *dx, int64_t M, int64_t N,
     return launch_bf16_gemm_nn(dy, w, dx, M, N, K, d->status, d->sms, (cudaStream_t)stream);
 }
 
+int gbq_linear_bf16(const void *x, const void *w, const void *bias, void *y, int64_t M, int64_t N, int64_t K,
+                    void *stream) {
+    REQUIRE(M >= 0 && N >= 1 && K >= 64, "gbq_linear_bf16: bad sizes M=%lld N=%lld K=%lld", (long long)M,
+            (long long)N, (long long)K);
+    REQUIRE(K % 64 == 0, "gbq_linear_bf16: K must be a multiple of 64");
+    REQUIRE(N <= ((int64_t)1 << 31) && K <= ((int64_t)1 << 31) && M <= ((int64_t)1 << 31),
+            "gbq_linear_bf16: sizes beyond 2^31");
+    if (M == 0) return GBQ_OK;
+    REQUIRE(a16(x) && a16(w) && a16(y), "gbq_linear_bf16: x, w, y must be non-NULL and 16-byte aligned");
+    REQUIRE(((uintptr_t)bias & 1) == 0, "gbq_linear_bf16: bias must be 2-byte aligned");
+    INIT(d);
+    return launch_bf16_gemm_tn(x, w, bias, y, M, N, K, d->status, d->sms, (cudaStream_t)stream);
+}
+
 int gbq_linear_dx_int8(const void *dy, const int8_t *w8, const float *w_scale, void *dx, int64_t M, int64_t N,
                        int64_t K, gbq_rot rot, void *workspace, size_t ws_bytes, void *stream) {
     // The GEMM contracts over N (W8's rows) and produces K output columns.

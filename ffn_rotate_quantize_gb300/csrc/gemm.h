@@ -51,6 +51,9 @@ int launch_i8gemm(const I8GemmProblem &p, cudaStream_t st);
 // bf16 GEMM dx[M][K] = dy[M][N] @ w[N][K] (fp32 accumulation).
 int launch_bf16_gemm_nn(const void *dy, const void *w, void *dx, int64_t M, int64_t N, int64_t K,
                         unsigned int *status, int num_sms, cudaStream_t st);
+// bf16 GEMM y[M][N] = x[M][K] @ w[N][K]^T + bias[N] (fp32 accumulation and bias add; bias nullable).
+int launch_bf16_gemm_tn(const void *x, const void *w, const void *bias, void *y, int64_t M, int64_t N, int64_t K,
+                        unsigned int *status, int num_sms, cudaStream_t st);
 
 // Decode GEMV (M <= 8): y[m][n] = dequant(sum_k q[m][k] w8[n][k]) from a rotated+quantized x.
 // Returns GBQ_ENOTSUP (nothing launched) for shapes it does not cover.

@@ -121,12 +121,24 @@ def dequant_act_quantize(acc_g, acc_u, x_scale, s_gate, s_up, r, stream=None):
     return q, s
 
 
-def rotate_bf16(x: torch.Tensor, r, stream=None):
+def rotate_bf16(x: torch.Tensor, r, stream=None, out=None):
     """bf16 [M,K] -> bf16(R x)."""
     _req(x, torch.bfloat16, "x")
     M, K = x.shape
-    y = torch.empty_like(x)
+    y = torch.empty_like(x) if out is None else out
     check(lib().gbq_rotate_bf16(_ptr(x), _ptr(y), M, K, _rot(r), _stream(stream)))
+    return y
+
+
+def linear_bf16(x: torch.Tensor, w: torch.Tensor, bias=None, out=None, stream=None):
+    """bf16 x [M,K] @ bf16 w[N,K]^T + bias [N] -> bf16 y [M,N] (the rotate-only path's linear)."""
+    _req(x, torch.bfloat16, "x")
+    _req(w, torch.bfloat16, "w")
+    M, K = x.shape
+    N = w.shape[0]
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device) if out is None else out
+    check(lib().gbq_linear_bf16(_ptr(x), _ptr(w), _ptr(bias), _ptr(y), M, N, K,
+                                _stream(stream)))
     return y
 
 

@@ -251,13 +251,30 @@ int gbq_linear_dx_int8(const void *dy, const int8_t *w8, const float *w_scale, v
  */
 int gbq_rotate_bf16(const void *x, void *xr, int64_t M, int64_t K, gbq_rot rot, void *stream);
 
+/*
+ * y = x @ w^T + bias: the bf16 linear layer of the rotate-only path ("Use from
+ * C": the BF16 comparator rotates the activation with gbq_rotate_bf16 and
+ * multiplies it by the weight stored pre-rotated in bf16, w = bf16(W R); since
+ * R is orthogonal, (x R)(W R)^T = x W^T up to the bf16 roundings).
+ * x bf16 [M,K] (activation, K contiguous); w bf16 [N,K] (K contiguous);
+ * bias bf16 [N] or NULL; y bf16 [M,N].  fp32 accumulation on the tensor cores,
+ * bias added in fp32, one rounding to bf16.  K must be a multiple of 64; M >= 0
+ * (M = 0 launches nothing), N >= 1 (any N; rows of y start 16-byte aligned only
+ * when N % 8 == 0, otherwise the epilogue stores element by element).
+ * x, w, y must be 16-byte aligned; bias needs bf16 alignment only.  All buffers
+ * caller-owned; nothing is allocated.
+ */
+int gbq_linear_bf16(const void *x, const void *w, const void *bias, void *y, int64_t M, int64_t N,
+                    int64_t K, void *stream);
+
 /* ---- kernel timing ------------------------------------------------------ */
 
 /* Kernel classes for gbq_prof_read(). */
 enum gbq_kernel {
     GBQ_K_ROTATE = 0,   /* rotate(+quantize) kernels            */
     GBQ_K_I8GEMM = 1,   /* exact int8 tensor-core GEMM          */
-    GBQ_K_BF16GEMM = 2, /* bf16 tensor-core GEMM (linear_dx)    */
+    GBQ_K_BF16GEMM = 2, /* bf16 tensor-core GEMMs (linear_dx,   */
+                        /* linear_bf16)                         */
     GBQ_K_GEMV = 3,     /* decode GEMV                          */
     GBQ_K_ELEMWISE = 4  /* dequant / operand coding / scaling   */
 };
