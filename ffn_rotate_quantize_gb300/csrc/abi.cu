@@ -683,8 +683,9 @@ int gbq_linear_dx_int8(const void *dy, const int8_t *w8, const float *w_scale, v
     void *qd = w.take((size_t)M * N * 2);
     float *t = (float *)w.take((size_t)M * 4);
     float *dxr = (float *)w.take((size_t)M * K * 4);
+    int32_t *l1 = (int32_t *)w.take((size_t)M * 4 * ((N + 1023) / 1024));  // block L1 norms: preferred size only
     // 1) dy' = dy * s[n] (column scale), per-row quantize, no rotation
-    IdArgs ia{dy, w_scale, N, qd, t, M, N};
+    IdArgs ia{dy, w_scale, N, qd, t, M, N, l1};
     cudaError_t e = launch_quant_identity(OUT_F16Q, ia, st);
     if (e != cudaSuccess) return cuda_fail(e, "gbq_linear_dx_int8 (quantize dy)");
     // 2) acc[m, k] = sum_n qd[m, n] w8[n, k]; dx_rot = fp32(acc) * t[m]
@@ -693,6 +694,7 @@ int gbq_linear_dx_int8(const void *dy, const int8_t *w8, const float *w_scale, v
     g.ld_w = K;
     g.w_rows_total0 = N;
     g.w_rows_total1 = N;
+    g.row_l1 = l1;
     g.pdl = 1;  // directly after the quantizer launch
     rc = launch_i8gemm(g, st);
     if (rc) return rc;

@@ -19,6 +19,7 @@ struct IdArgs {
     void *out;                // int8 or f16-coded int [M, K]
     float *out_scale;         // fp32 [M]
     int64_t M, K;
+    int32_t *out_l1;          // [M][ceil(K/1024)] sums of |code| over 1024-long blocks, or nullptr
 };
 
 // Launch a rotate(+quantize) kernel.  Returns cudaErrorNotSupported for a

@@ -142,6 +142,8 @@ size_t gemm_workspace_size_pref(int op, int64_t M, int64_t N, int64_t K, int64_t
             return base + align256((size_t)M * 4 * blocks(K));
         case GBQ_OP_FFN:
             return base + align256((size_t)M * 4 * blocks(K)) + align256((size_t)M * 4 * blocks(H));
+        case GBQ_OP_LINEAR_DX_INT8:  // the contraction runs over N
+            return base + align256((size_t)M * 4 * blocks(N));
         default:
             return base;
     }

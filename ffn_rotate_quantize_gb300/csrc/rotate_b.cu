@@ -26,6 +26,7 @@ constexpr int kIdChunkCap = 8;  // K <= 512 * 8 * 8 = 32768
 template <int OUT, int kIdMaxChunks, int kIdThreads>
 __global__ void __launch_bounds__(kIdThreads) quant_identity_kernel(IdArgs p) {
     __shared__ float s_warp[kIdThreads / 32];
+    __shared__ int s_l1[32];  // per 1024-long block: sum of |code| (K <= 32768)
     const int64_t row = blockIdx.x;
     const int tid = threadIdx.x;
     pdl_allow_dependents();  // a GEMM launched after this kernel may set itself up meanwhile
@@ -106,6 +107,23 @@ __global__ void __launch_bounds__(kIdThreads) quant_identity_kernel(IdArgs p) {
                 words[c][h] = w;
             }
         }
+    }
+    if (p.out_l1) {  // uniform over the CTA
+        // Chunk ch lies in block ch / 128; a warp's 32 chunks of one c share a block (threads come in
+        // groups of 128), so one warp sum per c goes into the block's shared counter.
+        const int nb = (int)((p.K + 1023) / 1024);
+        if (tid < 32) s_l1[tid] = 0;
+        __syncthreads();
+#pragma unroll
+        for (int c = 0; c < kIdMaxChunks; ++c) {
+            int l = __dp4a((int)__vabsss4(words[c][0]), 0x01010101, __dp4a((int)__vabsss4(words[c][1]), 0x01010101, 0));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+            const int b = (tid + c * kIdThreads) >> 7;
+            if ((tid & 31) == 0 && b < nb && l) atomicAdd(&s_l1[b], l);
+        }
+        __syncthreads();
+        if (tid < nb) p.out_l1[row * nb + tid] = s_l1[tid];
     }
 #pragma unroll
     for (int c = 0; c < kIdMaxChunks; ++c) {

@@ -85,12 +85,15 @@ enum gbq_op {
     GBQ_OP_LINEAR_DX_INT8 = 4 /* gbq_linear_dx_int8 (M,N,K)             */
 };
 /* Bytes of device workspace to pass to the entry point for `op` at these sizes.
- * The calls accept less, down to a minimum (linear / linear_acc: M*K*2 + M*4;
- * ffn: those of x and of the hidden h plus g|u; each term rounded up to 256
- * bytes) and reject a smaller workspace with GBQ_ENOSPC.  The reported size adds
- * one int32 per quantized token row (the sum of its |codes|), which lets the
- * int8 GEMM accumulate a token tile's whole K in one exact fp32 chunk when that
- * sum is at most 2^17; below it the GEMM uses 1024-long chunks throughout. */
+ * The calls accept less, down to a minimum (linear / linear_acc / int8_gemm:
+ * M*K*2 + M*4; ffn: those of x and of the hidden h plus g|u; linear_dx_int8:
+ * M*N*2 + M*4 + M*K*4; each term rounded up to 256 bytes) and reject a smaller
+ * workspace with GBQ_ENOSPC.  For linear, linear_acc, ffn and linear_dx_int8
+ * the reported size adds, per quantized token row, one int32 per 1024-long block
+ * of the contraction (the sum of the row's |codes| over the block): the int8
+ * GEMM then gives each 256-token tile the longest exact fp32 chunk of 2^j
+ * aligned blocks whose sums stay within 2^17 for all of its tokens; with the
+ * minimum it uses 1024-long chunks throughout.  The results are identical. */
 size_t gbq_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t H);
 
 /* ---- rotate + quantize (activation side) ------------------------------ */

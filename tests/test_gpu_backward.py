@@ -76,3 +76,39 @@ def test_linear_dx_int8_large_accumulators(ops):
     s = np.ones(N, np.float32)
     dx = ops.linear_dx_int8(bf16_dev(dy), d(w8), d(s), (16, 16, 1))
     assert_bf16_parity(bf16_np(dx), O.linear_dx_int8(dy, w8, s, (16, 16, 1)))
+
+
+def _a256(v):
+    return (v + 255) // 256 * 256
+
+
+def test_linear_dx_int8_chunk_plan(ops):
+    """With the preferred workspace the dy quantizer also writes each row's sum of |code| over every
+    1024-long block of N, and the int8 GEMM accumulates longer exact fp32 chunks for token tiles whose
+    sums allow it.  The result must equal, bit for bit, the one from the minimum workspace (1024-long
+    chunks), here with a tile of all-(+127) rows against all-(+127) weight columns (partial sums up to
+    127^2 * 1024 per block, so that tile must keep 1024-long chunks) beside Gaussian tiles."""
+    rng = np.random.default_rng(23)
+    M, N, K, rot = 300, 16384, 1024, (32, 32, 1)
+    dy = rng.standard_normal((M, N)).astype(np.float32) * np.float32(1e-3)
+    dy[:128] = np.float32(2e-3)  # codes +127 everywhere
+    dy_b = I.bf16_bits(dy)
+    w8 = rng.integers(-127, 128, (N, K)).astype(np.int8)
+    w8[:, :8] = 127
+    s = np.ones(N, np.float32)
+    dyd, w8d, sd = bf16_dev(dy_b), d(w8), d(s)
+    pref = ops.workspace_size(ops.OP_LINEAR_DX_INT8, M, N, K)
+    minimum = _a256(M * N * 2) + _a256(M * 4) + _a256(M * K * 4)
+    assert pref == minimum + _a256(M * 4 * (N // 1024))
+    ws_p = torch.zeros(pref, dtype=torch.uint8, device="cuda")
+    ws_m = torch.zeros(minimum, dtype=torch.uint8, device="cuda")
+    dx_p = ops.linear_dx_int8(dyd, w8d, sd, rot, ws_p)
+    dx_m = ops.linear_dx_int8(dyd, w8d, sd, rot, ws_m)
+    torch.cuda.synchronize()
+    assert torch.equal(dx_p.view(torch.int16), dx_m.view(torch.int16))
+    # the block sums written by the quantizer match its own codes
+    codes = ws_p[:M * N * 2].view(torch.float16).view(M, N).float().cpu().numpy().astype(np.int64)
+    l1 = ws_p[minimum:minimum + M * 4 * 16].view(torch.int32).view(M, 16).cpu().numpy()
+    assert np.array_equal(l1, np.abs(codes).reshape(M, 16, 1024).sum(axis=2))
+    assert l1[:128].min() == 127 * 1024 and l1[128:].max() < 2 ** 17 // 4  # tile 0: 1-block chunks only
+    assert_bf16_parity(bf16_np(dx_p), O.linear_dx_int8(dy_b, w8, s, rot))
