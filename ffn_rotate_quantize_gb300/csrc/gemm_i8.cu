@@ -9,14 +9,13 @@
 //   * int8 values are exact in fp16, products (|p| <= 127^2) are exact, and an
 //     fp32 accumulator is exact while every partial sum stays below 2^24 in
 //     magnitude; 1024 products of magnitude <= 127^2 sum to < 2^24.
-//   * K is cut into chunks of 1024.  After each chunk the epilogue warps drain
-//     the fp32 accumulator (fp32 -> int32, exact) into int32 running totals
-//     held in their registers; the MMA resumes once the accumulator is read.
-//   * The accumulator is split into two N = 128 halves, each with its own
-//     epilogue warpgroup and barriers.  The MMA issuer keeps one cursor per
-//     half over the stream of 64-deep sub-steps and issues whichever half can
-//     go (the lagging one first, the leading one at most 7 sub-steps ahead), so
-//     while one half is being drained the other keeps the tensor pipe busy.
+//   * K is cut into exact chunks: 1024 long for any int8 data, or 2^j x 1024
+//     for a token tile whose rows' sums of |q| over those blocks allow it (the
+//     chunk plan below).  After each chunk the eight epilogue warps drain the
+//     fp32 accumulator (fp32 -> int32, exact) into int32 running totals held in
+//     their registers; the MMA of the next chunk starts once all of them have
+//     read it.  There is one N = 256 accumulator: with the weight's A ring it
+//     fills the 512 TMEM columns, so drains cannot be double-buffered.
 //
 // CTA pairs.  Two CTAs of a cluster share one 256 x 256 tile: the pair MMA
 // (tcgen05 cta_group::2, M = 256, N = 256) takes weight rows 128r..128r+127 from
