@@ -394,6 +394,10 @@ int gbq_dequant_weight(const int8_t *w8, const float *w_scale, void *w, int64_t 
         cudaError_t e = launch_scale_rows_s8(w8, w_scale, w, N, K, (cudaStream_t)stream);
         return e == cudaSuccess ? GBQ_OK : cuda_fail(e, "gbq_dequant_weight");
     }
+    if (logn == 6) {  // integer-exact two-pass kernel
+        cudaError_t e = launch_dequant_weight64(w8, w_scale, w, N, rot.groups, d->sms, (cudaStream_t)stream);
+        return e == cudaSuccess ? GBQ_OK : cuda_fail(e, "gbq_dequant_weight");
+    }
     RotArgs a{};
     a.in0 = w8;
     a.in_scale = w_scale;

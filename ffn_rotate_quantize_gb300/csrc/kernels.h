@@ -27,6 +27,9 @@ struct IdArgs {
 cudaError_t launch_rotq(int logn, int in_kind, int out_kind, RotArgs a, cudaStream_t st);   // OUT_S8 / OUT_F16Q
 cudaError_t launch_rotb(int logn, int in_kind, RotArgs a, cudaStream_t st);                 // OUT_BF16
 cudaError_t launch_quant_identity(int out_kind, IdArgs a, cudaStream_t st);
+// W_hat = bf16((W8 * s) R) for n = 64 (N rows of `groups` 4096-long groups), integer-exact transform.
+cudaError_t launch_dequant_weight64(const int8_t *w8, const float *w_scale, void *out, int64_t N, int groups,
+                                    int num_sms, cudaStream_t st);
 
 // Whether the rotate+quantize launch for this rotation fills RotArgs::out_l1 (the three-pass
 // kernels: n = 64 or 128, one group per row); elsewhere out_l1 is left untouched.

@@ -175,3 +175,25 @@ def test_dequant_weight_many_rows(ops, rot, N):
     w8, s = O.prepare_weight(wb, rot)
     w = ops.dequant_weight(torch.from_numpy(w8).cuda(), torch.from_numpy(s).cuda(), rot)
     assert_bf16_parity(bf16_np(w), O.dequant_weight(w8, s, rot))
+
+
+@pytest.mark.parametrize("rot,N", [((64, 64, 1), 1), ((64, 64, 1), 3041), ((64, 64, 3), 77)])
+def test_dequant_weight_power_of_two_scales_exact(ops, rot, N):
+    """With power-of-two row scales, (W8 s) R is exact in fp64 and in the integer transform, so the
+    bf16 result is the one rounding of the same exact value on both sides: identical bits."""
+    K = rot[0] * rot[1] * rot[2]
+    rng = np.random.default_rng(N + K)
+    w8 = rng.integers(-127, 128, (N, K)).astype(np.int8)
+    w8[0, :7] = 127
+    s = np.ldexp(np.float32(1.0), rng.integers(-14, -4, N)).astype(np.float32)
+    w = ops.dequant_weight(torch.from_numpy(w8).cuda(), torch.from_numpy(s).cuda(), rot)
+    assert np.array_equal(bf16_np(w), O.dequant_weight(w8, s, rot))
+
+
+@pytest.mark.parametrize("rot", [(64, 64, 2), (64, 64, 5)])
+def test_dequant_weight_grouped(ops, rot):
+    K = rot[0] * rot[1] * rot[2]
+    wb = I.bf16_bits(np.random.default_rng(K).standard_normal((61, K), dtype=np.float32) * np.float32(0.02))
+    w8, s = O.prepare_weight(wb, rot)
+    w = ops.dequant_weight(torch.from_numpy(w8).cuda(), torch.from_numpy(s).cuda(), rot)
+    assert_bf16_parity(bf16_np(w), O.dequant_weight(w8, s, rot))
