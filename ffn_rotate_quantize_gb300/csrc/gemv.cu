@@ -37,6 +37,7 @@ struct GemvArgs {
     uint32_t stage_bytes;   // rows_per_stage * K, multiple of 128
     uint32_t x_off, t_off, misc_off;
     uint32_t xb_off;        // bf16 staging of the M token rows (three-pass n = 64 path), else 0
+    uint32_t wrow_off;      // register-streaming kernel: staging of slice rows 16.. (0: rows 16.. via registers)
     unsigned int *status;
 };
 
@@ -240,15 +241,102 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(GemvArgs p) {
 
 // ---------------------------------------------------------------------------
 // Register-streaming variant for K = 4096, n = 64, one group, and at most 32
-// weight rows per CTA (4 per warp): every thread issues the loads of its share
-// of the CTA's weight slice at entry, straight into registers (streaming loads,
-// no shared-memory ring), so the whole slice is in flight while threads 0..127
-// rotate and quantize x; the dot products then read the weight from registers.
+// weight rows per CTA (4 per warp), launched with programmatic stream
+// serialization so that consecutive decode calls overlap:
+//   entry: every thread asks L2 for its share of the CTA's weight slice
+//     (prefetch.global.L2: a hint that moves no data into the thread, so it is
+//     safe on memory the kernel before may still write), then lets the next
+//     launch start and waits (griddepcontrol.wait) for the kernel before it;
+//     every read of an input comes after that wait.
+//   The kernel holds at most 128 registers per thread, so the next call's CTA
+//   fits beside this one on the SM: its L2 prefetch streams the next layer's
+//   weight from HBM while this layer computes.
+//   body: the x rows are bulk-copied and rotated + quantized by threads 0..127
+//     (the three-pass n = 64 transform, bit-identical codes to
+//     gbq_quantize_act) while every warp loads its first two weight rows into
+//     registers and one bulk copy brings the slice's rows 16.. (each warp's
+//     third and fourth rows) into shared memory, so the whole slice is in
+//     flight before the rotation starts.  When that staging does not fit two
+//     CTAs per SM (more than two tokens), the third and fourth rows are loaded
+//     into registers after the first two rows' dot products.
+// Without a preceding launch of this kind (or after a kernel that never
+// signals), the wait returns at once and the launch behaves like a plain one.
 constexpr int kDxK = 4096;
 constexpr int kDxChunks = kDxK / 16 / 32;  // 16-byte chunks per lane per row
 
+// Dot products of one weight row (held as this lane's 8 chunks) against the quantized tokens, the
+// warp reduction and the dequant epilogue (wsn, bn: the row's scale and bias, already loaded).
+__device__ __forceinline__ void gemv_row_dot(const GemvArgs &p, const uint4 (&w)[kDxChunks], const int8_t *xq,
+                                             const float *xs_s, int64_t n, int lane, float wsn, float bn) {
+    int acc[kGvMaxM] = {0, 0, 0, 0};
+#pragma unroll
+    for (int k = 0; k < kDxChunks; ++k) {
+#pragma unroll
+        for (int m = 0; m < kGvMaxM; ++m) {
+            if (m < p.M) {
+                const uint4 xv = reinterpret_cast<const uint4 *>(xq + (int64_t)m * kDxK)[lane + 32 * k];
+                acc[m] = __dp4a((int)w[k].x, (int)xv.x, acc[m]);
+                acc[m] = __dp4a((int)w[k].y, (int)xv.y, acc[m]);
+                acc[m] = __dp4a((int)w[k].z, (int)xv.z, acc[m]);
+                acc[m] = __dp4a((int)w[k].w, (int)xv.w, acc[m]);
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < kGvMaxM; ++m) {
+        if (m < p.M) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], o);
+        }
+    }
+    if (lane < p.M) {
+        int a = acc[0];
+#pragma unroll
+        for (int m = 1; m < kGvMaxM; ++m)
+            if (lane == m) a = acc[m];
+        const float tv = __fmul_rn(__int2float_rn(a), xs_s[lane]);
+        p.y[(int64_t)lane * p.N + n] = __float2bfloat16_rn(__fmaf_rn(tv, wsn, bn));
+    }
+}
+
+// One token (M = 1): the dot product of a weight row with the lane's eight code chunks xr, in four
+// independent dp4a chains; the lane's partial sum (the warp reduction follows).
+__device__ __forceinline__ int gemv_dot_m1(const uint4 (&w)[kDxChunks], const uint4 (&xr)[kDxChunks]) {
+    int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+#pragma unroll
+    for (int k = 0; k < kDxChunks; ++k) {
+        a0 = __dp4a((int)w[k].x, (int)xr[k].x, a0);
+        a1 = __dp4a((int)w[k].y, (int)xr[k].y, a1);
+        a2 = __dp4a((int)w[k].z, (int)xr[k].z, a2);
+        a3 = __dp4a((int)w[k].w, (int)xr[k].w, a3);
+    }
+    return (a0 + a1) + (a2 + a3);
+}
+
+// Warp sums of four per-lane values v[0..3] in six shuffles: afterwards lanes 8 q .. 8 q + 7 hold
+// the total of v[q] (a transposing reduction: halve the values held, then sum within 8 lanes).
+__device__ __forceinline__ int warp_sum4(const int (&v)[4], int lane) {
+    const bool hi = (lane >> 4) & 1;
+    const int s0 = __shfl_xor_sync(0xffffffffu, hi ? v[0] : v[2], 16);
+    const int s1 = __shfl_xor_sync(0xffffffffu, hi ? v[1] : v[3], 16);
+    const int k0 = (hi ? v[2] : v[0]) + s0;  // row 2 hi
+    const int k1 = (hi ? v[3] : v[1]) + s1;  // row 2 hi + 1
+    const bool b = (lane >> 3) & 1;
+    int t = (b ? k1 : k0) + __shfl_xor_sync(0xffffffffu, b ? k0 : k1, 8);
+    t += __shfl_xor_sync(0xffffffffu, t, 4);
+    t += __shfl_xor_sync(0xffffffffu, t, 2);
+    t += __shfl_xor_sync(0xffffffffu, t, 1);
+    return t;
+}
+
+__device__ __forceinline__ void gemv_load_row(uint4 (&w)[kDxChunks], const int8_t *w8, int64_t n, int lane) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(w8 + n * kDxK);
+#pragma unroll
+    for (int k = 0; k < kDxChunks; ++k) w[k] = __ldcs(src + lane + 32 * k);
+}
+
 template <int RPW>
-__global__ void __launch_bounds__(kGvThreads, 1) gemv_direct_kernel(GemvArgs p) {
+__global__ void __launch_bounds__(kGvThreads, 2) gemv_direct_kernel(GemvArgs p) {
     extern __shared__ __align__(128) uint8_t smem[];
     int8_t *xq = reinterpret_cast<int8_t *>(smem + p.x_off);
     float2 *T = reinterpret_cast<float2 *>(smem + p.t_off);
@@ -256,28 +344,46 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_direct_kernel(GemvArgs p) 
     float *wmax = xs_s + kGvMaxM;
     uint64_t *xfull = reinterpret_cast<uint64_t *>(wmax + kGvMaxM);
     int *abort_flag = reinterpret_cast<int *>(xfull + 1);
+    uint64_t *wfull = xfull + 2;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int64_t r0 = (int64_t)blockIdx.x * p.rows_per_cta;
     const int nrows = (int)(min(p.N, r0 + p.rows_per_cta) - r0);
+    const int wrows = p.wrow_off ? max(0, nrows - 16) : 0;  // slice rows 16.. staged in shared memory
 
+    // L2 prefetch of the slice (nrows * 4096 bytes, 128-byte lines), spread over the threads.
+    {
+        const char *base = reinterpret_cast<const char *>(p.w8 + r0 * kDxK);
+        for (int l = tid; l < nrows * (kDxK / 128); l += kGvThreads)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(base + (size_t)l * 128));
+        if (tid < nrows) asm volatile("prefetch.global.L2 [%0];" ::"l"(p.ws + r0 + tid));
+    }
+    pdl_allow_dependents();  // the next call may start and prefetch its weight
+    pdl_wait();              // every input may come from the kernel before
     if (tid == 0) {
         mbar_init(xfull, 1);
+        mbar_init(wfull, 1);
         *abort_flag = 0;
         fence_mbar_init();
         mbar_arrive_expect_tx(xfull, (uint32_t)(p.M * kDxK * 2));
         bulk_g2s(smem + p.xb_off, p.x, (uint32_t)(p.M * kDxK * 2), xfull);
+        if (wrows > 0) {
+            mbar_arrive_expect_tx(wfull, (uint32_t)wrows * kDxK);
+            bulk_g2s(smem + p.wrow_off, p.w8 + (r0 + 16) * kDxK, (uint32_t)wrows * kDxK, wfull);
+        }
     }
-    // This warp's rows j = warp + 8 q of the slice: issue every load now (they land while x is rotated).
-    uint4 wv[RPW][kDxChunks];
-#pragma unroll
-    for (int q = 0; q < RPW; ++q) {
-        const int j = warp + 8 * q;
-        const uint4 *src = reinterpret_cast<const uint4 *>(p.w8 + (r0 + (j < nrows ? j : 0)) * kDxK);
-#pragma unroll
-        for (int k = 0; k < kDxChunks; ++k) wv[q][k] = j < nrows ? __ldcs(src + lane + 32 * k) : make_uint4(0, 0, 0, 0);
+    // Lane q < RPW holds the scale and bias of row warp + 8 q (loaded now, off the epilogue's path).
+    float ws_l = 0.0f, b_l = 0.0f;
+    if (lane < RPW && warp + 8 * lane < nrows) {
+        ws_l = __ldg(p.ws + r0 + warp + 8 * lane);
+        if (p.bias) b_l = __bfloat162float(p.bias[r0 + warp + 8 * lane]);
     }
+    // This warp's rows j = warp + 8 q: the first two now (they land while x is rotated).
+    uint4 wa[kDxChunks], wb[kDxChunks];
+    const bool has0 = warp < nrows, has1 = RPW > 1 && warp + 8 < nrows;
+    if (has0) gemv_load_row(wa, p.w8, r0 + warp, lane);
+    if (has1) gemv_load_row(wb, p.w8, r0 + warp + 8, lane);
     __syncthreads();  // the x barrier is initialised
 
     // ---- rotate + quantize x: the three-pass n = 64 row transform on threads 0..127 ----
@@ -311,46 +417,86 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_direct_kernel(GemvArgs p) 
         }
     }
     __syncthreads();
-    if (*(volatile int *)abort_flag) return;
-
-    // ---- dot products from registers, dequant epilogue ----
-#pragma unroll
-    for (int q = 0; q < RPW; ++q) {
-        const int j = warp + 8 * q;
-        if (j >= nrows) break;
-        int acc[kGvMaxM] = {0, 0, 0, 0};
-#pragma unroll
-        for (int k = 0; k < kDxChunks; ++k) {
-            const uint4 w = wv[q][k];
-#pragma unroll
-            for (int m = 0; m < kGvMaxM; ++m) {
-                if (m < p.M) {
-                    const uint4 xv = reinterpret_cast<const uint4 *>(xq + (int64_t)m * kDxK)[lane + 32 * k];
-                    acc[m] = __dp4a((int)w.x, (int)xv.x, acc[m]);
-                    acc[m] = __dp4a((int)w.y, (int)xv.y, acc[m]);
-                    acc[m] = __dp4a((int)w.z, (int)xv.z, acc[m]);
-                    acc[m] = __dp4a((int)w.w, (int)xv.w, acc[m]);
-                }
+    // Copies in flight when a wait gave up land (bounded) before the CTA leaves.
+    auto drain = [&] {
+        if (tid == 0 && wrows > 0) {
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(wfull, 0) && globaltimer() - t0 < kWaitLimitNs) {
             }
         }
-#pragma unroll
-        for (int m = 0; m < kGvMaxM; ++m) {
-            if (m < p.M) {
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], o);
-            }
-        }
-        const int64_t n = r0 + j;
-        if (lane < p.M) {
-            int a = acc[0];
-#pragma unroll
-            for (int m = 1; m < kGvMaxM; ++m)
-                if (lane == m) a = acc[m];
-            const float b = p.bias ? __bfloat162float(p.bias[n]) : 0.0f;
-            const float tv = __fmul_rn(__int2float_rn(a), xs_s[lane]);
-            p.y[(int64_t)lane * p.N + n] = __float2bfloat16_rn(__fmaf_rn(tv, __ldg(p.ws + n), b));
-        }
+    };
+    if (*(volatile int *)abort_flag) {
+        drain();
+        return;
     }
+
+    // ---- dot products: rows 0, 1 from registers; rows 2, 3 from shared memory or, after the first
+    // two, from L2 into the same registers ----
+    auto wsq = [&](int q) { return __shfl_sync(0xffffffffu, ws_l, q); };
+    auto bq = [&](int q) { return __shfl_sync(0xffffffffu, b_l, q); };
+    const bool has2 = RPW > 2 && warp + 16 < nrows, has3 = RPW > 3 && warp + 24 < nrows;
+    auto smem_row = [&](uint4 (&w)[kDxChunks], int j) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(smem + p.wrow_off + (size_t)(j - 16) * kDxK);
+#pragma unroll
+        for (int k = 0; k < kDxChunks; ++k) w[k] = src[lane + 32 * k];
+    };
+    if (p.M == 1) {
+        // One token: the lane's codes stay in registers for all rows; one reduction for the four rows.
+        uint4 xr[kDxChunks];
+#pragma unroll
+        for (int k = 0; k < kDxChunks; ++k) xr[k] = reinterpret_cast<const uint4 *>(xq)[lane + 32 * k];
+        int part[4] = {0, 0, 0, 0};
+        if (has0) part[0] = gemv_dot_m1(wa, xr);
+        if (has1) part[1] = gemv_dot_m1(wb, xr);
+        if (has2 || has3) {
+            if (wrows > 0) {
+                if (!mbar_wait(wfull, 0, p.status, abort_flag)) {
+                    drain();
+                    return;
+                }
+                if (has2) smem_row(wa, warp + 16);
+                if (has3) smem_row(wb, warp + 24);
+            } else {
+                if (has2) gemv_load_row(wa, p.w8, r0 + warp + 16, lane);
+                if (has3) gemv_load_row(wb, p.w8, r0 + warp + 24, lane);
+            }
+            if (has2) part[2] = gemv_dot_m1(wa, xr);
+            if (has3) part[3] = gemv_dot_m1(wb, xr);
+        }
+        const int tot = warp_sum4(part, lane);
+        const int q = lane >> 3;
+        const float wsv = __shfl_sync(0xffffffffu, ws_l, q), bv = __shfl_sync(0xffffffffu, b_l, q);
+        if ((lane & 7) == 0 && q < RPW && warp + 8 * q < nrows) {
+            const float tv = __fmul_rn(__int2float_rn(tot), xs_s[0]);
+            p.y[r0 + warp + 8 * q] = __float2bfloat16_rn(__fmaf_rn(tv, wsv, bv));
+        }
+        if (wrows > 0 && !(has2 || has3)) {  // this warp had no staged rows: the copy still lands before exit
+            if (!mbar_wait(wfull, 0, p.status, abort_flag)) drain();
+        }
+        return;
+    }
+    if (has0) gemv_row_dot(p, wa, xq, xs_s, r0 + warp, lane, wsq(0), bq(0));
+    if (wrows > 0) {
+        if (has1) gemv_row_dot(p, wb, xq, xs_s, r0 + warp + 8, lane, wsq(1), bq(1));
+        if (!mbar_wait(wfull, 0, p.status, abort_flag)) {
+            drain();
+            return;
+        }
+        if (has2) {
+            smem_row(wa, warp + 16);
+            gemv_row_dot(p, wa, xq, xs_s, r0 + warp + 16, lane, wsq(2), bq(2));
+        }
+        if (has3) {
+            smem_row(wb, warp + 24);
+            gemv_row_dot(p, wb, xq, xs_s, r0 + warp + 24, lane, wsq(3), bq(3));
+        }
+        return;
+    }
+    if (has2) gemv_load_row(wa, p.w8, r0 + warp + 16, lane);
+    if (has1) gemv_row_dot(p, wb, xq, xs_s, r0 + warp + 8, lane, wsq(1), bq(1));
+    if (has3) gemv_load_row(wb, p.w8, r0 + warp + 24, lane);
+    if (has2) gemv_row_dot(p, wa, xq, xs_s, r0 + warp + 16, lane, wsq(2), bq(2));
+    if (has3) gemv_row_dot(p, wb, xq, xs_s, r0 + warp + 24, lane, wsq(3), bq(3));
 }
 
 // Launch the register-streaming kernel when the shape fits it; GBQ_ENOTSUP otherwise.
@@ -366,7 +512,17 @@ int launch_gemv_direct(const GemvArgs &base, int num_sms, cudaStream_t st) {
     a.t_off = (uint32_t)(((size_t)a.M * kDxK + 127) & ~(size_t)127);
     a.misc_off = a.t_off + ((fast_tile_bytes(6) + 127) & ~127u);
     a.xb_off = a.misc_off + 128;
-    const size_t smem = a.xb_off + (size_t)a.M * kDxK * 2;
+    size_t smem = a.xb_off + (size_t)a.M * kDxK * 2;
+    // Stage the slice's rows 16.. in shared memory when two CTAs still fit per SM.
+    a.wrow_off = 0;
+    if (rpc > 16) {
+        const size_t off = (smem + 127) & ~(size_t)127;
+        const size_t with = off + (size_t)(rpc - 16) * kDxK;
+        if (2 * (with + 1024) <= 228 * 1024) {
+            a.wrow_off = (uint32_t)off;
+            smem = with;
+        }
+    }
     static bool attr[5] = {false, false, false, false, false};
     auto kern = rpw == 1 ? gemv_direct_kernel<1> : rpw == 2 ? gemv_direct_kernel<2>
               : rpw == 3 ? gemv_direct_kernel<3> : gemv_direct_kernel<4>;
@@ -375,10 +531,20 @@ int launch_gemv_direct(const GemvArgs &base, int num_sms, cudaStream_t st) {
             return gbq_fail(GBQ_ECUDA, "gemv: cannot set shared memory size");
         attr[rpw] = true;
     }
+    cudaLaunchAttribute lattr[1];
+    lattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    lattr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = st;
+    cfg.attrs = lattr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kGvThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
     prof_begin(3, st);
-    kern<<<(unsigned)grid, kGvThreads, smem, st>>>(a);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
     prof_end(st);
-    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? GBQ_OK : gbq_fail(GBQ_ECUDA, cudaGetErrorString(e));
 }
 

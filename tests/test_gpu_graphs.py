@@ -95,3 +95,47 @@ def test_graph_ffn_and_dx_int8(ops, M):
         (lambda out: ops.ffn_fused(x, *t, rd, rh, wsf, out=out), yf),
         (lambda out: ops.linear_dx_int8(dy, t[4], t[5], rh, wsx, out=out), dx),
     ])
+
+
+@pytest.mark.parametrize("M,K,rot", [(1, 4096, (64, 64, 1)), (3, 4096, (64, 64, 1)), (2, 1024, (32, 32, 1))])
+def test_decode_chain_back_to_back(ops, M, K, rot):
+    """Stacked decode layers, each reading the previous layer's output as its x, launched back to
+    back (the GEMV waits for the kernel before it while the next call's weight prefetch runs beside
+    it) give the bits of the same calls with a device synchronisation after each, and of a graph
+    replay of the chain."""
+    L, NW = 12, 4
+    ws_, w8s = [], []
+    for k in range(NW):
+        c = I.linear_case(M, K, K, n_outliers=I.outlier_count(K), outlier_scale=30.0, seed=100 + k)
+        w8, s = ops.prepare_weight(bf16_dev(c["w"]), rot)
+        w8s.append(w8)
+        ws_.append(s)
+    x0 = bf16_dev(I.linear_case(M, K, 8, n_outliers=I.outlier_count(K), outlier_scale=30.0, seed=7)["x"])
+    work = torch.empty(max(ops.workspace_size(ops.OP_LINEAR, M, K, K), 256), dtype=torch.uint8, device="cuda")
+
+    def run(sync):
+        bufs = [x0] + [torch.empty((M, K), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+        for i in range(L):
+            ops.linear(bufs[i], w8s[i % NW], ws_[i % NW], None, rot, workspace=work, out=bufs[i + 1])
+            if sync:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        return bufs
+
+    ref = run(True)
+    got = run(False)
+    for i in range(1, L + 1):
+        assert torch.equal(ref[i].view(torch.int16), got[i].view(torch.int16)), f"layer {i}"
+    assert torch.isfinite(ref[L].float()).all()
+    bufs = [x0] + [torch.empty((M, K), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(L):
+            ops.linear(bufs[i], w8s[i % NW], ws_[i % NW], None, rot, workspace=work, out=bufs[i + 1])
+    for _ in range(2):
+        for b in bufs[1:]:
+            b.fill_(0)
+        g.replay()
+        torch.cuda.synchronize()
+        for i in range(1, L + 1):
+            assert torch.equal(ref[i].view(torch.int16), bufs[i].view(torch.int16)), f"graph layer {i}"
