@@ -358,14 +358,17 @@ def run_ours(args):
         ach = DECODE_BYTES / (gv_ms * 1e-3) * 1e-9
         graph_ms = graph_batch_ms(torch, flush, decode_chain, reps=32)
         ach_g = DECODE_BYTES / (graph_ms * 1e-3) * 1e-9
-        dec = {"bound": "hbm", "kernel": "gemv_direct_kernel (decode 1x4096x4096, consecutive calls overlapped)",
-               "achieved": round(ach, 1),
-               "peak": peaks["hbm"], "unit": "GB/s", "frac": round(ach / peaks["hbm"], 4), "ms": round(gv_ms, 4),
+        # Decode is served from CUDA graphs: the primary figure is the replay of the captured chain (host
+        # launch overhead out of the timed region; device-side gaps and the per-layer dependency stay in).
+        # The eager chain is reported beside it: from Python it is bound by the host's launch rate.
+        dec = {"bound": "hbm", "kernel": "gemv_direct_kernel (decode 1x4096x4096)",
+               "achieved": round(ach_g, 1), "peak": peaks["hbm"], "unit": "GB/s",
+               "frac": round(ach_g / peaks["hbm"], 4), "ms": round(graph_ms, 4),
                "traffic": profiled_traffic("gemv_direct_kernel"),
-               "chain": "32 dependent layers: call i's x is call i-1's y",
-               "graph": {"ms": round(graph_ms, 4), "achieved": round(ach_g, 1),
-                         "frac": round(ach_g / peaks["hbm"], 4),
-                         "note": "the same 32 calls captured in one CUDA graph, replayed under one event pair"}}
+               "mode": "CUDA-graph replay of 32 dependent decode layers (call i's x is call i-1's y; 16 weight "
+                       "copies, 268 MB), one event pair",
+               "eager": {"ms": round(gv_ms, 4), "achieved": round(ach, 1), "frac": round(ach / peaks["hbm"], 4),
+                         "note": "the same chain launched from Python, one event pair (host launch rate bound)"}}
 
     out = {
         "metric": METRIC, "value": None if value is None else round(value, 2), "unit": "TOPS", "n_gpus": world, "steps": args.steps,

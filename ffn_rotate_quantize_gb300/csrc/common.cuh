@@ -141,11 +141,6 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *map, uin
 
 // Untiled bulk copies (both addresses 16-byte aligned, size a multiple of 16).
 // Global -> shared, completing `bytes` of transaction count on `bar`.
-// Hint: bring [src, src + bytes) into L2 (16-byte aligned, bytes a multiple of 16).  No data reaches
-// the thread, so it is safe on memory that an earlier kernel may still be writing.
-__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      smem_u32(dst)),

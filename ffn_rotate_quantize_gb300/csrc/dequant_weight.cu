@@ -56,6 +56,11 @@ __device__ __forceinline__ void h4_pairs(float2 &x0, float2 &x1, float2 &x2, flo
     x3 = y3;
 }
 
+// Hint: bring [src, src + bytes) into L2 (16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Word offset (fp32 units) of X[i][j] in the swizzled tile.
 __device__ __forceinline__ int dqw_tile_off(int i, int j) {
     const int c = j >> 2;
