@@ -368,10 +368,6 @@ __global__ void __launch_bounds__(kGvThreads, 2) gemv_direct_kernel(GemvArgs p) 
         fence_mbar_init();
         mbar_arrive_expect_tx(xfull, (uint32_t)(p.M * kDxK * 2));
         bulk_g2s(smem + p.xb_off, p.x, (uint32_t)(p.M * kDxK * 2), xfull);
-        if (wrows > 0) {
-            mbar_arrive_expect_tx(wfull, (uint32_t)wrows * kDxK);
-            bulk_g2s(smem + p.wrow_off, p.w8 + (r0 + 16) * kDxK, (uint32_t)wrows * kDxK, wfull);
-        }
     }
     // Lane q < RPW holds the scale and bias of row warp + 8 q (loaded now, off the epilogue's path).
     float ws_l = 0.0f, b_l = 0.0f;
@@ -379,18 +375,25 @@ __global__ void __launch_bounds__(kGvThreads, 2) gemv_direct_kernel(GemvArgs p) 
         ws_l = __ldg(p.ws + r0 + warp + 8 * lane);
         if (p.bias) b_l = __bfloat162float(p.bias[r0 + warp + 8 * lane]);
     }
-    // This warp's rows j = warp + 8 q: the first two now (they land while x is rotated).
+    __syncthreads();  // the barriers are initialised
+    // The x copy goes first (the rotation waits on it); the weight requests follow once it has landed
+    // and arrive while x is rotated: this warp's rows j = warp + 8 q, the first two into registers,
+    // the slice's rows 16.. into shared memory.
+    const bool xok = mbar_wait(xfull, 0, p.status, abort_flag);
+    if (tid == 0 && wrows > 0 && xok) {
+        mbar_arrive_expect_tx(wfull, (uint32_t)wrows * kDxK);
+        bulk_g2s(smem + p.wrow_off, p.w8 + (r0 + 16) * kDxK, (uint32_t)wrows * kDxK, wfull);
+    }
     uint4 wa[kDxChunks], wb[kDxChunks];
     const bool has0 = warp < nrows, has1 = RPW > 1 && warp + 8 < nrows;
     if (has0) gemv_load_row(wa, p.w8, r0 + warp, lane);
     if (has1) gemv_load_row(wb, p.w8, r0 + warp + 8, lane);
-    __syncthreads();  // the x barrier is initialised
 
     // ---- rotate + quantize x: the three-pass n = 64 row transform on threads 0..127 ----
     if (tid < 128) {
         auto bar = [] { named_bar_sync(1, 128); };
         RotArgs ra{};
-        const bool ok = named_bar_and(1, 128, mbar_wait(xfull, 0, p.status, abort_flag));
+        const bool ok = named_bar_and(1, 128, xok);
         for (int m = 0; m < p.M && ok; ++m) {
             const uint8_t *xb = smem + p.xb_off + (size_t)m * kDxK * 2;
             float2 v[16];
@@ -410,16 +413,17 @@ __global__ void __launch_bounds__(kGvThreads, 2) gemv_direct_kernel(GemvArgs p) 
             store_codes<OUT_S8, 4>(xq, (int64_t)m * kDxK + 128 * r + 64 + 16 * jq, words[1]);
             bar();  // the tile and the amax slots are free for the next token
         }
-        if (!ok && tid == 0) {  // the x copy never landed: let it finish (bounded) before leaving
+    }
+    __syncthreads();
+    // Copies in flight when a wait gave up land (bounded) before the CTA leaves: x (if its wait gave
+    // up) and the staged weight rows (issued only after x landed).
+    auto drain = [&] {
+        if (tid == 0 && !xok) {
             const uint64_t t0 = globaltimer();
             while (!mbar_try_wait(xfull, 0) && globaltimer() - t0 < kWaitLimitNs) {
             }
         }
-    }
-    __syncthreads();
-    // Copies in flight when a wait gave up land (bounded) before the CTA leaves.
-    auto drain = [&] {
-        if (tid == 0 && wrows > 0) {
+        if (tid == 0 && wrows > 0 && xok) {
             const uint64_t t0 = globaltimer();
             while (!mbar_try_wait(wfull, 0) && globaltimer() - t0 < kWaitLimitNs) {
             }
