@@ -29,7 +29,8 @@ def d(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
-DX_CASES = [(200, 2048, 1024, (32, 32, 1)), (64, 16384, 256, (16, 16, 1)), (129, 1024, 4096, (64, 64, 1))]
+DX_CASES = [(200, 2048, 1024, (32, 32, 1)), (64, 16384, 256, (16, 16, 1)), (129, 1024, 4096, (64, 64, 1)),
+            (700, 16384, 256, (16, 16, 1)), (160, 12288, 512, (16, 16, 2))]
 
 
 @pytest.mark.parametrize("M,N,K,rot", DX_CASES)

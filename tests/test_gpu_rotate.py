@@ -197,3 +197,18 @@ def test_dequant_weight_grouped(ops, rot):
     w8, s = O.prepare_weight(wb, rot)
     w = ops.dequant_weight(torch.from_numpy(w8).cuda(), torch.from_numpy(s).cuda(), rot)
     assert_bf16_parity(bf16_np(w), O.dequant_weight(w8, s, rot))
+
+
+@pytest.mark.parametrize("K,M", [(16384, 1000), (10000, 157), (8200, 3)])
+def test_quantize_act_identity_long_rows_exact(ops, K, M):
+    """R = I on long rows (persistent CTAs stream the rows through shared-memory stages; the ring wraps
+    for M = 1000): the values are the bf16 inputs themselves, so scales and codes equal the oracle's
+    exactly, including a zero row and a row of tiny values."""
+    xb = _x(M, K, seed=M + K, outliers=max(1, K // 100))
+    xb[0] = 0
+    if M > 2:
+        xb[2] = I.bf16_bits(np.full(K, 1e-30, np.float32) * np.sign(np.random.default_rng(K).standard_normal(K)))
+    q, s = ops.quantize_act(bf16_dev(xb), (1, 1, K))
+    qr, sr, _ = _oracle_q(xb, (1, 1, K))
+    assert np.array_equal(s.cpu().numpy(), sr)
+    assert np.array_equal(q.cpu().numpy(), qr)
