@@ -14,7 +14,8 @@ synthetic workload (shapes and distributions of the method's configurations):
   rotated bf16     the page's fair comparator on the prefill shape: rotate-only kernel on x,
                    then a bf16 linear against the pre-rotated bf16 weight (+ bias); the
                    line reports the int8 layer's speedup over it
-Inputs are resident in HBM; L2 is flushed (a 512 MB write) before every timed
+Inputs are resident in HBM; L2 is flushed (a 512 MB write, then a read of the
+same buffer so that its dirty lines are written back too) before every timed
 operation, outside its CUDA-event window.  `value` is the prefill linear's
 throughput 2*M*N*K / t.  The int8 contraction runs exactly on the f16 tensor
 pipe (sm_103a has no int8 MMA kind), so its roofline peak is the measured dense
@@ -267,7 +268,7 @@ def run_ours(args):
 
     def step(i, timed):
         for name, fn in ops:
-            flush.zero_()
+            flush_l2(flush)
             if timed:
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
@@ -375,7 +376,8 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(step_ms, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8", "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": M3, "N": N3, "K": K3, "rotation": "H64(x)H64/64",
-                   "l2": "step: flushed before every timed op (512 MB write); roofline kernels: back-to-back "
+                   "l2": "step: flushed before every timed op (512 MB write, then a read of it that evicts the "
+                         "dirty lines); roofline kernels: back-to-back "
                          "launches cycling inputs larger than L2 (4 prefill / 16 decode weight copies)",
                    "parallelism": f"replicas x{world}"},
         "roofline": roof, "decode_roofline": dec, "rows": rows, "gpu_launches": launches,
@@ -394,13 +396,22 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def flush_l2(flush):
+    """Write a buffer larger than L2 (512 MB), then read it back: the read evicts the write's dirty lines
+    (written back outside any timed window), so the next op starts from a clean L2 holding none of its
+    inputs and pays for no one else's write-back."""
+    import torch
+    flush.zero_()
+    flush.view(torch.int32).sum()
+
+
 def batch_ms(torch, flush, fn, reps=32):
     """Average duration of fn(i) launched reps times back to back on the current stream, one CUDA
     event pair around the batch (for single-kernel ops, whose per-launch events would add gaps).
     fn(i) must cycle through inputs whose total exceeds the L2 cache."""
     fn(0)
     torch.cuda.synchronize()
-    flush.zero_()
+    flush_l2(flush)
     st = torch.cuda.current_stream()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -423,7 +434,7 @@ def graph_batch_ms(torch, flush, fn, reps=32):
             fn(i)
     g.replay()  # first replay uploads the graph
     torch.cuda.synchronize()
-    flush.zero_()
+    flush_l2(flush)
     st = torch.cuda.current_stream()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -444,7 +455,7 @@ def kernel_ms(G, torch, flush, kind, fn, reps=10):
     through inputs whose total exceeds the L2 cache, so no call finds its operands there."""
     fn(0)  # warm-up (first-launch set-up outside the measurement)
     torch.cuda.synchronize()
-    flush.zero_()
+    flush_l2(flush)
     G.prof_enable(True)
     for i in range(reps):
         fn(i)
@@ -464,7 +475,7 @@ def measure_e2e(G, torch, dev, x3, w83, s3, b3, ws_lin, args):
     st = torch.cuda.current_stream()
     times = []
     for i in range(args.warmup + args.steps):
-        flush.zero_()
+        flush_l2(flush)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(st)

@@ -205,3 +205,16 @@ def test_linear_acc_chunk_plans_exact(ops):
     acc2, _ = ops.linear_acc(bf16_dev(x2), d(w2), rot2)
     q2, _ = ops.quantize_act(bf16_dev(x2), rot2)
     assert np.array_equal(acc2.cpu().numpy().astype(np.int64), O.gemm_s8(q2.cpu().numpy(), w2))
+
+
+@pytest.mark.parametrize("M,N,with_bias", [(70000, 16, True), (33, 100, True), (5, 2051, False), (300, 14336, True)])
+def test_dequant_shapes(ops, M, N, with_bias):
+    """The 8-column kernel (including rows striding past the 65535 grid rows) and the 4- and 1-column
+    kernels (N not a multiple of 8) compute the oracle's fp32 operations: identical bits."""
+    rng = np.random.default_rng(M + N)
+    acc = rng.integers(-2 ** 27, 2 ** 27, (M, N)).astype(np.int32)
+    xs = (rng.random(M) * 1e-4).astype(np.float32)
+    ws = (rng.random(N) * 1e-3).astype(np.float32)
+    bias = I.bf16_bits(rng.standard_normal(N).astype(np.float32) * 0.01) if with_bias else None
+    y = ops.dequant(d(acc), d(xs), d(ws), bf16_dev(bias) if with_bias else None)
+    assert np.array_equal(bf16_np(y), O.dequant(acc.astype(np.int64), xs, ws, bias))
