@@ -172,6 +172,12 @@ int gbq_dequant(const int32_t *acc, int64_t ld_acc, const float *x_scale,
  * [..,N]); rotate+quantize, int8 GEMM and the dequant epilogue fused in the
  * GEMM.  Bit-identical to gbq_dequant(gbq_linear_acc(x)).  M = 1..4 runs the
  * decode GEMV path (weight streaming) for a = b <= 64.  Workspace: GBQ_OP_LINEAR.
+ * At K = 4096 (a = b = 64, one group) the decode kernel is launched with
+ * programmatic stream serialization: it may start while the kernel before it on
+ * the stream is still running, but reads none of its inputs (x, w8, w_scale,
+ * bias) before that kernel has completed, so x may be that kernel's output;
+ * consecutive decode calls overlap (the next one's weight is fetched into L2
+ * meanwhile).  Results do not depend on the overlap.
  */
 int gbq_linear(const void *x, const int8_t *w8, const float *w_scale, const void *bias,
                void *y, int64_t M, int64_t N, int64_t K, gbq_rot rot, void *workspace,
