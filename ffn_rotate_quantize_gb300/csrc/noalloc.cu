@@ -64,6 +64,9 @@ extern "C" int gbq_linear_noalloc(const void *x, const int8_t *w8, const float *
                  (long long)M, (long long)K, need, kNoAllocScratchBytes);
         return gbq::gbq_fail(GBQ_ENOSPC, msg);
     }
+    // An empty batch needs no scratch: gbq_linear checks the arguments and launches nothing, as for
+    // every other entry point (no device work at all, so it also holds where no device is present).
+    if (M == 0) return gbq_linear(x, w8, w_scale, bias, y, M, N, K, rot, nullptr, 0, stream);
     void *scratch = nullptr;
     int rc = scratch_address(&scratch);
     if (rc != GBQ_OK) return rc;

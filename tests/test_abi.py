@@ -83,3 +83,34 @@ def test_no_device_reported(lib):
     p = ctypes.c_void_p(256)
     rc = lib.gbq_quantize_act(p, p, p, 4, 256, R(16, 16, 1), None)
     assert rc == -19 and _err(lib)
+
+
+def test_every_entry_point_accepts_empty_inputs(lib):
+    """An empty batch (M = 0, or N = 0 for the weight calls) is valid for every entry point: it returns 0
+    and launches nothing, before any device work (so it holds on a machine without a GPU too), with
+    valid-looking or null pointers (an empty tensor may report a null data pointer)."""
+    for p in (ctypes.c_void_p(256), None):
+        _check_empty_calls(lib, p)
+
+
+def _check_empty_calls(lib, p):
+    r1, r2 = R(16, 16, 1), R(64, 64, 1)
+    calls = {
+        "quantize_act": lambda: lib.gbq_quantize_act(p, p, p, 0, 256, r1, None),
+        "quantize_act_glu": lambda: lib.gbq_quantize_act_glu(p, p, p, p, 0, 256, r1, None),
+        "dequant_act_quantize": lambda: lib.gbq_dequant_act_quantize(p, p, 256, p, p, p, p, p, 0, 256, r1, None),
+        "prepare_weight": lambda: lib.gbq_prepare_weight(p, p, p, 0, 256, r1, None),
+        "int8_gemm": lambda: lib.gbq_int8_gemm(p, p, p, 64, 0, 64, 256, p, 1 << 20, None),
+        "linear_acc": lambda: lib.gbq_linear_acc(p, p, p, 64, p, 0, 64, 256, r1, p, 1 << 20, None),
+        "dequant": lambda: lib.gbq_dequant(p, 64, p, p, None, p, 64, 0, 64, None),
+        "linear": lambda: lib.gbq_linear(p, p, p, None, p, 0, 64, 256, r1, None, 0, None),
+        "ffn_fused": lambda: lib.gbq_ffn_fused(p, p, p, p, p, p, p, p, 0, 4096, 4096, r2, r2, None, 0, None),
+        "dequant_weight": lambda: lib.gbq_dequant_weight(p, p, p, 0, 256, r1, None),
+        "linear_dx": lambda: lib.gbq_linear_dx(p, p, p, 0, 256, 256, None),
+        "linear_bf16": lambda: lib.gbq_linear_bf16(p, p, None, p, 0, 64, 256, None),
+        "linear_dx_int8": lambda: lib.gbq_linear_dx_int8(p, p, p, p, 0, 1024, 256, r1, None, 0, None),
+        "rotate_bf16": lambda: lib.gbq_rotate_bf16(p, p, 0, 256, r1, None),
+        "linear_noalloc": lambda: lib.gbq_linear_noalloc(p, p, p, None, p, 0, 64, 256, r1, None),
+    }
+    failed = {name: (rc, _err(lib)) for name, call in calls.items() if (rc := call()) != 0}
+    assert not failed, failed
