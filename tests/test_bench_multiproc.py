@@ -1,0 +1,57 @@
+"""The N > 1 bench path on CPU: replicas report the maximum elapsed time over ranks and the sum of the
+units all ranks processed (weak scaling), through a world-size-2 gloo group on 127.0.0.1."""
+import os
+import socket
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ws, r, local = bench.dist_info()
+        ms, units = bench.aggregate(1.0 + rank, 100.0 * (rank + 1), ws)
+        out[rank] = (ws, r, local, ms, units)
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2])
+def test_replicas_aggregate_max_time_and_summed_units(world):
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.start_processes(_rank, args=(world, port, out), nprocs=world, start_method="spawn", join=True)
+        res = dict(out)
+    for rank in range(world):
+        ws, r, local, ms, units = res[rank]
+        assert (ws, r, local) == (world, rank, rank)
+        assert ms == float(world)                                   # the slowest rank's time
+        assert units == 100.0 * world * (world + 1) / 2             # all ranks' units
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    """Under a multi-rank launch the reference arm (the CPU oracle) runs on rank 0 alone; the other ranks
+    exit 0 without work or output."""
+    import subprocess
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1", MASTER_ADDR="127.0.0.1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1"],
+                       env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
