@@ -111,12 +111,13 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.lines = []  # (arrival time, csv line)
+        self.window = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -125,7 +126,11 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def mark(self, t0: float, t1: float):
+        """The host-time window of the timed region (samples arriving in it are the ones reported)."""
+        self.window = (t0, t1)
 
     def stop(self):
         if self.proc is None:
@@ -138,7 +143,12 @@ class ClockSampler:
         self.thread.join(timeout=2)
         sm, mx, reasons = [], 0.0, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        lines, scope = [ln for _, ln in self.lines], "all samples (none arrived during the timed steps)"
+        if self.window is not None:
+            inside = [ln for t, ln in self.lines if self.window[0] <= t <= self.window[1] + 0.06]
+            if inside:
+                lines, scope = inside, "samples arriving during the timed steps"
+        for ln in lines:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 8:
                 continue
@@ -152,7 +162,8 @@ class ClockSampler:
                     reasons.add(n)
         if not sm:
             return None
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm),
+                "window": scope}
 
 
 # ---------------------------------------------------------------------------------------------
@@ -304,11 +315,13 @@ def run_ours(args):
     torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    h0 = time.monotonic()
     t_start.record(stream)
     for i in range(args.steps):
         step(i, True)
     t_end.record(stream)
     torch.cuda.synchronize()
+    clocks.mark(h0, time.monotonic())
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
