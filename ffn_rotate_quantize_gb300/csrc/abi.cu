@@ -40,6 +40,11 @@ struct DevState {
     unsigned int *status = nullptr;
     int sms = 0;
     char name[256] = "";
+    // A second stream and fork/join events for work the library splits over two streams (created once);
+    // fork_mu keeps one call's record/wait sequence from interleaving with another's.
+    cudaStream_t aux = nullptr;
+    cudaEvent_t ev_fork = nullptr, ev_join = nullptr, ev_entry = nullptr, ev_zero = nullptr;
+    std::mutex fork_mu;
 };
 constexpr int kMaxDevices = 64;
 DevState g_dev[kMaxDevices];
@@ -76,6 +81,12 @@ int init_current(DevState **out) {
                 return fail(GBQ_ECUDA, "cuTensorMapEncodeTiled entry point unavailable");
             g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
         }
+        e = cudaStreamCreateWithFlags(&d.aux, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.ev_fork, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.ev_join, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.ev_entry, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.ev_zero, cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(e, "creating the library's auxiliary stream");
         d.status = static_cast<unsigned int *>(p);
         d.sms = prop.multiProcessorCount;
         snprintf(d.name, sizeof(d.name), "%s", prop.name);
@@ -688,29 +699,91 @@ int gbq_linear_dx_int8(const void *dy, const int8_t *w8, const float *w_scale, v
     float *t = (float *)w.take((size_t)M * 4);
     float *dxr = (float *)w.take((size_t)M * K * 4);
     int32_t *l1 = (int32_t *)w.take((size_t)M * 4 * ((N + 1023) / 1024));  // block L1 norms: preferred size only
+    if (logn == 0) return fail(GBQ_ENOTSUP, "gbq_linear_dx_int8: identity rotation not supported");
+    // A long contraction splits in two halves run side by side on two streams, each GEMM on half the CTA
+    // pairs: the 256 x 256 tiles then fill the SMs in about twice as many waves of half-length tiles
+    // (M = K = 4096: 6.7 waves of halves against 3.4 of whole tiles, whose last wave leaves most SMs idle).
+    // Each half adds its exact int32 sums into the (zeroed) accumulator; the rotation applies t[m].
+    const bool split = N >= 8192 && N % 2048 == 0;
+    int32_t *acc = reinterpret_cast<int32_t *>(dxr);  // the same workspace bytes, read as int32 when split
+    cudaError_t e;
+    std::unique_lock<std::mutex> fork_lock(d->fork_mu, std::defer_lock);
+    if (split) {
+        // The accumulator is cleared on the second stream while the quantizer runs on this one (after
+        // everything enqueued on this stream before the call, which may still use the workspace).
+        fork_lock.lock();
+        e = cudaEventRecord(d->ev_entry, st);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(d->aux, d->ev_entry, 0);
+        if (e == cudaSuccess) e = cudaMemsetAsync(acc, 0, (size_t)M * K * 4, d->aux);
+        if (e == cudaSuccess) e = cudaEventRecord(d->ev_zero, d->aux);
+        if (e != cudaSuccess) return cuda_fail(e, "gbq_linear_dx_int8 (clear the accumulator)");
+    }
     // 1) dy' = dy * s[n] (column scale), per-row quantize, no rotation
     IdArgs ia{dy, w_scale, N, qd, t, M, N, l1};
-    cudaError_t e = launch_quant_identity(OUT_F16Q, ia, st);
-    if (e != cudaSuccess) return cuda_fail(e, "gbq_linear_dx_int8 (quantize dy)");
-    // 2) acc[m, k] = sum_n qd[m, n] w8[n, k]; dx_rot = fp32(acc) * t[m]
-    I8GemmProblem g = gemm_problem(d, qd, w8, M, K, N, EPI_ROWSCALE_F32, dxr, K, t, nullptr, nullptr);
-    g.w_layout = W_NMAJOR;
-    g.ld_w = K;
-    g.w_rows_total0 = N;
-    g.w_rows_total1 = N;
-    g.row_l1 = l1;
-    g.pdl = 1;  // directly after the quantizer launch
-    rc = launch_i8gemm(g, st);
-    if (rc) return rc;
-    // 3) dx = bf16(dx_rot R)
-    if (logn == 0) return fail(GBQ_ENOTSUP, "gbq_linear_dx_int8: identity rotation not supported");
+    e = launch_quant_identity(OUT_F16Q, ia, st);
+    if (e != cudaSuccess) {
+        if (split) (void)cudaStreamWaitEvent(st, d->ev_zero, 0);  // the caller's stream stays after the clear
+        return cuda_fail(e, "gbq_linear_dx_int8 (quantize dy)");
+    }
     RotArgs a{};
-    a.in0 = dxr;
     a.ld_in = K;
     a.out = dx;
     a.M = M;
     a.K = K;
-    return run_rotq("gbq_linear_dx_int8 (rotate dx)", rot, logn, IN_F32, OUT_BF16, a, st);
+    if (!split) {
+        // 2) acc[m, k] = sum_n qd[m, n] w8[n, k]; dx_rot = fp32(acc) * t[m]
+        I8GemmProblem g = gemm_problem(d, qd, w8, M, K, N, EPI_ROWSCALE_F32, dxr, K, t, nullptr, nullptr);
+        g.w_layout = W_NMAJOR;
+        g.ld_w = K;
+        g.w_rows_total0 = N;
+        g.w_rows_total1 = N;
+        g.row_l1 = l1;
+        g.pdl = 1;  // directly after the quantizer launch
+        rc = launch_i8gemm(g, st);
+        if (rc) return rc;
+        // 3) dx = bf16(dx_rot R)
+        a.in0 = dxr;
+        return run_rotq("gbq_linear_dx_int8 (rotate dx)", rot, logn, IN_F32, OUT_BF16, a, st);
+    }
+    // 2) acc[m, k] += sum over each half of n of qd[m, n] w8[n, k], the halves on two streams
+    const int64_t nh = N / 2;
+    const int nb = (int)((N + 1023) / 1024);
+    int half_pairs = i8gemm_max_pairs(d->sms) / 2;
+    if (half_pairs < 1) half_pairs = 1;
+    I8GemmProblem g0 = gemm_problem(d, qd, w8, M, K, nh, EPI_ACC_I32, acc, K, nullptr, nullptr, nullptr);
+    g0.w_layout = W_NMAJOR;
+    g0.ld_w = K;
+    g0.w_rows_total0 = nh;
+    g0.w_rows_total1 = nh;
+    g0.ld_b = N;
+    g0.row_l1 = l1;
+    g0.l1_ld = nb;
+    g0.reduce_out = 1;
+    g0.max_pairs = half_pairs;
+    g0.pdl = 0;  // the fork's event record sits between the quantizer and this launch
+    I8GemmProblem g1 = g0;
+    g1.b_f16 = reinterpret_cast<const uint16_t *>(qd) + nh;
+    g1.w0 = w8 + nh * K;
+    g1.w1 = g1.w0;
+    g1.row_l1 = l1 ? l1 + nh / 1024 : nullptr;
+    {
+        e = cudaEventRecord(d->ev_fork, st);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(d->aux, d->ev_fork, 0);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(st, d->ev_zero, 0);
+        if (e != cudaSuccess) return cuda_fail(e, "gbq_linear_dx_int8 (fork)");
+        rc = launch_i8gemm(g0, st);
+        if (rc == GBQ_OK) rc = launch_i8gemm(g1, d->aux);
+        // the join is recorded even after a failed launch, so that the auxiliary stream never runs ahead
+        e = cudaEventRecord(d->ev_join, d->aux);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(st, d->ev_join, 0);
+        fork_lock.unlock();
+        if (rc) return rc;
+        if (e != cudaSuccess) return cuda_fail(e, "gbq_linear_dx_int8 (join)");
+    }
+    // 3) dx = bf16((fp32(acc) * t[m]) R)
+    a.in0 = acc;
+    a.in_scale = t;
+    return run_rotq("gbq_linear_dx_int8 (rotate dx)", rot, logn, IN_ACC_ROWSCALE, OUT_BF16, a, st);
 }
 
 }  // extern "C"

@@ -160,6 +160,14 @@ __device__ __forceinline__ void tma_store_2d(const void *map, const void *smem_s
                  "r"(y), "r"(smem_u32(smem_src))
                  : "memory");
 }
+// Element-wise add of a shared-memory box into global memory through a tensor map (the map's element
+// type; int32 here: an exact reduction).  Same bulk-group completion as tma_store_2d.
+__device__ __forceinline__ void tma_reduce_add_2d(const void *map, const void *smem_src, int x, int y) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     map),
+                 "r"(x), "r"(y), "r"(smem_u32(smem_src))
+                 : "memory");
+}
 __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void tma_store_wait_read() {

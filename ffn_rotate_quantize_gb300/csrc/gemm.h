@@ -43,10 +43,17 @@ struct I8GemmProblem {
     const int32_t *row_l1;    // optional [M][K/1024]: sum of |q| over each 1024-long block of a token row
     int pdl;                  // launch so the kernel may start while the preceding (quantizer) kernel runs:
                               // it reads the tokens, scales and L1 sums only after that kernel completes
+    int64_t ld_b;             // elements between token rows of b_f16 (0: K)
+    int64_t l1_ld;            // blocks between token rows of row_l1 (0: K / 1024)
+    int max_pairs;            // at most this many co-resident CTA pairs (0: as many as the device holds)
+    int reduce_out;           // EPI_ACC_I32 only: add the accumulator into out (exact int32 reduction)
+                              // instead of storing it, so launches over parts of K can sum into one buffer
 };
 
 // Enqueue the exact int8 GEMM (tcgen05, fp16-coded operands, chunked fp32 -> int32).
 int launch_i8gemm(const I8GemmProblem &p, cudaStream_t st);
+// CTA pairs of the int8 GEMM that fit the current device at once.
+int i8gemm_max_pairs(int num_sms);
 
 // bf16 GEMM dx[M][K] = dy[M][N] @ w[N][K] (fp32 accumulation).
 int launch_bf16_gemm_nn(const void *dy, const void *w, void *dx, int64_t M, int64_t N, int64_t K,

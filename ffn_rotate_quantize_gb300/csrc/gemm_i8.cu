@@ -98,11 +98,13 @@ struct Params {
     const float *w_scale0;
     const float *w_scale1;
     const __nv_bfloat16 *bias;
-    const int32_t *row_l1;  // optional [M][K/1024]: sum of |q| over each 1024-long block of a token row
+    const int32_t *row_l1;  // optional [M][l1_ld]: sum of |q| over each 1024-long block of a token row
+    int64_t l1_ld;
     unsigned int *status;
     int w_layout;
     int epi;
     int use_tma_out;
+    int reduce_out;  // EPI_ACC_I32: add into out instead of storing
 };
 
 struct Bars {
@@ -205,7 +207,10 @@ __device__ __forceinline__ void store_tile_tma(const Params &p, const int32_t (&
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            tma_store_2d(&p.tm_out, buf, (int)(n0 + 32 * q), (int)mb);
+            if (EPI == EPI_ACC_I32 && p.reduce_out)
+                tma_reduce_add_2d(&p.tm_out, buf, (int)(n0 + 32 * q), (int)mb);
+            else
+                tma_store_2d(&p.tm_out, buf, (int)(n0 + 32 * q), (int)mb);
             tma_store_commit();
         }
     }
@@ -433,7 +438,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) i8gemm_
             for (int64_t m = et; m < mmax; m += 32 * kEpiWarps) {
                 int s16[kPlanMaxBlocks];
 #pragma unroll
-                for (int b2 = 0; b2 < kPlanMaxBlocks; ++b2) s16[b2] = b2 < nb ? __ldg(p.row_l1 + m * nb + b2) : 0;
+                for (int b2 = 0; b2 < kPlanMaxBlocks; ++b2) s16[b2] = b2 < nb ? __ldg(p.row_l1 + m * p.l1_ld + b2) : 0;
                 uint32_t okb = 1u;  // level 0 always holds
 #pragma unroll
                 for (int j = 1, w = kPlanMaxBlocks / 2; w >= 1; ++j, w >>= 1) {
@@ -522,7 +527,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) i8gemm_
                     if (!n_ok || m >= p.M) continue;
                     const int32_t acc = tot[32 * j + i];
                     if (p.epi == EPI_ACC_I32) {
-                        reinterpret_cast<int32_t *>(p.out)[m * p.ld_out + n] = acc;
+                        int32_t *o = reinterpret_cast<int32_t *>(p.out) + m * p.ld_out + n;
+                        if (p.reduce_out)
+                            atomicAdd(o, acc);
+                        else
+                            *o = acc;
                     } else if (p.epi == EPI_DEQUANT_BF16) {
                         const float tv = __fmul_rn(__int2float_rn(acc), xs);
                         const float y = __fmaf_rn(tv, ws, bias);
@@ -567,13 +576,17 @@ int max_pairs_for_device(int num_sms) {
 
 }  // namespace
 
+int i8gemm_max_pairs(int num_sms) { return max_pairs_for_device(num_sms); }
+
 int launch_i8gemm(const I8GemmProblem &q, cudaStream_t st) {
     Params p;  // host staging; copied into the launch's parameter buffer
     memset(&p, 0, sizeof(p));
     int rc;
     // Activations: fp16 [M][K], box 64 x 128, 128-byte swizzle (each CTA stages its 128-token half).
+    if (q.reduce_out && q.epi != EPI_ACC_I32) return gbq_fail(GBQ_EINVAL, "int8 GEMM: reduce_out needs EPI_ACC_I32");
+    const int64_t ld_b = q.ld_b > 0 ? q.ld_b : q.K;
     rc = encode_tmap_2d(&p.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, q.b_f16, (uint64_t)q.K, (uint64_t)q.M,
-                        (uint64_t)q.K * 2, kSub, kBNHalf, CU_TENSOR_MAP_SWIZZLE_128B);
+                        (uint64_t)ld_b * 2, kSub, kBNHalf, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
     for (int s = 0; s < 2; ++s) {
         const int8_t *w = s ? q.w1 : q.w0;
@@ -611,6 +624,8 @@ int launch_i8gemm(const I8GemmProblem &q, cudaStream_t st) {
     p.w_scale1 = q.w_scale1;
     p.bias = reinterpret_cast<const __nv_bfloat16 *>(q.bias);
     p.row_l1 = q.row_l1;
+    p.l1_ld = q.l1_ld > 0 ? q.l1_ld : q.K / 1024;
+    p.reduce_out = q.reduce_out;
     p.status = q.status;
     p.w_layout = q.w_layout;
     p.epi = q.epi;
@@ -628,7 +643,8 @@ int launch_i8gemm(const I8GemmProblem &q, cudaStream_t st) {
         attr = true;
     }
     const int64_t tiles = ((q.M + kBN - 1) / kBN) * ((q.N + kPairM - 1) / kPairM);
-    const int64_t pairs_max = max_pairs_for_device(q.num_sms);
+    int64_t pairs_max = max_pairs_for_device(q.num_sms);
+    if (q.max_pairs > 0 && q.max_pairs < pairs_max) pairs_max = q.max_pairs;
     const int grid = 2 * (int)(tiles < pairs_max ? tiles : pairs_max);
     prof_begin(1, st);
     cudaLaunchConfig_t cfg = {};

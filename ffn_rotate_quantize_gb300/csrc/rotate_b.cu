@@ -8,6 +8,7 @@ cudaError_t launch_rotb(int logn, int in_kind, RotArgs a, cudaStream_t st) {
         case IN_BF16: return launch_rotq_logn<IN_BF16, OUT_BF16>(logn, a, st);
         case IN_F32: return launch_rotq_logn<IN_F32, OUT_BF16>(logn, a, st);
         case IN_S8_ROWSCALE: return launch_rotq_logn<IN_S8_ROWSCALE, OUT_BF16>(logn, a, st);
+        case IN_ACC_ROWSCALE: return launch_rotq_logn<IN_ACC_ROWSCALE, OUT_BF16>(logn, a, st);
         default: return cudaErrorNotSupported;
     }
 }

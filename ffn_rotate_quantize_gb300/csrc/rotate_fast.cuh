@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(128) rot64_kernel(const __grid_constant__ Fast
             break;
         }
         float rs = 0.0f;
-        if (IN == IN_S8_ROWSCALE || IN == IN_ACC_GLU) rs = __ldg(p.in_scale + row);
+        if (IN == IN_S8_ROWSCALE || IN == IN_ACC_GLU || IN == IN_ACC_ROWSCALE) rs = __ldg(p.in_scale + row);
 
         float2 v[16];
         rot64_row<IN>(
@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(512, 2) rot128_kernel(const __grid_constant__ 
             break;
         }
         float rs = 0.0f;
-        if (IN == IN_S8_ROWSCALE || IN == IN_ACC_GLU) rs = __ldg(p.in_scale + row);
+        if (IN == IN_S8_ROWSCALE || IN == IN_ACC_GLU || IN == IN_ACC_ROWSCALE) rs = __ldg(p.in_scale + row);
         float2 v[16];
         // ---- pass A: regs i0..i3, pair i6; thread = (j0..j6, i4 i5) ----
         {

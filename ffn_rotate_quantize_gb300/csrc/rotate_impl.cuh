@@ -36,13 +36,15 @@
 
 namespace gbq {
 
-enum InKind { IN_BF16 = 0, IN_F32 = 1, IN_GLU_BF16 = 2, IN_S8_ROWSCALE = 3, IN_ACC_GLU = 4 };
+// IN_ACC_ROWSCALE: int32 accumulators times a row scale, fl(fp32(acc) * in_scale[row]) (the dx route's
+// rotated gradient, with the same operation as the GEMM's row-scale epilogue).
+enum InKind { IN_BF16 = 0, IN_F32 = 1, IN_GLU_BF16 = 2, IN_S8_ROWSCALE = 3, IN_ACC_GLU = 4, IN_ACC_ROWSCALE = 5 };
 enum OutKind { OUT_S8 = 0, OUT_F16Q = 1, OUT_BF16 = 2 };
 
 struct RotArgs {
     const void *in0;          // x / g / W8 / acc_g
     const void *in1;          // u / acc_u (GLU inputs), else unused
-    const float *in_scale;    // IN_S8_ROWSCALE: s[row]; IN_ACC_GLU: x_scale[row]
+    const float *in_scale;    // IN_S8_ROWSCALE: s[row]; IN_ACC_GLU: x_scale[row]; IN_ACC_ROWSCALE: t[row]
     const float *col_scale0;  // IN_ACC_GLU: s_gate[col]
     const float *col_scale1;  // IN_ACC_GLU: s_up[col]
     int64_t ld_in;            // elements between consecutive input rows
@@ -205,6 +207,8 @@ __device__ __forceinline__ float load_in(const RotArgs &p, int64_t row, int64_t 
                         bf16_to_float(__ldg(reinterpret_cast<const uint16_t *>(p.in1) + idx)));
     } else if constexpr (IN == IN_S8_ROWSCALE) {
         return __fmul_rn((float)__ldg(reinterpret_cast<const int8_t *>(p.in0) + idx), __ldg(p.in_scale + row));
+    } else if constexpr (IN == IN_ACC_ROWSCALE) {
+        return __fmul_rn(__int2float_rn(__ldg(reinterpret_cast<const int32_t *>(p.in0) + idx)), __ldg(p.in_scale + row));
     } else {  // IN_ACC_GLU
         const float xs = __ldg(p.in_scale + row);
         const float gv = dequant_bf16_value(__ldg(reinterpret_cast<const int32_t *>(p.in0) + idx), xs,
@@ -415,13 +419,13 @@ __device__ __forceinline__ void store_codes(void *out, int64_t off, const uint32
 // Number of input tensors and bytes per input element of an input kind.
 __host__ __device__ constexpr int in_count(int in_kind) { return (in_kind == IN_GLU_BF16 || in_kind == IN_ACC_GLU) ? 2 : 1; }
 __host__ __device__ constexpr int in_elem_bytes(int in_kind) {
-    return in_kind == IN_S8_ROWSCALE ? 1 : (in_kind == IN_F32 || in_kind == IN_ACC_GLU) ? 4 : 2;
+    return in_kind == IN_S8_ROWSCALE ? 1 : (in_kind == IN_F32 || in_kind == IN_ACC_GLU || in_kind == IN_ACC_ROWSCALE) ? 4 : 2;
 }
 __host__ __device__ constexpr int out_elem_bytes(int out_kind) { return out_kind == OUT_S8 ? 1 : 2; }
 
 // Elements idx, idx + 1 (idx even, index within the row) of a staged row as an
 // fp32 pair, with the same arithmetic as load_in2.  s0 / s1: the row's staged
-// input(s); rs: the row's scale (IN_S8_ROWSCALE: s[row]; IN_ACC_GLU: x_scale[row]).
+// input(s); rs: the row's scale (IN_S8_ROWSCALE: s[row]; IN_ACC_GLU: x_scale[row]; IN_ACC_ROWSCALE: t[row]).
 template <int IN>
 __device__ __forceinline__ float2 staged_pair(const RotArgs &p, const uint8_t *s0, const uint8_t *s1, float rs,
                                               int idx) {
@@ -438,6 +442,9 @@ __device__ __forceinline__ float2 staged_pair(const RotArgs &p, const uint8_t *s
     } else if constexpr (IN == IN_S8_ROWSCALE) {
         const char2 q = *reinterpret_cast<const char2 *>(s0 + idx);
         return __fmul2_rn(f2((float)q.x, (float)q.y), f2(rs, rs));
+    } else if constexpr (IN == IN_ACC_ROWSCALE) {
+        const int2 a = *reinterpret_cast<const int2 *>(s0 + 4 * idx);
+        return f2(__fmul_rn(__int2float_rn(a.x), rs), __fmul_rn(__int2float_rn(a.y), rs));
     } else {  // IN_ACC_GLU
         const int2 ag = *reinterpret_cast<const int2 *>(s0 + 4 * idx);
         const int2 au = *reinterpret_cast<const int2 *>(s1 + 4 * idx);
@@ -460,6 +467,8 @@ __device__ __forceinline__ float staged_one(const RotArgs &p, const uint8_t *s0,
                         bf16_to_float(*reinterpret_cast<const uint16_t *>(s1 + 2 * idx)));
     } else if constexpr (IN == IN_S8_ROWSCALE) {
         return __fmul_rn((float)*reinterpret_cast<const int8_t *>(s0 + idx), rs);
+    } else if constexpr (IN == IN_ACC_ROWSCALE) {
+        return __fmul_rn(__int2float_rn(*reinterpret_cast<const int32_t *>(s0 + 4 * idx)), rs);
     } else {
         const int32_t ag = *reinterpret_cast<const int32_t *>(s0 + 4 * idx);
         const int32_t au = *reinterpret_cast<const int32_t *>(s1 + 4 * idx);
@@ -587,7 +596,7 @@ __global__ void __launch_bounds__(RotqMaxThreads<LOGN>::value) rotq_kernel(const
         if (active) {
             const uint8_t *s0 = sbuf + (size_t)(slot * NIN) * in_row_bytes;
             float rs = 0.0f;
-            if (IN == IN_S8_ROWSCALE || IN == IN_ACC_GLU) rs = __ldg(p.in_scale + row);
+            if (IN == IN_S8_ROWSCALE || IN == IN_ACC_GLU || IN == IN_ACC_ROWSCALE) rs = __ldg(p.in_scale + row);
             staged_columns<LOGN, IN>(p, s0, s0 + in_row_bytes, rs, g, t, c);
         } else {
 #pragma unroll

@@ -97,6 +97,21 @@ def test_graph_ffn_and_dx_int8(ops, M):
     ])
 
 
+def test_linear_dx_int8_two_stream_split_graph(ops):
+    """linear_dx_int8 over a long contraction (N = 8192: two GEMM halves on the library's second stream and
+    the caller's, summed exactly into one accumulator) captured in a graph replays the eager bits, which
+    match the oracle."""
+    M, N, K, rot = 200, 8192, 1024, (32, 32, 1)
+    c = I.backward_case(M, N, K, seed=81)
+    w8, s = O.prepare_weight(c["w"], rot)
+    dy, w8d, sd = bf16_dev(c["dy"]), d(w8), d(s)
+    ws = torch.empty(ops.workspace_size(ops.OP_LINEAR_DX_INT8, M, N, K), dtype=torch.uint8, device="cuda")
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    _capture_and_compare(ops, [(lambda out: ops.linear_dx_int8(dy, w8d, sd, rot, ws, out=out), dx)])
+    from parity import assert_bf16_parity, bf16_np
+    assert_bf16_parity(bf16_np(dx), O.linear_dx_int8(c["dy"], w8, s, rot))
+
+
 @pytest.mark.parametrize("M,K,rot", [(1, 4096, (64, 64, 1)), (3, 4096, (64, 64, 1)), (2, 1024, (32, 32, 1))])
 def test_decode_chain_back_to_back(ops, M, K, rot):
     """Stacked decode layers, each reading the previous layer's output as its x, launched back to
