@@ -146,7 +146,7 @@ int run_rotq(const char *what, gbq_rot rot, int logn, int in_kind, int out_kind,
         if (in_kind != IN_BF16 || out_kind == OUT_BF16)
             return fail(GBQ_ENOTSUP, "%s: identity rotation is supported for bf16 quantization only", what);
         REQUIRE(a.K % 8 == 0, "%s: identity rotation needs K %% 8 == 0 (K=%lld)", what, (long long)a.K);
-        IdArgs ia{a.in0, nullptr, a.ld_in, a.out, a.out_scale, a.M, a.K};
+        IdArgs ia{a.in0, nullptr, a.ld_in, a.out, a.out_scale, a.M, a.K, nullptr, d->status, d->sms};
         e = launch_quant_identity(out_kind, ia, st);
     } else {
         a.G = rot.groups;
@@ -719,7 +719,7 @@ int gbq_linear_dx_int8(const void *dy, const int8_t *w8, const float *w_scale, v
         if (e != cudaSuccess) return cuda_fail(e, "gbq_linear_dx_int8 (clear the accumulator)");
     }
     // 1) dy' = dy * s[n] (column scale), per-row quantize, no rotation
-    IdArgs ia{dy, w_scale, N, qd, t, M, N, l1};
+    IdArgs ia{dy, w_scale, N, qd, t, M, N, l1, d->status, d->sms};
     e = launch_quant_identity(OUT_F16Q, ia, st);
     if (e != cudaSuccess) {
         if (split) (void)cudaStreamWaitEvent(st, d->ev_zero, 0);  // the caller's stream stays after the clear

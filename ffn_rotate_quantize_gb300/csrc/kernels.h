@@ -20,6 +20,8 @@ struct IdArgs {
     float *out_scale;         // fp32 [M]
     int64_t M, K;
     int32_t *out_l1;          // [M][ceil(K/1024)] sums of |code| over 1024-long blocks, or nullptr
+    unsigned int *status = nullptr;  // device status word; with num_sms > 0 it enables the streaming
+    int num_sms = 0;                 // kernel for long rows (8192 <= K <= 16384)
 };
 
 // Launch a rotate(+quantize) kernel.  Returns cudaErrorNotSupported for a

@@ -113,3 +113,29 @@ def test_linear_dx_int8_chunk_plan(ops):
     assert np.array_equal(l1, np.abs(codes).reshape(M, 16, 1024).sum(axis=2))
     assert l1[:128].min() == 127 * 1024 and l1[128:].max() < 2 ** 17 // 4  # tile 0: 1-block chunks only
     assert_bf16_parity(bf16_np(dx_p), O.linear_dx_int8(dy_b, w8, s, rot))
+
+
+def test_linear_dx_int8_dy_codes_long_run(ops):
+    """The dy quantizer's codes, row scales and block sums with more rows than SMs times row stages (each
+    persistent CTA of the long-row quantizer reuses its shared-memory stages), a zero row among them: equal,
+    bit for bit, to the oracle's per-row quantization of dy * s (R = I, so no rotation rounding)."""
+    rng = np.random.default_rng(29)
+    M, N, K, rot = 1500, 16384, 256, (16, 16, 1)
+    dy_b = I.bf16_bits(rng.standard_normal((M, N)).astype(np.float32) * np.float32(1e-3))
+    dy_b[5] = 0
+    w8 = rng.integers(-127, 128, (N, K)).astype(np.int8)
+    s = rng.random(N).astype(np.float32) * np.float32(0.01) + np.float32(1e-3)
+    pref = ops.workspace_size(ops.OP_LINEAR_DX_INT8, M, N, K)
+    minimum = _a256(M * N * 2) + _a256(M * 4) + _a256(M * K * 4)
+    ws_p = torch.zeros(pref, dtype=torch.uint8, device="cuda")
+    dx = ops.linear_dx_int8(bf16_dev(dy_b), d(w8), d(s), rot, ws_p)
+    torch.cuda.synchronize()
+    dx_r, mid = O.linear_dx_int8(dy_b, w8, s, rot, keep=True)
+    codes = ws_p[:M * N * 2].view(torch.float16).view(M, N).float().cpu().numpy().astype(np.int64)
+    t = ws_p[_a256(M * N * 2):_a256(M * N * 2) + M * 4].view(torch.float32).cpu().numpy()
+    assert t[5] == 0 and not codes[5].any()
+    assert np.array_equal(t, mid["t"])
+    assert np.array_equal(codes, mid["qd"].astype(np.int64))
+    l1 = ws_p[minimum:minimum + M * 4 * 16].view(torch.int32).view(M, 16).cpu().numpy()
+    assert np.array_equal(l1, np.abs(codes).reshape(M, 16, 1024).sum(axis=2))
+    assert_bf16_parity(bf16_np(dx), dx_r)

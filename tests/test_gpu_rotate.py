@@ -201,9 +201,9 @@ def test_dequant_weight_grouped(ops, rot):
 
 @pytest.mark.parametrize("K,M", [(16384, 1000), (10000, 157), (8200, 3)])
 def test_quantize_act_identity_long_rows_exact(ops, K, M):
-    """R = I on long rows (persistent CTAs stream the rows through shared-memory stages; the ring wraps
-    for M = 1000): the values are the bf16 inputs themselves, so scales and codes equal the oracle's
-    exactly, including a zero row and a row of tiny values."""
+    """R = I on long rows (one CTA of 256 or 512 threads per row, the row held in registers): the values
+    are the bf16 inputs themselves, so scales and codes equal the oracle's exactly, including a zero row
+    and a row of tiny values."""
     xb = _x(M, K, seed=M + K, outliers=max(1, K // 100))
     xb[0] = 0
     if M > 2:
