@@ -187,7 +187,7 @@ int gbq_linear(const void *x, const int8_t *w8, const float *w_scale, const void
  * y = linear(x, w8, w_scale, bias) with no workspace argument: the same
  * computation and kernels as gbq_linear, with the scratch taken from a 16 MiB
  * static device array inside the library instead of a caller workspace.  The
- * paper has no counterpart to this entry point; it exists for callers that
+ * method's API ("Use from C") has no counterpart to it; it exists for callers that
  * cannot allocate device memory at the point of the call (a plugin inside a
  * framework that owns all device memory through its own pool, or a
  * latency-critical loop that cannot afford cudaMalloc's implicit
