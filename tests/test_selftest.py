@@ -39,6 +39,10 @@ def _run():
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="the no-GPU behaviour")
 def test_selftest_without_gpu_skips():
+    from ffn_rotate_quantize_gb300 import _lib as L
+    if not os.path.exists(L.LIB_PATH):
+        from ffn_rotate_quantize_gb300.build import build_lib
+        build_lib()
     r = _run()
     assert r.returncode == 2, r.stdout + r.stderr
     lines = r.stdout.strip().splitlines()
