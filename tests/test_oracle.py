@@ -301,6 +301,30 @@ def test_dequant_weight_recovers_w():
     assert np.linalg.norm(lit - wr) / np.linalg.norm(wr) < 0.011
 
 
+def test_dequant_weight_against_exact_integer_transform():
+    """(W8 s) R has a closed form: s / 64 times the integer row W8 H (H = H64 (x) H64 built here from the
+    printed H4 by digits; |W8 H| < 127 * 4096 < 2^24, so fp64 holds it exactly).  The oracle, which rounds
+    W8 s to fp32 before its fp64 sum, lies within one bf16 unit of it plus the residue of those roundings
+    (at most 64 * 127 * s * 2^-24), and equals bf16 of it exactly when s is a power of two."""
+    g = np.random.default_rng(12)
+    N, K, rot = 48, 4096, (64, 64, 1)
+    w8 = g.integers(-127, 128, (N, K)).astype(np.int8)
+    w8[0] = 0
+    w8[1] = 127
+    H = _digit_hadamard(6)
+    v = w8.astype(np.int64) @ H
+    for s in ((g.random(N) * 1e-3 + 1e-5).astype(np.float32),
+              np.ldexp(np.float32(1), g.integers(-14, -4, N)).astype(np.float32)):
+        exact = s[:, None].astype(np.float64) * v.astype(np.float64) / 64.0
+        got = O.dequant_weight(w8, s, rot)
+        o = O.bf16_to_f32(got).astype(np.float64)
+        resid = 64.0 * 127.0 * s[:, None].astype(np.float64) * 2.0 ** -24
+        mag = np.abs(exact) + resid
+        ulp = np.exp2(np.floor(np.log2(np.maximum(mag, 1e-38))) - 7)
+        assert np.all(np.abs(o - exact) <= resid + ulp)
+    assert np.array_equal(got, O.f32_to_bf16(exact.astype(np.float32)))  # power-of-two scales: exact
+
+
 def test_linear_dx_matches_numpy():
     rng = np.random.default_rng(11)
     dy = I.bf16_bits(rng.standard_normal((8, 96)).astype(np.float32))
