@@ -7,6 +7,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/gbq.h"
@@ -36,7 +37,8 @@ int cuda_fail(cudaError_t e, const char *what) {
 __device__ unsigned int g_status_word;
 
 struct DevState {
-    bool ready = false;
+    // Set (release) once every other field is in place; read (acquire) without the lock.
+    std::atomic<bool> ready{false};
     unsigned int *status = nullptr;
     int sms = 0;
     char name[256] = "";
@@ -58,12 +60,12 @@ int init_current(DevState **out) {
     if (e != cudaSuccess) return fail(GBQ_ENODEV, "no CUDA device: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= kMaxDevices) return fail(GBQ_ENODEV, "device index %d out of range", dev);
     DevState &d = g_dev[dev];
-    if (d.ready) {
+    if (d.ready.load(std::memory_order_acquire)) {
         *out = &d;
         return GBQ_OK;
     }
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!d.ready) {
+    if (!d.ready.load(std::memory_order_relaxed)) {
         cudaDeviceProp prop;
         e = cudaGetDeviceProperties(&prop, dev);
         if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceProperties");
@@ -81,6 +83,10 @@ int init_current(DevState **out) {
                 return fail(GBQ_ECUDA, "cuTensorMapEncodeTiled entry point unavailable");
             g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
         }
+        // The static scratch of gbq_linear_noalloc: its module is loaded (and its memory reserved)
+        // here, at the device's set-up, not inside a later call.
+        int rc = noalloc_setup_current(dev);
+        if (rc != GBQ_OK) return rc;
         e = cudaStreamCreateWithFlags(&d.aux, cudaStreamNonBlocking);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.ev_fork, cudaEventDisableTiming);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.ev_join, cudaEventDisableTiming);
@@ -90,7 +96,7 @@ int init_current(DevState **out) {
         d.status = static_cast<unsigned int *>(p);
         d.sms = prop.multiProcessorCount;
         snprintf(d.name, sizeof(d.name), "%s", prop.name);
-        d.ready = true;
+        d.ready.store(true, std::memory_order_release);
     }
     *out = &d;
     return GBQ_OK;
@@ -116,44 +122,69 @@ int ilog2(int v) {
     return l;
 }
 
-// Validates a rotation descriptor for row length K; sets *logn (0 = identity).
-int check_rot(gbq_rot r, int64_t K, int *logn) {
+// A validated rotation descriptor and the kernel family that serves it.
+struct RotSel {
+    int logn;    // 0: identity; 4..7: a = b = 2^logn, the square kernels; -1: the generic kernel
+    int la, lb;  // log2 a, log2 b
+    int a, b, groups;
+};
+
+// Validates a rotation descriptor for row length K.  Any powers of two a, b >= 1 with a*b*groups = K
+// are accepted.  a = b in {16, 32, 64, 128} with few enough groups for one CTA per row go to the
+// square kernels; every other shape (a != b, factors 2..8 or above 128, many groups) to the generic
+// kernel, which needs K % 16 == 0 and K <= kGenMaxK (GBQ_ENOTSUP otherwise).  Both produce the same
+// values for a descriptor they can both serve.
+int check_rot(gbq_rot r, int64_t K, RotSel *sel) {
     REQUIRE(r.a >= 1 && r.b >= 1 && r.groups >= 1, "rotation (a=%d, b=%d, groups=%d): all must be >= 1", r.a, r.b,
             r.groups);
     REQUIRE((r.a & (r.a - 1)) == 0 && (r.b & (r.b - 1)) == 0, "rotation a=%d, b=%d: must be powers of two", r.a, r.b);
     REQUIRE((int64_t)r.a * r.b * r.groups == K, "rotation a*b*groups = %lld != K = %lld",
             (long long)r.a * r.b * r.groups, (long long)K);
+    sel->la = ilog2(r.a);
+    sel->lb = ilog2(r.b);
+    sel->a = r.a;
+    sel->b = r.b;
+    sel->groups = r.groups;
     if (r.a == 1 && r.b == 1) {
-        *logn = 0;
+        sel->logn = 0;
         return GBQ_OK;
     }
-    if (r.a != r.b || r.a < 16 || r.a > 128)
-        return fail(GBQ_ENOTSUP, "rotation (a=%d, b=%d): supported factors are a = b in {1, 16, 32, 64, 128}", r.a,
-                    r.b);
-    *logn = ilog2(r.a);
+    if (r.a == r.b && sel->la >= 4 && sel->la <= 7 &&
+        (int64_t)rotq_row_threads(sel->la, 1) * r.groups <= (sel->la >= 6 ? 256 : 512)) {
+        sel->logn = sel->la;
+        return GBQ_OK;
+    }
+    if (!rotg_fits(K))
+        return fail(GBQ_ENOTSUP,
+                    "rotation (a=%d, b=%d, groups=%d) over K=%lld: this shape is served for K %% 16 == 0 and "
+                    "K <= %lld only",
+                    r.a, r.b, r.groups, (long long)K, (long long)kGenMaxK);
+    sel->logn = -1;
     return GBQ_OK;
 }
 
 // Rotate(+quantize) rows of an input through the right kernel.
-int run_rotq(const char *what, gbq_rot rot, int logn, int in_kind, int out_kind, RotArgs a, cudaStream_t st) {
+int run_rotq(const char *what, const RotSel &rot, int in_kind, int out_kind, RotArgs a, cudaStream_t st) {
     cudaError_t e;
     DevState *d = nullptr;
     int rc = init_current(&d);
     if (rc != GBQ_OK) return rc;
     a.status = d->status;
     a.num_sms = d->sms;
-    if (logn == 0) {
-        if (in_kind != IN_BF16 || out_kind == OUT_BF16)
-            return fail(GBQ_ENOTSUP, "%s: identity rotation is supported for bf16 quantization only", what);
+    if (rot.logn == 0 && in_kind == IN_BF16 && out_kind != OUT_BF16) {
         REQUIRE(a.K % 8 == 0, "%s: identity rotation needs K %% 8 == 0 (K=%lld)", what, (long long)a.K);
         IdArgs ia{a.in0, nullptr, a.ld_in, a.out, a.out_scale, a.M, a.K, nullptr, d->status, d->sms};
         e = launch_quant_identity(out_kind, ia, st);
-    } else {
+    } else if (rot.logn > 0) {
         a.G = rot.groups;
         if (out_kind == OUT_BF16)
-            e = launch_rotb(logn, in_kind, a, st);
+            e = launch_rotb(rot.logn, in_kind, a, st);
         else
-            e = launch_rotq(logn, in_kind, out_kind, a, st);
+            e = launch_rotq(rot.logn, in_kind, out_kind, a, st);
+        // A shape the square kernels cannot stage (shared memory): the generic kernel gives the same values.
+        if (e == cudaErrorNotSupported && rotg_fits(a.K)) e = launch_rotg(in_kind, out_kind, a, rot.la, rot.lb, st);
+    } else {
+        e = launch_rotg(in_kind, out_kind, a, rot.la, rot.lb, st);
     }
     if (e != cudaSuccess) return cuda_fail(e, what);
     return GBQ_OK;
@@ -219,7 +250,8 @@ int gbq_init(void) {
 const char *gbq_device_name(void) {
     int dev = -1;
     g_name_out[0] = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices && g_dev[dev].ready)
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices &&
+        g_dev[dev].ready.load(std::memory_order_acquire))
         snprintf(g_name_out, sizeof(g_name_out), "%s", g_dev[dev].name);
     return g_name_out;
 }
@@ -286,8 +318,8 @@ size_t gbq_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t H) {
 
 int gbq_quantize_act(const void *x, int8_t *q, float *x_scale, int64_t M, int64_t K, gbq_rot rot, void *stream) {
     REQUIRE(M >= 0 && K >= 1, "gbq_quantize_act: bad sizes M=%lld K=%lld", (long long)M, (long long)K);
-    int logn = 0;
-    int rc = check_rot(rot, K, &logn);
+    RotSel rs{};
+    int rc = check_rot(rot, K, &rs);
     if (rc) return rc;
     if (M == 0) return GBQ_OK;
     REQUIRE(a16(x) && a16(q) && a16(x_scale), "gbq_quantize_act: pointers must be non-NULL and 16-byte aligned");
@@ -299,14 +331,14 @@ int gbq_quantize_act(const void *x, int8_t *q, float *x_scale, int64_t M, int64_
     a.out_scale = x_scale;
     a.M = M;
     a.K = K;
-    return run_rotq("gbq_quantize_act", rot, logn, IN_BF16, OUT_S8, a, (cudaStream_t)stream);
+    return run_rotq("gbq_quantize_act", rs, IN_BF16, OUT_S8, a, (cudaStream_t)stream);
 }
 
 int gbq_prepare_weight(const void *w, int8_t *w8, float *w_scale, int64_t N, int64_t K, gbq_rot rot,
                        void *stream) {
     REQUIRE(N >= 0 && K >= 1, "gbq_prepare_weight: bad sizes N=%lld K=%lld", (long long)N, (long long)K);
-    int logn = 0;
-    int rc = check_rot(rot, K, &logn);
+    RotSel rs{};
+    int rc = check_rot(rot, K, &rs);
     if (rc) return rc;
     if (N == 0) return GBQ_OK;
     REQUIRE(a16(w) && a16(w8) && a16(w_scale), "gbq_prepare_weight: pointers must be non-NULL and 16-byte aligned");
@@ -318,14 +350,14 @@ int gbq_prepare_weight(const void *w, int8_t *w8, float *w_scale, int64_t N, int
     a.out_scale = w_scale;
     a.M = N;
     a.K = K;
-    return run_rotq("gbq_prepare_weight", rot, logn, IN_BF16, OUT_S8, a, (cudaStream_t)stream);
+    return run_rotq("gbq_prepare_weight", rs, IN_BF16, OUT_S8, a, (cudaStream_t)stream);
 }
 
 int gbq_quantize_act_glu(const void *g, const void *u, int8_t *q, float *h_scale, int64_t M, int64_t H,
                          gbq_rot rot, void *stream) {
     REQUIRE(M >= 0 && H >= 1, "gbq_quantize_act_glu: bad sizes M=%lld H=%lld", (long long)M, (long long)H);
-    int logn = 0;
-    int rc = check_rot(rot, H, &logn);
+    RotSel rs{};
+    int rc = check_rot(rot, H, &rs);
     if (rc) return rc;
     if (M == 0) return GBQ_OK;
     REQUIRE(a16(g) && a16(u) && a16(q) && a16(h_scale),
@@ -339,7 +371,7 @@ int gbq_quantize_act_glu(const void *g, const void *u, int8_t *q, float *h_scale
     a.out_scale = h_scale;
     a.M = M;
     a.K = H;
-    return run_rotq("gbq_quantize_act_glu", rot, logn, IN_GLU_BF16, OUT_S8, a, (cudaStream_t)stream);
+    return run_rotq("gbq_quantize_act_glu", rs, IN_GLU_BF16, OUT_S8, a, (cudaStream_t)stream);
 }
 
 int gbq_dequant_act_quantize(const int32_t *acc_g, const int32_t *acc_u, int64_t ld_acc, const float *x_scale,
@@ -347,15 +379,14 @@ int gbq_dequant_act_quantize(const int32_t *acc_g, const int32_t *acc_u, int64_t
                              gbq_rot rot, void *stream) {
     REQUIRE(M >= 0 && H >= 1 && ld_acc >= H, "gbq_dequant_act_quantize: bad sizes M=%lld H=%lld ld_acc=%lld",
             (long long)M, (long long)H, (long long)ld_acc);
-    int logn = 0;
-    int rc = check_rot(rot, H, &logn);
+    RotSel rs{};
+    int rc = check_rot(rot, H, &rs);
     if (rc) return rc;
     if (M == 0) return GBQ_OK;
     REQUIRE(a16(acc_g) && a16(acc_u) && a16(x_scale) && a16(s_gate) && a16(s_up) && a16(q) && a16(h_scale),
             "gbq_dequant_act_quantize: pointers must be non-NULL and 16-byte aligned");
     REQUIRE(ld_acc % 4 == 0, "gbq_dequant_act_quantize: ld_acc must be a multiple of 4");
     INIT(d);
-    if (logn == 0) return fail(GBQ_ENOTSUP, "gbq_dequant_act_quantize: identity rotation not supported");
     RotArgs a{};
     a.in0 = acc_g;
     a.in1 = acc_u;
@@ -367,18 +398,18 @@ int gbq_dequant_act_quantize(const int32_t *acc_g, const int32_t *acc_u, int64_t
     a.out_scale = h_scale;
     a.M = M;
     a.K = H;
-    return run_rotq("gbq_dequant_act_quantize", rot, logn, IN_ACC_GLU, OUT_S8, a, (cudaStream_t)stream);
+    return run_rotq("gbq_dequant_act_quantize", rs, IN_ACC_GLU, OUT_S8, a, (cudaStream_t)stream);
 }
 
 int gbq_rotate_bf16(const void *x, void *xr, int64_t M, int64_t K, gbq_rot rot, void *stream) {
     REQUIRE(M >= 0 && K >= 1, "gbq_rotate_bf16: bad sizes M=%lld K=%lld", (long long)M, (long long)K);
-    int logn = 0;
-    int rc = check_rot(rot, K, &logn);
+    RotSel rs{};
+    int rc = check_rot(rot, K, &rs);
     if (rc) return rc;
     if (M == 0) return GBQ_OK;
     REQUIRE(a16(x) && a16(xr), "gbq_rotate_bf16: pointers must be non-NULL and 16-byte aligned");
     INIT(d);
-    if (logn == 0) {
+    if (rs.logn == 0) {
         cudaError_t e = cudaMemcpyAsync(xr, x, (size_t)(M * K * 2), cudaMemcpyDeviceToDevice, (cudaStream_t)stream);
         return e == cudaSuccess ? GBQ_OK : cuda_fail(e, "gbq_rotate_bf16");
     }
@@ -388,24 +419,24 @@ int gbq_rotate_bf16(const void *x, void *xr, int64_t M, int64_t K, gbq_rot rot, 
     a.out = xr;
     a.M = M;
     a.K = K;
-    return run_rotq("gbq_rotate_bf16", rot, logn, IN_BF16, OUT_BF16, a, (cudaStream_t)stream);
+    return run_rotq("gbq_rotate_bf16", rs, IN_BF16, OUT_BF16, a, (cudaStream_t)stream);
 }
 
 int gbq_dequant_weight(const int8_t *w8, const float *w_scale, void *w, int64_t N, int64_t K, gbq_rot rot,
                        void *stream) {
     REQUIRE(N >= 0 && K >= 1, "gbq_dequant_weight: bad sizes N=%lld K=%lld", (long long)N, (long long)K);
-    int logn = 0;
-    int rc = check_rot(rot, K, &logn);
+    RotSel rs{};
+    int rc = check_rot(rot, K, &rs);
     if (rc) return rc;
     if (N == 0) return GBQ_OK;
     REQUIRE(a16(w8) && a16(w_scale) && a16(w), "gbq_dequant_weight: pointers must be non-NULL and 16-byte aligned");
     INIT(d);
-    if (logn == 0) {
+    if (rs.logn == 0) {
         REQUIRE(K % 16 == 0, "gbq_dequant_weight: identity rotation needs K %% 16 == 0");
         cudaError_t e = launch_scale_rows_s8(w8, w_scale, w, N, K, (cudaStream_t)stream);
         return e == cudaSuccess ? GBQ_OK : cuda_fail(e, "gbq_dequant_weight");
     }
-    if (logn == 6) {  // integer-exact two-pass kernel
+    if (rot.a == 64 && rot.b == 64) {  // integer-exact two-pass kernel
         cudaError_t e = launch_dequant_weight64(w8, w_scale, w, N, rot.groups, d->sms, (cudaStream_t)stream);
         return e == cudaSuccess ? GBQ_OK : cuda_fail(e, "gbq_dequant_weight");
     }
@@ -416,7 +447,7 @@ int gbq_dequant_weight(const int8_t *w8, const float *w_scale, void *w, int64_t 
     a.out = w;
     a.M = N;
     a.K = K;
-    return run_rotq("gbq_dequant_weight", rot, logn, IN_S8_ROWSCALE, OUT_BF16, a, (cudaStream_t)stream);
+    return run_rotq("gbq_dequant_weight", rs, IN_S8_ROWSCALE, OUT_BF16, a, (cudaStream_t)stream);
 }
 
 }  // extern "C"
@@ -456,7 +487,7 @@ int check_ws(const char *what, int op, void *workspace, size_t ws_bytes, int64_t
 
 // Quantize x into the f16-coded GEMM operand.
 int quantize_f16q(const char *what, const void *x, int64_t ld, void *qf16, float *xs, int64_t M, int64_t K,
-                  gbq_rot rot, int logn, cudaStream_t st, int32_t *l1 = nullptr) {
+                  const RotSel &rot, cudaStream_t st, int32_t *l1 = nullptr) {
     RotArgs a{};
     a.in0 = x;
     a.ld_in = ld;
@@ -465,7 +496,7 @@ int quantize_f16q(const char *what, const void *x, int64_t ld, void *qf16, float
     a.out_l1 = l1;
     a.M = M;
     a.K = K;
-    return run_rotq(what, rot, logn, IN_BF16, OUT_F16Q, a, st);
+    return run_rotq(what, rot, IN_BF16, OUT_F16Q, a, st);
 }
 
 I8GemmProblem gemm_problem(DevState *d, const void *b_f16, const int8_t *w8, int64_t M, int64_t N, int64_t K,
@@ -496,6 +527,21 @@ I8GemmProblem gemm_problem(DevState *d, const void *b_f16, const int8_t *w8, int
 
 }  // namespace
 
+namespace gbq {
+// The argument checks of gbq_linear that need no pointer, then the device set-up (gbq_linear_noalloc
+// runs them before its own scratch checks, so a bad argument gets the same code as from gbq_linear).
+int linear_args_check(const char *what, int64_t M, int64_t N, int64_t K, gbq_rot rot) {
+    int rc = check_gemm_sizes(what, M, N, K);
+    if (rc) return rc;
+    RotSel rs{};
+    rc = check_rot(rot, K, &rs);
+    if (rc) return rc;
+    if (M == 0) return GBQ_OK;
+    DevState *d = nullptr;
+    return init_current(&d);
+}
+}  // namespace gbq
+
 extern "C" {
 
 int gbq_int8_gemm(const int8_t *q, const int8_t *w8, int32_t *acc, int64_t ld_acc, int64_t M, int64_t N, int64_t K,
@@ -521,8 +567,8 @@ int gbq_linear_acc(const void *x, const int8_t *w8, int32_t *acc, int64_t ld_acc
                    int64_t N, int64_t K, gbq_rot rot, void *workspace, size_t ws_bytes, void *stream) {
     int rc = check_gemm_sizes("gbq_linear_acc", M, N, K);
     if (rc) return rc;
-    int logn = 0;
-    rc = check_rot(rot, K, &logn);
+    RotSel rs{};
+    rc = check_rot(rot, K, &rs);
     if (rc) return rc;
     REQUIRE(ld_acc >= N, "gbq_linear_acc: ld_acc < N");
     if (M == 0) return GBQ_OK;
@@ -536,8 +582,8 @@ int gbq_linear_acc(const void *x, const int8_t *w8, int32_t *acc, int64_t ld_acc
     void *qf = w.take((size_t)M * K * 2);
     (void)w.take((size_t)M * 4);                      // (gbq_linear's x_scale slot)
     int32_t *l1 = (int32_t *)w.take((size_t)M * 4 * ((K + 1023) / 1024));  // block L1 norms: preferred size only
-    if (!rotq_writes_l1(logn, rot.groups)) l1 = nullptr;
-    rc = quantize_f16q("gbq_linear_acc", x, K, qf, x_scale, M, K, rot, logn, st, l1);
+    if (!rotq_writes_l1(rs.logn, rs.groups)) l1 = nullptr;
+    rc = quantize_f16q("gbq_linear_acc", x, K, qf, x_scale, M, K, rs, st, l1);
     if (rc) return rc;
     I8GemmProblem g = gemm_problem(d, qf, w8, M, N, K, EPI_ACC_I32, acc, ld_acc, nullptr, nullptr, nullptr);
     g.row_l1 = l1;
@@ -562,8 +608,8 @@ int gbq_linear(const void *x, const int8_t *w8, const float *w_scale, const void
                int64_t K, gbq_rot rot, void *workspace, size_t ws_bytes, void *stream) {
     int rc = check_gemm_sizes("gbq_linear", M, N, K);
     if (rc) return rc;
-    int logn = 0;
-    rc = check_rot(rot, K, &logn);
+    RotSel rs{};
+    rc = check_rot(rot, K, &rs);
     if (rc) return rc;
     if (M == 0) return GBQ_OK;
     REQUIRE(a16(x) && a16(w8) && a16(w_scale) && a16(y) && (bias == nullptr || a16(bias)),
@@ -572,16 +618,16 @@ int gbq_linear(const void *x, const int8_t *w8, const float *w_scale, const void
     if (rc) return rc;
     INIT(d);
     cudaStream_t st = (cudaStream_t)stream;
-    if (M <= 4 && logn != 0) {
-        rc = launch_gemv(x, w8, w_scale, bias, y, M, N, K, logn, rot.groups, d->sms, st, d->status);
+    if (M <= 4 && rs.logn > 0) {  // the square shapes (others run the GEMM below)
+        rc = launch_gemv(x, w8, w_scale, bias, y, M, N, K, rs.logn, rs.groups, d->sms, st, d->status);
         if (rc != GBQ_ENOTSUP) return rc;
     }
     Ws w{(uint8_t *)workspace, ws_bytes};
     void *qf = w.take((size_t)M * K * 2);
     float *xs = (float *)w.take((size_t)M * 4);
     int32_t *l1 = (int32_t *)w.take((size_t)M * 4 * ((K + 1023) / 1024));  // block L1 norms: preferred size only
-    if (!rotq_writes_l1(logn, rot.groups)) l1 = nullptr;
-    rc = quantize_f16q("gbq_linear", x, K, qf, xs, M, K, rot, logn, st, l1);
+    if (!rotq_writes_l1(rs.logn, rs.groups)) l1 = nullptr;
+    rc = quantize_f16q("gbq_linear", x, K, qf, xs, M, K, rs, st, l1);
     if (rc) return rc;
     I8GemmProblem g = gemm_problem(d, qf, w8, M, N, K, EPI_DEQUANT_BF16, y, N, xs, w_scale, bias);
     g.row_l1 = l1;
@@ -597,12 +643,13 @@ int gbq_ffn_fused(const void *x, const int8_t *wg8, const float *s_gate, const i
     rc = check_gemm_sizes("gbq_ffn_fused (down)", M, d, H);
     if (rc) return rc;
     REQUIRE(H % 128 == 0, "gbq_ffn_fused: H=%lld must be a multiple of 128", (long long)H);
-    int logd = 0, logh = 0;
-    rc = check_rot(rot_d, d, &logd);
+    RotSel rsd{}, rsh{};
+    rc = check_rot(rot_d, d, &rsd);
     if (rc) return rc;
-    rc = check_rot(rot_h, H, &logh);
+    rc = check_rot(rot_h, H, &rsh);
     if (rc) return rc;
-    if (logh == 0) return fail(GBQ_ENOTSUP, "gbq_ffn_fused: identity hidden rotation not supported");
+    if (rsh.logn == 0 && !rotg_fits(H))
+        return fail(GBQ_ENOTSUP, "gbq_ffn_fused: identity hidden rotation needs H <= %lld", (long long)kGenMaxK);
     if (M == 0) return GBQ_OK;
     REQUIRE(a16(x) && a16(wg8) && a16(s_gate) && a16(wu8) && a16(s_up) && a16(wd8) && a16(s_down) && a16(y),
             "gbq_ffn_fused: pointers must be non-NULL and 16-byte aligned");
@@ -618,10 +665,10 @@ int gbq_ffn_fused(const void *x, const int8_t *wg8, const float *s_gate, const i
     float *hs = (float *)w.take((size_t)M * 4);
     int32_t *l1x = (int32_t *)w.take((size_t)M * 4 * ((d + 1023) / 1024));  // block L1 norms: preferred size only
     int32_t *l1h = (int32_t *)w.take((size_t)M * 4 * ((H + 1023) / 1024));
-    if (!rotq_writes_l1(logd, rot_d.groups)) l1x = nullptr;
-    if (!rotq_writes_l1(logh, rot_h.groups)) l1h = nullptr;
+    if (!rotq_writes_l1(rsd.logn, rsd.groups)) l1x = nullptr;
+    if (!rotq_writes_l1(rsh.logn, rsh.groups)) l1h = nullptr;
     // 1) rotate + quantize x over d
-    rc = quantize_f16q("gbq_ffn_fused (x)", x, d, qx, xs, M, d, rot_d, logd, st, l1x);
+    rc = quantize_f16q("gbq_ffn_fused (x)", x, d, qx, xs, M, d, rsd, st, l1x);
     if (rc) return rc;
     // 2) gate and up GEMMs in one launch over the virtual weight [W_gate; W_up],
     //    dequantized to bf16 g | u (row stride 2H)
@@ -645,7 +692,7 @@ int gbq_ffn_fused(const void *x, const int8_t *wg8, const float *s_gate, const i
     a.out_l1 = l1h;
     a.M = M;
     a.K = H;
-    rc = run_rotq("gbq_ffn_fused (h)", rot_h, logh, IN_GLU_BF16, OUT_F16Q, a, st);
+    rc = run_rotq("gbq_ffn_fused (h)", rsh, IN_GLU_BF16, OUT_F16Q, a, st);
     if (rc) return rc;
     // 4) down GEMM + dequant
     I8GemmProblem gd = gemm_problem(dv, qh, wd8, M, d, H, EPI_DEQUANT_BF16, y, d, hs, s_down, nullptr);
@@ -684,8 +731,8 @@ int gbq_linear_dx_int8(const void *dy, const int8_t *w8, const float *w_scale, v
     int rc = check_gemm_sizes("gbq_linear_dx_int8", M, K, N);
     if (rc) return rc;
     REQUIRE(K % 16 == 0, "gbq_linear_dx_int8: K must be a multiple of 16");
-    int logn = 0;
-    rc = check_rot(rot, K, &logn);
+    RotSel rs{};
+    rc = check_rot(rot, K, &rs);
     if (rc) return rc;
     if (M == 0) return GBQ_OK;
     REQUIRE(a16(dy) && a16(w8) && a16(w_scale) && a16(dx),
@@ -699,7 +746,8 @@ int gbq_linear_dx_int8(const void *dy, const int8_t *w8, const float *w_scale, v
     float *t = (float *)w.take((size_t)M * 4);
     float *dxr = (float *)w.take((size_t)M * K * 4);
     int32_t *l1 = (int32_t *)w.take((size_t)M * 4 * ((N + 1023) / 1024));  // block L1 norms: preferred size only
-    if (logn == 0) return fail(GBQ_ENOTSUP, "gbq_linear_dx_int8: identity rotation not supported");
+    if (rs.logn == 0 && !rotg_fits(K))
+        return fail(GBQ_ENOTSUP, "gbq_linear_dx_int8: identity rotation needs K <= %lld", (long long)kGenMaxK);
     // A long contraction splits in two halves run side by side on two streams, each GEMM on half the CTA
     // pairs: the 256 x 256 tiles then fill the SMs in about twice as many waves of half-length tiles
     // (M = K = 4096: 6.7 waves of halves against 3.4 of whole tiles, whose last wave leaves most SMs idle).
@@ -743,7 +791,7 @@ int gbq_linear_dx_int8(const void *dy, const int8_t *w8, const float *w_scale, v
         if (rc) return rc;
         // 3) dx = bf16(dx_rot R)
         a.in0 = dxr;
-        return run_rotq("gbq_linear_dx_int8 (rotate dx)", rot, logn, IN_F32, OUT_BF16, a, st);
+        return run_rotq("gbq_linear_dx_int8 (rotate dx)", rs, IN_F32, OUT_BF16, a, st);
     }
     // 2) acc[m, k] += sum over each half of n of qd[m, n] w8[n, k], the halves on two streams
     const int64_t nh = N / 2;
@@ -783,7 +831,7 @@ int gbq_linear_dx_int8(const void *dy, const int8_t *w8, const float *w_scale, v
     // 3) dx = bf16((fp32(acc) * t[m]) R)
     a.in0 = acc;
     a.in_scale = t;
-    return run_rotq("gbq_linear_dx_int8 (rotate dx)", rot, logn, IN_ACC_ROWSCALE, OUT_BF16, a, st);
+    return run_rotq("gbq_linear_dx_int8 (rotate dx)", rs, IN_ACC_ROWSCALE, OUT_BF16, a, st);
 }
 
 }  // extern "C"

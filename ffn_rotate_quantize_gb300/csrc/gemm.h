@@ -84,5 +84,10 @@ void prof_end(cudaStream_t st);
 int encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint64_t inner, uint64_t outer,
                    uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
 int gbq_fail(int code, const char *msg);
+// gbq_linear's size and rotation checks, then the device set-up (nothing else; no pointer is read).
+int linear_args_check(const char *what, int64_t M, int64_t N, int64_t K, gbq_rot rot);
+// Per-device set-up of gbq_linear_noalloc's static scratch (noalloc.cu), run by the library's device
+// set-up with `dev` current: looks up the array's device address once.
+int noalloc_setup_current(int dev);
 
 }  // namespace gbq

@@ -33,8 +33,15 @@ cudaError_t launch_quant_identity(int out_kind, IdArgs a, cudaStream_t st);
 cudaError_t launch_dequant_weight64(const int8_t *w8, const float *w_scale, void *out, int64_t N, int groups,
                                     int num_sms, cudaStream_t st);
 
+// The rotation for every descriptor (rotate_g.cu): any powers of two a = 2^la, b = 2^lb
+// (la = lb = 0: the identity, quantization or conversion only), rows of K values with
+// K % 16 == 0 and K <= kGenMaxK.  Bit-identical to the square kernels where both apply.
+constexpr int64_t kGenMaxK = 49152;
+bool rotg_fits(int64_t K);
+cudaError_t launch_rotg(int in_kind, int out_kind, const RotArgs &a, int la, int lb, cudaStream_t st);
+
 // Whether the rotate+quantize launch for this rotation fills RotArgs::out_l1 (the three-pass
-// kernels: n = 64 or 128, one group per row); elsewhere out_l1 is left untouched.
+// kernels: a = b = 64 or 128, one group per row); elsewhere out_l1 is left untouched.
 inline bool rotq_writes_l1(int logn, int groups) { return (logn == 6 || logn == 7) && groups == 1; }
 
 // Threads of one rotq launch row (G groups of n/CPT threads).

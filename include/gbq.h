@@ -30,7 +30,15 @@
  * K = a*b*groups.  H_n = H4^(x)j for n = 4^j (H4 as printed in the page's
  * "Algorithm: fused ConvRot rotation"), H_n = H2 (x) H4^(x)j for n = 2*4^j
  * (H2 on the most significant index bit; the page is silent there).
- * a = b = 1 is the identity.  Supported: a = b in {1, 16, 32, 64, 128}.
+ * a = b = 1 is the identity.  Any powers of two a, b >= 1 with a*b*groups = K
+ * are accepted (a != b included).  a = b in {16, 32, 64, 128} with at most
+ * 64, 32, 8, 2 groups run the square kernels; every other shape runs one
+ * generic kernel, which needs K % 16 == 0 and K <= 49152 (GBQ_ENOTSUP
+ * otherwise).  Where both could serve a descriptor they give identical values:
+ * the levels of a descriptor (H4/2 on a base-4 digit of the group index, or an
+ * unnormalised H2 on one bit, whose factor is removed once at the end: an exact
+ * halving for two of them, a multiplication by fl(sqrt(1/2)) for one) run in one
+ * fixed order with the same fp32 operations in every kernel.
  * R is symmetric and orthogonal, so rotating x and the weight rows by the
  * same R leaves x @ W^T unchanged.
  */
@@ -64,7 +72,9 @@ typedef struct gbq_rot {
 
 /* Selects nothing, checks that the current device is an sm_103 GPU and sets up
  * per-device state (device status word, driver entry point for TMA
- * descriptors).  Called implicitly by every entry point; safe to call again. */
+ * descriptors, a second stream, and the 16 MiB static scratch of
+ * gbq_linear_noalloc).  Called implicitly by every entry point; safe to call
+ * again.  Call it once at start-up, before any stream capture. */
 int gbq_init(void);
 /* Name of the current device ("" before a successful gbq_init). */
 const char *gbq_device_name(void);
@@ -171,7 +181,8 @@ int gbq_dequant(const int32_t *acc, int64_t ld_acc, const float *x_scale,
  * y = linear(x, w8, w_scale, bias) ("Use from Python": bf16 [..,K] -> bf16
  * [..,N]); rotate+quantize, int8 GEMM and the dequant epilogue fused in the
  * GEMM.  Bit-identical to gbq_dequant(gbq_linear_acc(x)).  M = 1..4 runs the
- * decode GEMV path (weight streaming) for a = b <= 64.  Workspace: GBQ_OP_LINEAR.
+ * decode GEMV path (weight streaming) for a = b in {16, 32, 64}; other
+ * rotations run the GEMM (same values).  Workspace: GBQ_OP_LINEAR.
  * At K = 4096 (a = b = 64, one group) the decode kernel is launched with
  * programmatic stream serialization: it may start while the kernel before it on
  * the stream is still running, but reads none of its inputs (x, w8, w_scale,
@@ -186,21 +197,24 @@ int gbq_linear(const void *x, const int8_t *w8, const float *w_scale, const void
 /*
  * y = linear(x, w8, w_scale, bias) with no workspace argument: the same
  * computation and kernels as gbq_linear, with the scratch taken from a 16 MiB
- * static device array inside the library instead of a caller workspace.  The
- * method's API ("Use from C") has no counterpart to it; it exists for callers that
- * cannot allocate device memory at the point of the call (a plugin inside a
- * framework that owns all device memory through its own pool, or a
- * latency-critical loop that cannot afford cudaMalloc's implicit
- * synchronisation).
+ * static device array inside the library instead of a caller workspace.  It is
+ * outside the method; it exists for callers that cannot allocate device memory
+ * at the point of the call (a plugin inside a framework that owns all device
+ * memory through its own pool, or a latency-critical loop that cannot afford
+ * cudaMalloc's implicit synchronisation).
  * Limit: M*K*2 + M*4 bytes (each part rounded up to 256) must fit in 16 MiB,
  * e.g. M*K <= ~8.3 million; larger calls return GBQ_ENOSPC and launch nothing.
- * Every device that loads the library holds the 16 MiB until the process
- * exits.  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  All calls share the one array and it keeps the
- * last call's contents (nothing needs clearing: each call writes all the
- * scratch it reads); calls that overlap on the GPU -- on different streams,
- * or from different host threads -- race on it.  Allocates nothing.
+ * Sizes and the rotation are checked first, exactly as by gbq_linear.
+ * The array is reserved, and its device address looked up (cudaGetSymbolAddress
+ * with the device current), by the library's per-device set-up: gbq_init() or
+ * the first call of any entry point on that device.  That set-up can therefore
+ * fail with GBQ_ECUDA when the device lacks the 16 MiB; run it (gbq_init) at
+ * start-up, before any stream capture.  Every device set up this way holds the
+ * 16 MiB until the process exits; calls after the set-up allocate nothing.
+ * All calls share the one array and it keeps the last call's contents (nothing
+ * needs clearing: each call writes all the scratch it reads); calls that overlap
+ * on the GPU -- on different streams, or from different host threads -- race
+ * on it.
  */
 int gbq_linear_noalloc(const void *x, const int8_t *w8, const float *w_scale, const void *bias,
                        void *y, int64_t M, int64_t N, int64_t K, gbq_rot rot, void *stream);

@@ -39,12 +39,79 @@ def _err(lib):
 
 def test_bad_rotation_rejected(lib):
     p = ctypes.c_void_p(16)
-    rc = lib.gbq_quantize_act(p, p, p, 4, 256, R(16, 8, 2), None)
-    assert rc == -95 and "supported factors" in _err(lib)
+    rc = lib.gbq_quantize_act(p, p, p, 4, 8, R(2, 4, 1), None)  # valid, but rows of 8 values
+    assert rc == -95 and "K % 16 == 0" in _err(lib)
+    rc = lib.gbq_quantize_act(p, p, p, 4, 65536, R(128, 512, 1), None)  # valid, but beyond the generic kernel
+    assert rc == -95 and "K <= 49152" in _err(lib)
     rc = lib.gbq_quantize_act(p, p, p, 4, 256, R(16, 16, 2), None)
     assert rc == -22 and "!= K" in _err(lib)
     rc = lib.gbq_quantize_act(p, p, p, 4, 256, R(3, 16, 1), None)
     assert rc == -22 and "powers of two" in _err(lib)
+
+
+# Every power-of-two factor pair of the rotation descriptor (a != b, small factors, many groups) is
+# accepted by every rotation entry point; M = 0 runs the full argument check and launches nothing.
+ACCEPTED = [(32, 64, 1), (64, 32, 1), (64, 128, 1), (128, 64, 1), (16, 32, 1), (32, 16, 2), (2, 32, 1),
+            (8, 8, 1), (4, 16, 4), (16, 4, 1), (2, 2, 16), (1, 64, 1), (64, 1, 2), (256, 8, 1), (16, 16, 128),
+            (64, 64, 9), (128, 128, 3)]
+
+
+@pytest.mark.parametrize("rot", ACCEPTED)
+def test_every_descriptor_accepted(lib, rot):
+    p = ctypes.c_void_p(256)
+    K = rot[0] * rot[1] * rot[2]
+    r = R(*rot)
+    calls = {
+        "quantize_act": lambda: lib.gbq_quantize_act(p, p, p, 0, K, r, None),
+        "quantize_act_glu": lambda: lib.gbq_quantize_act_glu(p, p, p, p, 0, K, r, None),
+        "dequant_act_quantize": lambda: lib.gbq_dequant_act_quantize(p, p, K, p, p, p, p, p, 0, K, r, None),
+        "prepare_weight": lambda: lib.gbq_prepare_weight(p, p, p, 0, K, r, None),
+        "rotate_bf16": lambda: lib.gbq_rotate_bf16(p, p, 0, K, r, None),
+        "dequant_weight": lambda: lib.gbq_dequant_weight(p, p, p, 0, K, r, None),
+    }
+    if K % 64 == 0:
+        calls.update({
+            "linear_acc": lambda: lib.gbq_linear_acc(p, p, p, 64, p, 0, 64, K, r, p, 1 << 20, None),
+            "linear": lambda: lib.gbq_linear(p, p, p, None, p, 0, 64, K, r, None, 0, None),
+            "linear_noalloc": lambda: lib.gbq_linear_noalloc(p, p, p, None, p, 0, 64, K, r, None),
+            "linear_dx_int8": lambda: lib.gbq_linear_dx_int8(p, p, p, p, 0, 1024, K, r, None, 0, None),
+        })
+    if K % 128 == 0:
+        calls["ffn_fused (rot_h)"] = lambda: lib.gbq_ffn_fused(p, p, p, p, p, p, p, p, 0, 256, K, R(16, 16, 1), r,
+                                                               None, 0, None)
+        calls["ffn_fused (rot_d)"] = lambda: lib.gbq_ffn_fused(p, p, p, p, p, p, p, p, 0, K, 256, r, R(16, 16, 1),
+                                                               None, 0, None)
+    failed = {name: (rc, _err(lib)) for name, call in calls.items() if (rc := call()) != 0}
+    assert not failed, failed
+
+
+def test_identity_accepted_where_it_was_refused(lib):
+    """The identity descriptor on the outputs that used to need a rotation (dx, the FFN hidden, the fused
+    dequant-activation-quantize): accepted like every other descriptor."""
+    p = ctypes.c_void_p(256)
+    ident = lambda k: R(1, 1, k)
+    assert lib.gbq_linear_dx_int8(p, p, p, p, 0, 1024, 256, ident(256), None, 0, None) == 0, _err(lib)
+    assert lib.gbq_ffn_fused(p, p, p, p, p, p, p, p, 0, 256, 1024, R(16, 16, 1), ident(1024), None, 0, None) == 0
+    assert lib.gbq_dequant_act_quantize(p, p, 256, p, p, p, p, p, 0, 256, ident(256), None) == 0
+
+
+def test_noalloc_checks_arguments_before_its_scratch(lib):
+    """gbq_linear_noalloc runs gbq_linear's size and rotation checks first: a K that is not a multiple of 64
+    is GBQ_EINVAL even when M is far beyond the static scratch, and a bad rotation is reported as such."""
+    p = ctypes.c_void_p(256)
+    assert lib.gbq_linear_noalloc(p, p, p, None, p, 1 << 20, 64, 100, R(1, 1, 100), None) == -22
+    assert "multiple of 64" in _err(lib)
+    assert lib.gbq_linear_noalloc(p, p, p, None, p, 1 << 20, 64, 4096, R(64, 64, 2), None) == -22
+    assert "!= K" in _err(lib)
+
+
+def test_noalloc_without_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    p = ctypes.c_void_p(256)
+    # valid sizes: the device set-up comes next and reports the missing device (not a scratch error)
+    assert lib.gbq_linear_noalloc(p, p, p, None, p, 1 << 20, 64, 4096, R(64, 64, 1), None) == -19
 
 
 def test_bad_sizes_and_pointers_rejected(lib):

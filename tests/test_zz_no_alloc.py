@@ -57,6 +57,44 @@ def test_noalloc_matches_linear_on_two_calls(ops, M, K, N, rot, with_bias):
     assert ops.device_status() == 0
 
 
+def _linear_pair(ops, M, K, N, rot, seed, with_bias=True):
+    """(noalloc output, gbq_linear output on a caller workspace) for one seeded case."""
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    c = I.linear_case(M, K, N, n_outliers=max(1, K // 100), outlier_scale=30.0, bias_std=0.01, seed=seed)
+    w8, ws = O.prepare_weight(c["w"], rot)
+    x = bf16_dev(c["x"])
+    bias = bf16_dev(c["bias"]) if with_bias else None
+    y_ref = ops.linear(x, d(w8), d(ws), bias, rot)
+    y = torch.empty_like(y_ref)
+    rc = _call_noalloc(x, d(w8), d(ws), bias, y, rot)
+    assert rc == 0, L.lib().gbq_last_error().decode()
+    torch.cuda.synchronize()
+    return y, y_ref
+
+
+def test_noalloc_large_call_then_smaller_calls(ops):
+    """A call that fills most of the scratch, then smaller ones (whose scratch is a prefix of what the large
+    call wrote), then a non-square rotation: every result equals gbq_linear on a workspace, bit for bit, so
+    nothing left in the shared array by an earlier call reaches a later one."""
+    cases = [(1500, 4096, 256, (64, 64, 1)), (37, 4096, 300, (64, 64, 1)), (2, 4096, 520, (64, 64, 1)),
+             (129, 2048, 200, (32, 64, 1))]
+    for i, (M, K, N, rot) in enumerate(cases):
+        y, y_ref = _linear_pair(ops, M, K, N, rot, seed=300 + i)
+        assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16)), (M, K, N, rot)
+    assert ops.device_status() == 0
+
+
+def test_noalloc_at_its_limit(ops):
+    """M = 2047, K = 4096: codes and scales take exactly the 16 MiB, so the optional per-block code sums
+    do not fit and the GEMM runs its default exact chunks; still bit-identical to gbq_linear with the
+    full workspace (which has room for the sums)."""
+    M, K, N, rot = 2047, 4096, 256, (64, 64, 1)
+    assert M * K * 2 + (M * 4 + 255) // 256 * 256 == 16 << 20
+    y, y_ref = _linear_pair(ops, M, K, N, rot, seed=400, with_bias=False)
+    assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
+    assert ops.device_status() == 0
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch(ops):
     M, K, N = 2048, 8192, 256  # 32 MiB of codes > the 16 MiB static scratch
     x = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
