@@ -14,12 +14,14 @@ synthetic workload (shapes and distributions of the method's configurations):
   rotated bf16     the page's fair comparator on the prefill shape: rotate-only kernel on x,
                    then a bf16 linear against the pre-rotated bf16 weight (+ bias); the
                    line reports the int8 layer's speedup over it
+  quantize_act     x [4096,16384] rotated + quantized as H128 (x) H128 (the three-pass
+                   kernel) and as H64 (x) H256 (the generic-descriptor kernel)
 Inputs are resident in HBM; L2 is flushed (a 512 MB write, then a read of the
 same buffer so that its dirty lines are written back too) before every timed
 operation, outside its CUDA-event window.  `value` is the prefill linear's
 throughput 2*M*N*K / t.  The int8 contraction runs exactly on the f16 tensor
-pipe (sm_103a has no int8 MMA kind), so its roofline peak is the measured dense
-f16/bf16 figure.
+pipe (sm_103a has no int8 MMA kind; its legacy mma.sync int8 path peaks at
+158 TOPS, measured), so its roofline peak is the measured dense f16/bf16 figure.
 
 --impl reference times the CPU oracle (the only other implementation that
 exists) on a bounded sample of the same workload.
@@ -44,6 +46,7 @@ PREFILL = dict(M=1024, K=4096, N=14336, rot=(64, 64, 1))
 DECODE = dict(M=1, K=4096, N=4096, rot=(64, 64, 1))
 FFN = dict(M=1024, d=4096, H=16384, rot_d=(64, 64, 1), rot_h=(128, 128, 1))
 BWD = dict(M=4096, N=16384, K=4096, rot=(64, 64, 1))
+QACT = dict(M=4096, K=16384)  # activation rotate+quantize rows: square (128 x 128) vs non-square (64 x 256)
 DECODE_BYTES = 4096 * 4096 + 4096 * 4 + 4096 * 2 + 4096 * 2  # W8 + s + x + y
 DEQW_BYTES = 16384 * 4096 * 3 + 16384 * 4  # int8 read + bf16 write + scales
 WORKLOAD = ("prefill INT8 linear x[1024,4096] @ W8[14336,4096]^T + bias, R=H64(x)H64/64; "
@@ -263,6 +266,16 @@ def run_ours(args):
             ops.append(("linear_dx", lambda i: G.linear_dx(dy5, what, out=dx)))
         if want("linear_dx_int8"):
             ops.append(("linear_dx_int8", lambda i: G.linear_dx_int8(dy5, w85, s5, BWD["rot"], ws_dx8, out=dx8)))
+    if want("quantize_act_128x128", "quantize_act_64x256"):
+        # The activation rotate+quantize of a 16384-wide row as a square descriptor (the three-pass kernel)
+        # and as a non-square one of the same width (the generic-descriptor kernel).
+        xq = bf(I.bf16_bits(np.random.default_rng(5).standard_normal((QACT["M"], QACT["K"]), dtype=np.float32)))
+        qq = torch.empty((QACT["M"], QACT["K"]), dtype=torch.int8, device=dev)
+        sq = torch.empty((QACT["M"],), dtype=torch.float32, device=dev)
+        for name, r in (("quantize_act_128x128", (128, 128, 1)), ("quantize_act_64x256", (64, 256, 1))):
+            if want(name):
+                ops.append((name, lambda i, r=r: G.lib().gbq_quantize_act(
+                    G._ptr(xq), G._ptr(qq), G._ptr(sq), QACT["M"], QACT["K"], G._rot(r), G._stream())))
     opfn = dict(ops)
     work = {  # algorithmic units per call
         "linear": (2.0 * M3 * N3 * K3, "TOPS"),
@@ -274,6 +287,8 @@ def run_ours(args):
         "linear_dx": (2.0 * BWD["M"] * BWD["N"] * BWD["K"], "TFLOP/s"),
         "linear_dx_int8": (2.0 * BWD["M"] * BWD["N"] * BWD["K"], "TOPS"),
         "linear_bf16_rotated": (2.0 * M3 * N3 * K3, "TFLOP/s"),
+        "quantize_act_128x128": (float(QACT["M"] * QACT["K"] * 3 + QACT["M"] * 4), "GB/s"),
+        "quantize_act_64x256": (float(QACT["M"] * QACT["K"] * 3 + QACT["M"] * 4), "GB/s"),
     }
     evs = {name: [] for name, _ in ops}
 
@@ -355,7 +370,8 @@ def run_ours(args):
                 "frac": round(achieved / peaks["bf16"], 4), "traffic": profiled_traffic("i8gemm_kernel"),
                 "ms": round(gemm_ms, 4),
                 "peak_note": f"dense f16/bf16 tensor peak ({peaks['src']}, burst): the int8 contraction runs "
-                             "exactly on the f16 pipe"}
+                             "exactly on the f16 pipe, the fastest int8 route of sm_103a (no tcgen05 int8 kind; "
+                             "mma.sync s8 measured at 158 TOPS)"}
         e2e = measure_e2e(G, torch, dev, x3, w83, s3, b3, ws_lin, args)
     if "decode_gemv" in opfn:
         # gbq_linear at M = 1 is one GEMV launch: time a chain of 32 dependent decode layers (call i reads
@@ -481,50 +497,75 @@ def kernel_ms(G, torch, flush, kind, fn, reps=10):
 def measure_e2e(G, torch, dev, x3, w83, s3, b3, ws_lin, args):
     """Prefill linear through the public API with pinned host input/output copies inside the timed region.
 
-    The rows are independent, so the step runs as a user overlapping transfers would: two row halves on two
-    streams (each with its own workspace), each half's host->device copy, linear and device->host copy in
-    order on its stream, so one half's transfers overlap the other's compute. The result equals a single
-    call's bit for bit (checked once)."""
+    The rows are independent, so the step runs as a user overlapping transfers would: four chunks of 256
+    token rows (one GEMM token tile each) on three streams -- host->device copies on one, the linear layer
+    on a second (chunk c waits for its copy), device->host copies on a third (chunk c waits for its linear)
+    -- so every transfer after the first chunk's overlaps compute and the other direction. The result
+    equals a single call's bit for bit (checked once). The copy-only floor moves the same bytes with the
+    two directions concurrent and no compute."""
     M, N = PREFILL["M"], PREFILL["N"]
-    chunks, nst = 2, 2
+    chunks = 4
     xh = x3.cpu().pin_memory()
     yh = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
     xd = torch.empty_like(x3)
     yd = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     main = torch.cuda.current_stream()
-    streams = [torch.cuda.Stream() for _ in range(nst)]
-    wss = [ws_lin] + [torch.empty_like(ws_lin) for _ in range(nst - 1)]
+    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     rows = M // chunks
     ref = G.linear(x3, w83, s3, b3, PREFILL["rot"], ws_lin).cpu()
-    times = []
-    for i in range(args.warmup + args.steps):
-        flush_l2(flush)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(main)
-        for s in streams:
-            s.wait_event(e0)
+    ev = lambda: torch.cuda.Event()
+
+    def step():
+        e_in = [ev() for _ in range(chunks)]
+        e_comp = [ev() for _ in range(chunks)]
         for c in range(chunks):
-            s, r0, r1 = streams[c % nst], c * rows, (c + 1) * rows
-            with torch.cuda.stream(s):
+            r0, r1 = c * rows, (c + 1) * rows
+            with torch.cuda.stream(s_in):
                 xd[r0:r1].copy_(xh[r0:r1], non_blocking=True)
-                G.linear(xd[r0:r1], w83, s3, b3, PREFILL["rot"], wss[c % nst], out=yd[r0:r1])
+                e_in[c].record(s_in)
+            with torch.cuda.stream(s_comp):
+                s_comp.wait_event(e_in[c])
+                G.linear(xd[r0:r1], w83, s3, b3, PREFILL["rot"], ws_lin, out=yd[r0:r1])
+                e_comp[c].record(s_comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(e_comp[c])
                 yh[r0:r1].copy_(yd[r0:r1], non_blocking=True)
-        for s in streams:
-            ev = torch.cuda.Event()
-            ev.record(s)
-            main.wait_event(ev)
-        e1.record(main)
-        torch.cuda.synchronize()
-        if i >= args.warmup:
-            times.append(e0.elapsed_time(e1))
+
+    def copies_only():
+        with torch.cuda.stream(s_in):
+            xd.copy_(xh, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            yh.copy_(yd, non_blocking=True)
+
+    def timed(fn):
+        times = []
+        for i in range(args.warmup + args.steps):
+            flush_l2(flush)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(main)
+            for s in (s_in, s_comp, s_out):
+                s.wait_event(e0)
+            fn()
+            for s in (s_in, s_comp, s_out):
+                e = ev()
+                e.record(s)
+                main.wait_event(e)
+            e1.record(main)
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                times.append(e0.elapsed_time(e1))
+        return float(np.median(times))
+
+    ms = timed(step)
     assert torch.equal(yh.view(torch.int16), ref.view(torch.int16)), "chunked e2e result differs"
-    ms = float(np.median(times))
+    copy_ms = timed(copies_only)
     units = 2.0 * M * N * PREFILL["K"]
     return {"value": round(units / (ms * 1e-3) * 1e-12, 2), "unit": "TOPS", "ms": round(ms, 4),
             "h2d_bytes_per_step": int(xh.numel() * 2), "d2h_bytes_per_step": int(yh.numel() * 2),
-            "pipeline": f"{chunks} row chunks on {nst} streams: copy in, linear, copy out per chunk"}
+            "copy_only_ms": round(copy_ms, 4), "vs_copy_only": round(ms / copy_ms, 3),
+            "pipeline": f"{chunks} chunks of {rows} token rows on 3 streams (copy in | linear | copy out)"}
 
 
 # ---------------------------------------------------------------------------------------------

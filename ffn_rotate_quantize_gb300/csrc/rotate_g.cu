@@ -123,36 +123,64 @@ __device__ __forceinline__ void gen_load8(const GenArgs &p, int64_t grow, int co
     }
 }
 
-// ---- one level on register bits [RB, RB + W) of a thread's values.
-template <int W, int RB, int NV>
+// ---- one level on register bits [RB, RB + W) of a thread's values; with PB >= 0 the values are taken
+// in pairs across register bit PB (outside the level's bits), so each operation runs on the packed
+// fp32x2 pipe.  Per value the operations are the scalar ones.
+template <int W, int RB, int NV, int PB>
 __device__ __forceinline__ void gen_level(float (&v)[NV]) {
     if constexpr (W == 2) {
 #pragma unroll
         for (int base = 0; base < NV; ++base) {
             if ((base >> RB) & 3) continue;
+            if (PB >= 0 && ((base >> (PB < 0 ? 0 : PB)) & 1)) continue;
             const int b1 = base | (1 << RB), b2 = base | (2 << RB), b3 = base | (3 << RB);
-            const float x0 = v[base], x1 = v[b1], x2 = v[b2], x3 = v[b3];
-            const float h = __fmul_rn(__fadd_rn(__fadd_rn(x0, x1), __fadd_rn(x2, x3)), 0.5f);  // exact halving
-            v[base] = __fmaf_rn(x3, -1.0f, h);
-            v[b1] = __fmaf_rn(x2, -1.0f, h);
-            v[b2] = __fmaf_rn(x1, -1.0f, h);
-            v[b3] = __fmaf_rn(x0, -1.0f, h);
+            if constexpr (PB >= 0) {
+                constexpr int o = 1 << (PB < 0 ? 0 : PB);
+                const float2 x0 = make_float2(v[base], v[base | o]), x1 = make_float2(v[b1], v[b1 | o]);
+                const float2 x2 = make_float2(v[b2], v[b2 | o]), x3 = make_float2(v[b3], v[b3 | o]);
+                const float2 m1 = make_float2(-1.0f, -1.0f);
+                const float2 h = __fmul2_rn(__fadd2_rn(__fadd2_rn(x0, x1), __fadd2_rn(x2, x3)), make_float2(0.5f, 0.5f));
+                const float2 y0 = __ffma2_rn(x3, m1, h), y1 = __ffma2_rn(x2, m1, h);
+                const float2 y2 = __ffma2_rn(x1, m1, h), y3 = __ffma2_rn(x0, m1, h);
+                v[base] = y0.x; v[base | o] = y0.y;
+                v[b1] = y1.x; v[b1 | o] = y1.y;
+                v[b2] = y2.x; v[b2 | o] = y2.y;
+                v[b3] = y3.x; v[b3 | o] = y3.y;
+            } else {
+                const float x0 = v[base], x1 = v[b1], x2 = v[b2], x3 = v[b3];
+                const float h = __fmul_rn(__fadd_rn(__fadd_rn(x0, x1), __fadd_rn(x2, x3)), 0.5f);  // exact halving
+                v[base] = __fmaf_rn(x3, -1.0f, h);
+                v[b1] = __fmaf_rn(x2, -1.0f, h);
+                v[b2] = __fmaf_rn(x1, -1.0f, h);
+                v[b3] = __fmaf_rn(x0, -1.0f, h);
+            }
         }
     } else if constexpr (W == 1) {
 #pragma unroll
         for (int base = 0; base < NV; ++base) {
             if ((base >> RB) & 1) continue;
+            if (PB >= 0 && ((base >> (PB < 0 ? 0 : PB)) & 1)) continue;
             const int b1 = base | (1 << RB);
-            const float a = v[base], b = v[b1];
-            v[base] = __fadd_rn(a, b);
-            v[b1] = __fmaf_rn(b, -1.0f, a);
+            if constexpr (PB >= 0) {
+                constexpr int o = 1 << (PB < 0 ? 0 : PB);
+                const float2 a = make_float2(v[base], v[base | o]), b = make_float2(v[b1], v[b1 | o]);
+                const float2 sm = __fadd2_rn(a, b), df = __ffma2_rn(b, make_float2(-1.0f, -1.0f), a);
+                v[base] = sm.x; v[base | o] = sm.y;
+                v[b1] = df.x; v[b1 | o] = df.y;
+            } else {
+                const float a = v[base], b = v[b1];
+                v[base] = __fadd_rn(a, b);
+                v[b1] = __fmaf_rn(b, -1.0f, a);
+            }
         }
     }
 }
 
 // ---- one pass: the levels (p1, W1) and, when W2 > 0, (p2, W2), on every item of the chunk.
 // An item is the 2^(W1+W2) values whose group indices differ only in those bits; items are
-// enumerated by inserting zero bits at the two positions into the item number.
+// enumerated by inserting zero bits at the two positions into the item number.  An item's base index
+// and its offsets use disjoint bits, so the padded index is tix(base) + tix(offset): the offsets are
+// computed once per pass.
 template <int W1, int W2, bool LAST, int OUT>
 __device__ __forceinline__ void gen_pass(float *T, int E, int p1, int p2, const GenArgs &p, unsigned int *rowmax) {
     constexpr int NV = 1 << (W1 + W2);
@@ -164,19 +192,22 @@ __device__ __forceinline__ void gen_pass(float *T, int E, int p1, int p2, const 
         ph = p1;
         wh = W1;
     }
+    int toff[NV];
+#pragma unroll
+    for (int r = 0; r < NV; ++r) {
+        const int d1 = r & ((1 << W1) - 1), d2 = r >> W1;
+        toff[r] = tix(d1 << p1) + (W2 > 0 ? tix(d2 << p2) : 0);
+    }
     for (int w = threadIdx.x; w < items; w += kGenThreads) {
         int base = (w & ((1 << pl) - 1)) | ((w >> pl) << (pl + wl));
         if (W2 > 0) base = (base & ((1 << ph) - 1)) | ((base >> ph) << (ph + wh));
-        int idx[NV];
+        float *tb = T + tix(base);
         float v[NV];
 #pragma unroll
-        for (int r = 0; r < NV; ++r) {
-            const int d1 = r & ((1 << W1) - 1), d2 = r >> W1;
-            idx[r] = tix(base + (d1 << p1) + (W2 > 0 ? (d2 << p2) : 0));
-            v[r] = T[idx[r]];
-        }
-        gen_level<W1, 0, NV>(v);
-        gen_level<W2, W1, NV>(v);
+        for (int r = 0; r < NV; ++r) v[r] = tb[toff[r]];
+        // level 1 pairs across the top register bit (level 2's), level 2 across register bit 0
+        gen_level<W1, 0, NV, (W2 > 0 ? W1 + W2 - 1 : -1)>(v);
+        gen_level<W2, W1, NV, 0>(v);
         if constexpr (LAST) {
             if (p.post != 1.0f) {
 #pragma unroll
@@ -190,7 +221,7 @@ __device__ __forceinline__ void gen_pass(float *T, int E, int p1, int p2, const 
             }
         }
 #pragma unroll
-        for (int r = 0; r < NV; ++r) T[idx[r]] = v[r];
+        for (int r = 0; r < NV; ++r) tb[toff[r]] = v[r];
     }
 }
 
