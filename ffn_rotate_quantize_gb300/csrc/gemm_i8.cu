@@ -105,6 +105,7 @@ struct Params {
     int epi;
     int use_tma_out;
     int reduce_out;  // EPI_ACC_I32: add into out instead of storing
+    int wfast;       // tile order: weight blocks fastest (see tile_coords)
 };
 
 struct Bars {
@@ -123,10 +124,23 @@ struct Bars {
 
 static_assert(sizeof(Bars) <= 1024, "barriers exceed their shared-memory slot");
 
-// Pair tile t: weight rows [n0, n0 + 256), tokens [m0, m0 + 256).
-__device__ __forceinline__ void tile_coords(int64_t t, int64_t m_tiles, int64_t *n0, int64_t *m0) {
-    *n0 = (t / m_tiles) * kPairM;
-    *m0 = (t % m_tiles) * kBN;
+// Pair tile t: weight rows [n0, n0 + 256), tokens [m0, m0 + 256).  Consecutive tiles (run side by side
+// by consecutive CTA pairs) share their weight block and walk the token tiles, so each wave reads its
+// few weight blocks once and re-reads the token operand from L2 -- unless the token operand is the
+// larger one per unit of K (wfast: more token bytes than weight bytes, e.g. the dx contraction over
+// 4096 tokens), which then walks the weight blocks instead, reading each wave's token tiles once.
+__device__ __forceinline__ void tile_coords(int64_t t, int64_t m_tiles, int64_t n_tiles, int wfast, int64_t *n0,
+                                            int64_t *m0) {
+    if (wfast) {
+        *n0 = (t % n_tiles) * kPairM;
+        *m0 = (t / n_tiles) * kBN;
+    } else {
+        *n0 = (t / m_tiles) * kPairM;
+        *m0 = (t % m_tiles) * kBN;
+    }
+}
+__device__ __forceinline__ int64_t tile_token_index(int64_t t, int64_t m_tiles, int64_t n_tiles, int wfast) {
+    return wfast ? t / n_tiles : t % m_tiles;
 }
 
 // 4 int8 (one 32-bit word, k ascending) -> 2 words of fp16x2 pairs (k, k+1).
@@ -277,7 +291,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) i8gemm_
                 bool ok = true, dep_done = false;
                 for (int64_t t = pair; t < num_tiles && ok; t += npairs) {
                     int64_t n0, m0;
-                    tile_coords(t, m_tiles, &n0, &m0);
+                    tile_coords(t, m_tiles, n_tiles, p.wfast, &n0, &m0);
                     const int64_t nr = n0 + kBM * rank;  // this CTA's weight rows
                     const bool src1 = nr >= p.n_split;
                     const CUtensorMap *tw = src1 ? &p.tm_w1 : &p.tm_w0;
@@ -315,7 +329,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) i8gemm_
                 uint32_t gs = 0, gsub = 0, chunk = 0;
                 bool ok = mbar_wait_cluster(&bars->plan_ready, 0, p.status, abort, peer_abort);
                 for (int64_t t = pair; t < num_tiles && ok; t += npairs) {
-                    const int csubs = tile_chunk_subs(bars->plan, p, t % m_tiles, tile_subs);
+                    const int csubs =
+                        tile_chunk_subs(bars->plan, p, tile_token_index(t, m_tiles, n_tiles, p.wfast), tile_subs);
                     int cpos = 0;  // sub-step within the current chunk (kept incrementally: no division here)
                     for (int kt = 0; kt < KT && ok; ++kt) {
                         const uint32_t my = gs++;
@@ -466,7 +481,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) i8gemm_
         bool ok = true;
         for (int64_t t = pair; t < num_tiles && ok; t += npairs) {
             int64_t n0, m0;
-            tile_coords(t, m_tiles, &n0, &m0);
+            tile_coords(t, m_tiles, n_tiles, p.wfast, &n0, &m0);
             n0 += kBM * rank;                      // this CTA's output columns
             const int64_t n = n0 + q * 32 + lane;  // output column owned by this thread
             const bool n_ok = n < p.N;
@@ -486,7 +501,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) i8gemm_
             int32_t tot[128];  // exact running sums for this thread's 128 token columns
 #pragma unroll
             for (int i = 0; i < 128; ++i) tot[i] = 0;
-            const int csubs = tile_chunk_subs(bars->plan, p, t % m_tiles, tile_subs);
+            const int csubs =
+                tile_chunk_subs(bars->plan, p, tile_token_index(t, m_tiles, n_tiles, p.wfast), tile_subs);
             const int nchunks = (tile_subs + csubs - 1) / csubs;
             for (int c = 0; c < nchunks; ++c) {
                 ok = mbar_wait_cluster(&bars->accfull, chunk & 1u, p.status, abort, peer_abort);
@@ -626,6 +642,7 @@ int launch_i8gemm(const I8GemmProblem &q, cudaStream_t st) {
     p.row_l1 = q.row_l1;
     p.l1_ld = q.l1_ld > 0 ? q.l1_ld : q.K / 1024;
     p.reduce_out = q.reduce_out;
+    p.wfast = 2 * q.M > q.N ? 1 : 0;  // fp16-coded tokens: 2 M bytes per unit of K against N weight bytes
     p.status = q.status;
     p.w_layout = q.w_layout;
     p.epi = q.epi;

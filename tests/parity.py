@@ -88,3 +88,22 @@ def assert_rows_explained(y_gpu_bits, y_ref_bits, same_rows, what="y"):
     nr = np.linalg.norm(y - r) / max(np.linalg.norm(r), 1e-30)
     assert nr <= BF16_NORMREL, f"{what}: norm-rel {nr:.3e} > {BF16_NORMREL}"
     return mr, nr
+
+
+def bf16_half_ulp(v: np.ndarray) -> np.ndarray:
+    """Half the bf16 spacing at |v| (8 significant bits): the largest error of rounding v to bf16."""
+    a = np.abs(np.asarray(v, np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return 2.0 ** (e - 8)
+
+
+def acc_error_usage(y_gpu_bits, exact, n: int) -> float:
+    """How much of the derived accumulation-error bound E*rms (E = (n/16) * 2^-21, the max-rel floor's
+    premise) a tensor-core float dot product of length n used: the largest excess of |y - exact| over the
+    bf16 rounding (half a bf16 unit at the larger of |y|, |exact|), in units of E*rms(exact).  `exact` is the dot
+    product in fp64 (no rounding)."""
+    y = f32(y_gpu_bits).astype(np.float64)
+    x = np.asarray(exact, np.float64)
+    rms = np.sqrt(np.mean(x * x))
+    excess = np.maximum(np.abs(y - x) - bf16_half_ulp(np.maximum(np.abs(x), np.abs(y))), 0.0)
+    return float(excess.max() / ((n / 16.0) * 2.0 ** -21 * rms))

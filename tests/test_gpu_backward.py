@@ -5,7 +5,7 @@ import torch
 
 import oracle as O
 from ffn_rotate_quantize_gb300 import inputs as I
-from parity import assert_bf16_parity, assert_int8_parity, bf16_dev, bf16_np
+from parity import acc_error_usage, assert_bf16_parity, assert_int8_parity, bf16_dev, bf16_np, bf16_half_ulp, f32
 
 pytestmark = pytest.mark.gpu
 
@@ -40,6 +40,11 @@ def test_linear_dx(ops, M, N, K, rot):
     what = O.dequant_weight(w8, s, rot)
     dx = ops.linear_dx(bf16_dev(c["dy"]), bf16_dev(what))
     assert_bf16_parity(bf16_np(dx), O.linear_dx(c["dy"], what), acc_len=N)
+    # The max-rel floor rests on a bound E * rms of the fp32 accumulation error: show how much of it is used.
+    exact = f32(c["dy"]).astype(np.float64) @ f32(what).astype(np.float64)
+    usage = acc_error_usage(bf16_np(dx), exact, N)
+    print(f"linear_dx {M}x{N}x{K}: accumulation error uses {usage:.3g} of E*rms")
+    assert usage <= 0.5
 
 
 @pytest.mark.parametrize("M,N,K,rot", DX_CASES)
@@ -49,6 +54,24 @@ def test_linear_dx_int8(ops, M, N, K, rot):
     dx = ops.linear_dx_int8(bf16_dev(c["dy"]), d(w8), d(s), rot)
     dx_r, mid = O.linear_dx_int8(c["dy"], w8, s, rot, keep=True)
     assert_bf16_parity(bf16_np(dx), dx_r)
+
+
+@pytest.mark.parametrize("N,K,groups", [(300, 4096, 1), (64, 8192, 2), (1000, 4096, 1)])
+def test_dequant_weight_at_its_rounding_bound(ops, N, K, groups):
+    """dequant_weight for H64 (x) H64 transforms the codes exactly and rounds once, W_hat = bf16(fl((W8 s) R));
+    the oracle rounds W8 s to fp32 first and sums in fp64 (reading R-17).  So every element is within one
+    bf16 unit of the oracle's plus the residue of its fp32 roundings, 64 * 127 * s[n] * 2^-24, and not
+    merely within the generic bf16 tolerance."""
+    rot = (64, 64, groups)
+    c = I.backward_case(8, N, K, seed=N + K)
+    w8, s = O.prepare_weight(c["w"], rot)
+    w = f32(bf16_np(ops.dequant_weight(d(w8), d(s), rot))).astype(np.float64)
+    r = f32(O.dequant_weight(w8, s, rot)).astype(np.float64)
+    bound = 2.0 * bf16_half_ulp(np.maximum(np.abs(w), np.abs(r))) + 64 * 127 * s.astype(np.float64)[:, None] * 2.0 ** -24
+    err = np.abs(w - r)
+    assert np.all(err <= bound), f"worst {np.max(err / bound):.3f} of the bound"
+    print(f"dequant_weight {N}x{K}: {np.count_nonzero(err)} of {err.size} elements differ, worst "
+          f"{np.max(err / bound):.3f} of the bound")
 
 
 def test_linear_dx_int8_gemm_exact(ops):

@@ -6,7 +6,7 @@ import torch
 
 import oracle as O
 from ffn_rotate_quantize_gb300 import inputs as I
-from parity import assert_bf16_parity, bf16_dev, bf16_np
+from parity import acc_error_usage, assert_bf16_parity, bf16_dev, bf16_np, f32
 
 pytestmark = pytest.mark.gpu
 
@@ -40,6 +40,12 @@ def test_linear_bf16(ops, M, N, K, with_bias):
     b = I.bf16_bits(rng.standard_normal(N).astype(np.float32) * np.float32(0.05)) if with_bias else None
     y = ops.linear_bf16(bf16_dev(x), bf16_dev(w), bf16_dev(b) if with_bias else None)
     assert_bf16_parity(bf16_np(y), O.linear_bf16(x, w, b), acc_len=K)
+    exact = f32(x).astype(np.float64) @ f32(w).astype(np.float64).T
+    if with_bias:
+        exact = exact + f32(b).astype(np.float64)[None, :]
+    usage = acc_error_usage(bf16_np(y), exact, K)
+    print(f"linear_bf16 {M}x{N}x{K}: accumulation error uses {usage:.3g} of E*rms")
+    assert usage <= 0.5
 
 
 def test_linear_bf16_exact_on_small_integers(ops):

@@ -181,6 +181,39 @@ def test_linear_large_accumulators_exact(ops):
     assert np.abs(O.linear_acc(xb, w8, rot)[0]).max() == 127 * 127 * K
 
 
+def test_linear_acc_extended_chunk_at_its_bound(ops):
+    """The tightest case of the chunk plan: every token's codes are positive and each aligned pair of
+    1024-long blocks sums to just under 2^17, so the tile takes 2048-long exact chunks whose partial sums
+    against all-(+127) weight rows reach 127 * sum|q| ~ 0.99 * 2^24 (a 4096-long chunk would pass 2^24 and
+    round).  x = R v for target codes v (R is symmetric and orthogonal, so x rotates back to v up to the
+    bf16 rounding of x); the accumulators must equal the int64 product of the GPU's own codes."""
+    rot, M, K, N = (64, 64, 1), 300, 4096, 256
+    rng = np.random.default_rng(53)
+    v = rng.integers(51, 79, (M, K)).astype(np.float64)
+    v[:, 0] = 127.0
+    for m in range(M):  # each 2048-long half sums to at most 130300 (a margin for the bf16 rounding of x)
+        for h in range(2):
+            seg = v[m, 2048 * h:2048 * (h + 1)]
+            extra = int(seg.sum() - 130300)
+            if extra > 0:
+                np.subtract.at(seg, rng.integers(1, 2048, extra), 1.0)
+    x = I.bf16_bits(O.rotate(v.astype(np.float32), rot))  # R v (fp64 sums, rounded), then bf16
+    w8 = rng.integers(-127, 128, (N, K)).astype(np.int8)
+    w8[:8] = 127
+    w8[8:16] = np.where(np.arange(K) % 2 == 0, 127, -127)
+    acc, _ = ops.linear_acc(bf16_dev(x), d(w8), rot)
+    q = ops.quantize_act(bf16_dev(x), rot)[0].cpu().numpy().astype(np.int64)
+    assert q.min() >= 0
+    blk = np.abs(q).reshape(M, 4, 1024).sum(axis=2)
+    pairs = blk[:, 0::2] + blk[:, 1::2]
+    assert pairs.max() <= 2 ** 17 and pairs.min() > 2 ** 17 - 2000, (pairs.min(), pairs.max())
+    assert blk.sum(axis=1).min() > 2 ** 17  # a 4096-long chunk would not be exact
+    assert 127 * pairs.max() > 0.98 * 2 ** 24
+    acc_r = O.gemm_s8(q.astype(np.int8), w8)
+    assert np.array_equal(acc.cpu().numpy().astype(np.int64), acc_r)
+    assert acc_r[:, :8].min() > 1.9 * 2 ** 24  # totals far past 2^24, from exact 2048-long chunks
+
+
 def test_linear_acc_chunk_plans_exact(ops):
     """Token tiles whose codes have small sums of |q| over their 1024-long K blocks accumulate
     longer exact fp32 chunks, tiles with large ones (one-hot rows rotate to all-|127| codes) take
