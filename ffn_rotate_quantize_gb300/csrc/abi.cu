@@ -433,11 +433,11 @@ int gbq_dequant_weight(const int8_t *w8, const float *w_scale, void *w, int64_t 
     INIT(d);
     if (rs.logn == 0) {
         REQUIRE(K % 16 == 0, "gbq_dequant_weight: identity rotation needs K %% 16 == 0");
-        cudaError_t e = launch_scale_rows_s8(w8, w_scale, w, N, K, (cudaStream_t)stream);
+        cudaError_t e = launch_scale_rows_s8(w8, w_scale, w, N, K, (cudaStream_t)stream, d->status);
         return e == cudaSuccess ? GBQ_OK : cuda_fail(e, "gbq_dequant_weight");
     }
     if (rot.a == 64 && rot.b == 64) {  // integer-exact two-pass kernel
-        cudaError_t e = launch_dequant_weight64(w8, w_scale, w, N, rot.groups, d->sms, (cudaStream_t)stream);
+        cudaError_t e = launch_dequant_weight64(w8, w_scale, w, N, rot.groups, d->sms, (cudaStream_t)stream, d->status);
         return e == cudaSuccess ? GBQ_OK : cuda_fail(e, "gbq_dequant_weight");
     }
     RotArgs a{};
@@ -557,7 +557,7 @@ int gbq_int8_gemm(const int8_t *q, const int8_t *w8, int32_t *acc, int64_t ld_ac
     cudaStream_t st = (cudaStream_t)stream;
     Ws w{(uint8_t *)workspace, ws_bytes};
     void *qf = w.take((size_t)M * K * 2);
-    cudaError_t e = launch_s8_to_f16(q, qf, M * K, st);
+    cudaError_t e = launch_s8_to_f16(q, qf, M * K, st, d->status);
     if (e != cudaSuccess) return cuda_fail(e, "gbq_int8_gemm (operand coding)");
     I8GemmProblem g = gemm_problem(d, qf, w8, M, N, K, EPI_ACC_I32, acc, ld_acc, nullptr, nullptr, nullptr);
     return launch_i8gemm(g, st);
@@ -600,7 +600,7 @@ int gbq_dequant(const int32_t *acc, int64_t ld_acc, const float *x_scale, const 
                 ((uintptr_t)y & 1) == 0 && ((uintptr_t)bias & 1) == 0,
             "gbq_dequant: pointers must be aligned to their element size");
     INIT(d);
-    cudaError_t e = launch_dequant(acc, ld_acc, x_scale, w_scale, bias, y, ld_y, M, N, (cudaStream_t)stream);
+    cudaError_t e = launch_dequant(acc, ld_acc, x_scale, w_scale, bias, y, ld_y, M, N, (cudaStream_t)stream, d->status);
     return e == cudaSuccess ? GBQ_OK : cuda_fail(e, "gbq_dequant");
 }
 

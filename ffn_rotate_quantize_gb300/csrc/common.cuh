@@ -17,6 +17,22 @@
 
 namespace gbq {
 
+// Debug builds (-DGBQ_DEBUG_BOUNDS) check every computed global-memory access of the kernels against
+// the extent of the tensor it addresses: elements [off, off + len) must lie in [0, extent).  A failed
+// check records GBQ_DEV_BOUNDS in the device status word and the caller skips the access (a load
+// yields zeros); nothing traps.  Release builds compile the checks away.
+__device__ __forceinline__ bool dbg_range_check(unsigned int *status, int64_t off, int64_t len, int64_t extent) {
+    const bool ok = off >= 0 && len >= 0 && off + len <= extent;
+    if (!ok && status) atomicOr(status, GBQ_DEV_BOUNDS);
+    return ok;
+}
+#ifdef GBQ_DEBUG_BOUNDS
+#define GBQ_IN_RANGE(status, off, len, extent) \
+    ::gbq::dbg_range_check((status), (int64_t)(off), (int64_t)(len), (int64_t)(extent))
+#else
+#define GBQ_IN_RANGE(status, off, len, extent) true
+#endif
+
 // Limit for one mbarrier wait, in nanoseconds of %globaltimer.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 

@@ -75,7 +75,7 @@ __device__ __forceinline__ float2 dp4a_pair(uint32_t w, int ra, int rb) {
 __global__ void __launch_bounds__(32, kDqwMinBlocks) dqw64_kernel(const int8_t *__restrict__ w8,
                                                                   const float *__restrict__ w_scale,
                                                                   __nv_bfloat16 *__restrict__ out, int64_t rows,
-                                                                  int groups) {
+                                                                  int groups, unsigned int *status) {
     __shared__ __align__(16) float tile[64 * 64];
     const int L = threadIdx.x;
     int64_t row = blockIdx.x;
@@ -87,8 +87,9 @@ __global__ void __launch_bounds__(32, kDqwMinBlocks) dqw64_kernel(const int8_t *
         if (L == 0 && next < rows) bulk_prefetch_l2(w8 + next * kDqwK, kDqwK);  // the next row waits in L2
         uint4 ld[8];
         const uint4 *src = reinterpret_cast<const uint4 *>(w8 + row * kDqwK);
+        const bool row_ok = GBQ_IN_RANGE(status, row * kDqwK, kDqwK, rows * kDqwK);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) ld[c] = __ldcs(src + L + 32 * c);
+        for (int c = 0; c < 8; ++c) ld[c] = row_ok ? __ldcs(src + L + 32 * c) : make_uint4(0u, 0u, 0u, 0u);
         const float f = __fmul_rn(__ldg(w_scale + row / groups), 0.015625f);
         // ---- pass 1: level j01 (dp4a), j23 (over the words of a chunk), i45 (over the chunks) ----
         float2 p[8][4][2];  // [c = i3 + 2 i45][q = j23][h]: pair (a = 2h, 2h + 1), a = j01
@@ -143,6 +144,7 @@ __global__ void __launch_bounds__(32, kDqwMinBlocks) dqw64_kernel(const int8_t *
 #pragma unroll
             for (int i01 = 0; i01 < 4; ++i01)
                 h4_pairs(v[jj][i01], v[jj][i01 + 4], v[jj][i01 + 8], v[jj][i01 + 12]);  // i23
+        if (!row_ok) continue;
         uint32_t *orow = reinterpret_cast<uint32_t *>(out + row * kDqwK);
         const float2 ff = make_float2(f, f);
 #pragma unroll
@@ -159,7 +161,7 @@ __global__ void __launch_bounds__(32, kDqwMinBlocks) dqw64_kernel(const int8_t *
 
 // W_hat for rotations with n = 64 (rows of `groups` 4096-long groups).  rows = N * groups.
 cudaError_t launch_dequant_weight64(const int8_t *w8, const float *w_scale, void *out, int64_t N, int groups,
-                                    int num_sms, cudaStream_t st) {
+                                    int num_sms, cudaStream_t st, unsigned int *status) {
     const int64_t rows = N * groups;
     if (rows == 0) return cudaSuccess;
     static int per_sm = 0;
@@ -171,7 +173,7 @@ cudaError_t launch_dequant_weight64(const int8_t *w8, const float *w_scale, void
     const int64_t resident = (int64_t)per_sm * (num_sms > 0 ? num_sms : 1);
     const unsigned grid = (unsigned)(rows < resident ? rows : resident);
     prof_begin(0, st);
-    dqw64_kernel<<<grid, 32, 0, st>>>(w8, w_scale, reinterpret_cast<__nv_bfloat16 *>(out), rows, groups);
+    dqw64_kernel<<<grid, 32, 0, st>>>(w8, w_scale, reinterpret_cast<__nv_bfloat16 *>(out), rows, groups, status);
     prof_end(st);
     return cudaGetLastError();
 }

@@ -69,9 +69,10 @@ int launch_gemv(const void *x, const int8_t *w8, const float *w_scale, const voi
 
 // Elementwise helpers.
 cudaError_t launch_dequant(const int32_t *acc, int64_t ld_acc, const float *xs, const float *ws, const void *bias,
-                           void *y, int64_t ld_y, int64_t M, int64_t N, cudaStream_t st);
-cudaError_t launch_s8_to_f16(const int8_t *q, void *out, int64_t n, cudaStream_t st);
-cudaError_t launch_scale_rows_s8(const int8_t *w8, const float *s, void *w, int64_t N, int64_t K, cudaStream_t st);
+                           void *y, int64_t ld_y, int64_t M, int64_t N, cudaStream_t st, unsigned int *status = nullptr);
+cudaError_t launch_s8_to_f16(const int8_t *q, void *out, int64_t n, cudaStream_t st, unsigned int *status = nullptr);
+cudaError_t launch_scale_rows_s8(const int8_t *w8, const float *s, void *w, int64_t N, int64_t K, cudaStream_t st,
+                                 unsigned int *status = nullptr);
 
 size_t gemm_workspace_size(int op, int64_t M, int64_t N, int64_t K, int64_t H);       // minimum
 size_t gemm_workspace_size_pref(int op, int64_t M, int64_t N, int64_t K, int64_t H);  // what gbq_workspace_size reports

@@ -168,7 +168,8 @@ __global__ void __launch_bounds__(kThreads, 1) bf16_gemm_kernel(const __grid_con
                 tmem_ld32(lane_addr + ab * 256 + 32 * j, r);
                 tc_wait_ld();
                 const int64_t kb = k0 + 32 * j;
-                if (m < p.M && kb < p.cols) {
+                if (m < p.M && kb < p.cols &&
+                    GBQ_IN_RANGE(p.status, m * p.cols + kb, min((int64_t)32, p.cols - kb), p.M * p.cols)) {
                     if (p.bias) {  // the same 32 values for every lane: broadcast loads
 #pragma unroll
                         for (int i = 0; i < 32; ++i)

@@ -521,6 +521,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) i8gemm_
                 ++chunk;
             }
             if (!ok) break;
+            // Debug builds: the pair tile's corner lies inside the output (TMA clips the rest; the second
+            // CTA's 128 columns may lie wholly past N in the last tile).
+            if (!(GBQ_IN_RANGE(p.status, m0, 1, p.M) && GBQ_IN_RANGE(p.status, n0 - kBM * rank, 1, p.N))) continue;
             if (p.use_tma_out) {
                 uint8_t *mine = obuf + (uint32_t)(warp - 8) * 2 * kOutBlock;
                 if (p.epi == EPI_ACC_I32)

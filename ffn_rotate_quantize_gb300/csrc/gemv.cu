@@ -91,7 +91,8 @@ __device__ __forceinline__ void gemv_dot_phase(const GemvArgs &p, uint8_t *stage
                     if (lane == m) a = acc[m];
                 const float b = p.bias ? __bfloat162float(p.bias[n]) : 0.0f;
                 const float tv = __fmul_rn(__int2float_rn(a), xs_s[lane]);
-                p.y[(int64_t)lane * p.N + n] = __float2bfloat16_rn(__fmaf_rn(tv, __ldg(p.ws + n), b));
+                if (GBQ_IN_RANGE(p.status, (int64_t)lane * p.N + n, 1, p.M * p.N))
+                    p.y[(int64_t)lane * p.N + n] = __float2bfloat16_rn(__fmaf_rn(tv, __ldg(p.ws + n), b));
             }
         }
         __syncthreads();
@@ -118,6 +119,8 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(GemvArgs p) {
     const int64_t r0 = (int64_t)blockIdx.x * p.rows_per_cta;
     const int64_t r1 = min(p.N, r0 + p.rows_per_cta);
     const int nrows = (int)(r1 - r0);
+    // Debug builds: the CTA's weight slice (every weight copy below) lies inside W8.
+    if (!GBQ_IN_RANGE(p.status, r0 * p.K, (int64_t)nrows * p.K, p.N * p.K)) return;
     const int nchunks = (nrows + p.rows_per_stage - 1) / p.rows_per_stage;
 
     if (tid == 0) {
@@ -295,7 +298,8 @@ __device__ __forceinline__ void gemv_row_dot(const GemvArgs &p, const uint4 (&w)
         for (int m = 1; m < kGvMaxM; ++m)
             if (lane == m) a = acc[m];
         const float tv = __fmul_rn(__int2float_rn(a), xs_s[lane]);
-        p.y[(int64_t)lane * p.N + n] = __float2bfloat16_rn(__fmaf_rn(tv, wsn, bn));
+        if (GBQ_IN_RANGE(p.status, (int64_t)lane * p.N + n, 1, p.M * p.N))
+            p.y[(int64_t)lane * p.N + n] = __float2bfloat16_rn(__fmaf_rn(tv, wsn, bn));
     }
 }
 
@@ -350,6 +354,8 @@ __global__ void __launch_bounds__(kGvThreads, 2) gemv_direct_kernel(GemvArgs p) 
     const int warp = tid >> 5, lane = tid & 31;
     const int64_t r0 = (int64_t)blockIdx.x * p.rows_per_cta;
     const int nrows = (int)(min(p.N, r0 + p.rows_per_cta) - r0);
+    // Debug builds: the CTA's weight slice (every weight copy and load below) lies inside W8.
+    if (!GBQ_IN_RANGE(p.status, r0 * kDxK, (int64_t)nrows * kDxK, p.N * kDxK)) return;
     const int wrows = p.wrow_off ? max(0, nrows - 16) : 0;  // slice rows 16.. staged in shared memory
 
     // L2 prefetch of the slice (nrows * 4096 bytes, 128-byte lines), spread over the threads.
@@ -472,7 +478,8 @@ __global__ void __launch_bounds__(kGvThreads, 2) gemv_direct_kernel(GemvArgs p) 
         const float wsv = __shfl_sync(0xffffffffu, ws_l, q), bv = __shfl_sync(0xffffffffu, b_l, q);
         if ((lane & 7) == 0 && q < RPW && warp + 8 * q < nrows) {
             const float tv = __fmul_rn(__int2float_rn(tot), xs_s[0]);
-            p.y[r0 + warp + 8 * q] = __float2bfloat16_rn(__fmaf_rn(tv, wsv, bv));
+            if (GBQ_IN_RANGE(p.status, r0 + warp + 8 * q, 1, p.N))
+                p.y[r0 + warp + 8 * q] = __float2bfloat16_rn(__fmaf_rn(tv, wsv, bv));
         }
         if (wrows > 0 && !(has2 || has3)) {  // this warp had no staged rows: the copy still lands before exit
             if (!mbar_wait(wfull, 0, p.status, abort_flag)) drain();

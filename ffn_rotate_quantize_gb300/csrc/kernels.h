@@ -31,7 +31,7 @@ cudaError_t launch_rotb(int logn, int in_kind, RotArgs a, cudaStream_t st);     
 cudaError_t launch_quant_identity(int out_kind, IdArgs a, cudaStream_t st);
 // W_hat = bf16((W8 * s) R) for n = 64 (N rows of `groups` 4096-long groups), integer-exact transform.
 cudaError_t launch_dequant_weight64(const int8_t *w8, const float *w_scale, void *out, int64_t N, int groups,
-                                    int num_sms, cudaStream_t st);
+                                    int num_sms, cudaStream_t st, unsigned int *status = nullptr);
 
 // The rotation for every descriptor (rotate_g.cu): any powers of two a = 2^la, b = 2^lb
 // (la = lb = 0: the identity, quantization or conversion only), rows of K values with

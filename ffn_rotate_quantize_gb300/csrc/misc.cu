@@ -9,12 +9,14 @@ namespace {
 // "API": out = acc * x_scale[m] * w_scale[n] + bias[n]); 4 columns per thread when aligned.
 __global__ void dequant_kernel(const int32_t *__restrict__ acc, int64_t ld_acc, const float *__restrict__ xs,
                                const float *__restrict__ ws, const __nv_bfloat16 *__restrict__ bias,
-                               __nv_bfloat16 *__restrict__ y, int64_t ld_y, int64_t M, int64_t N, int vec4) {
+                               __nv_bfloat16 *__restrict__ y, int64_t ld_y, int64_t M, int64_t N, int vec4,
+                               unsigned int *status) {
     const int64_t per_row = vec4 ? N / 4 : N;
     const int64_t total = M * per_row;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t m = i / per_row;
         const int64_t c = i - m * per_row;
+        if (!(GBQ_IN_RANGE(status, m, 1, M) && GBQ_IN_RANGE(status, vec4 ? 4 * c : c, vec4 ? 4 : 1, N))) continue;
         const float x = __ldg(xs + m);
         if (vec4) {
             const int64_t n = 4 * c;
@@ -47,8 +49,10 @@ __global__ void dequant_kernel(const int32_t *__restrict__ acc, int64_t ld_acc, 
 }
 
 // Exact int8 -> fp16 (the tensor-core coding of quantized activations), 16 per thread-step.
-__global__ void s8_to_f16_kernel(const int8_t *__restrict__ q, __half *__restrict__ out, int64_t n16) {
+__global__ void s8_to_f16_kernel(const int8_t *__restrict__ q, __half *__restrict__ out, int64_t n16,
+                                 unsigned int *status) {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x) {
+        if (!GBQ_IN_RANGE(status, 16 * i, 16, 16 * n16)) continue;
         const uint4 v = __ldg(reinterpret_cast<const uint4 *>(q) + i);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         uint32_t o[8];
@@ -65,11 +69,12 @@ __global__ void s8_to_f16_kernel(const int8_t *__restrict__ q, __half *__restric
 
 // w[n, k] = bf16(fp32(w8[n, k]) * s[n]): dequant_weight with an identity rotation.
 __global__ void scale_rows_s8_kernel(const int8_t *__restrict__ w8, const float *__restrict__ s,
-                                     __nv_bfloat16 *__restrict__ w, int64_t N, int64_t K) {
+                                     __nv_bfloat16 *__restrict__ w, int64_t N, int64_t K, unsigned int *status) {
     const int64_t per_row = K / 16;
     const int64_t total = N * per_row;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t n = i / per_row;
+        if (!(GBQ_IN_RANGE(status, n, 1, N) && GBQ_IN_RANGE(status, 16 * i, 16, N * K))) continue;
         const float sc = __ldg(s + n);
         const uint4 v = __ldg(reinterpret_cast<const uint4 *>(w8) + i);
         const int8_t *b = reinterpret_cast<const int8_t *>(&v);
@@ -96,7 +101,7 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 }  // namespace
 
 cudaError_t launch_dequant(const int32_t *acc, int64_t ld_acc, const float *xs, const float *ws, const void *bias,
-                           void *y, int64_t ld_y, int64_t M, int64_t N, cudaStream_t st) {
+                           void *y, int64_t ld_y, int64_t M, int64_t N, cudaStream_t st, unsigned int *status) {
     const int vec4 = (N % 4 == 0 && ld_acc % 4 == 0 && ld_y % 4 == 0 && ((uintptr_t)acc & 15) == 0 &&
                       ((uintptr_t)y & 7) == 0 && ((uintptr_t)ws & 15) == 0 && ((uintptr_t)bias & 7) == 0)
                          ? 1
@@ -105,23 +110,24 @@ cudaError_t launch_dequant(const int32_t *acc, int64_t ld_acc, const float *xs, 
     prof_begin(4, st);
     dequant_kernel<<<grid_for(work, 256), 256, 0, st>>>(acc, ld_acc, xs, ws,
                                                          reinterpret_cast<const __nv_bfloat16 *>(bias),
-                                                         reinterpret_cast<__nv_bfloat16 *>(y), ld_y, M, N, vec4);
+                                                         reinterpret_cast<__nv_bfloat16 *>(y), ld_y, M, N, vec4, status);
     prof_end(st);
     return cudaGetLastError();
 }
 
-cudaError_t launch_s8_to_f16(const int8_t *q, void *out, int64_t n, cudaStream_t st) {
+cudaError_t launch_s8_to_f16(const int8_t *q, void *out, int64_t n, cudaStream_t st, unsigned int *status) {
     if (n % 16) return cudaErrorInvalidValue;
     prof_begin(4, st);
-    s8_to_f16_kernel<<<grid_for(n / 16, 256), 256, 0, st>>>(q, reinterpret_cast<__half *>(out), n / 16);
+    s8_to_f16_kernel<<<grid_for(n / 16, 256), 256, 0, st>>>(q, reinterpret_cast<__half *>(out), n / 16, status);
     prof_end(st);
     return cudaGetLastError();
 }
 
-cudaError_t launch_scale_rows_s8(const int8_t *w8, const float *s, void *w, int64_t N, int64_t K, cudaStream_t st) {
+cudaError_t launch_scale_rows_s8(const int8_t *w8, const float *s, void *w, int64_t N, int64_t K, cudaStream_t st,
+                                 unsigned int *status) {
     if (K % 16) return cudaErrorInvalidValue;
     prof_begin(4, st);
-    scale_rows_s8_kernel<<<grid_for(N * K / 16, 256), 256, 0, st>>>(w8, s, reinterpret_cast<__nv_bfloat16 *>(w), N, K);
+    scale_rows_s8_kernel<<<grid_for(N * K / 16, 256), 256, 0, st>>>(w8, s, reinterpret_cast<__nv_bfloat16 *>(w), N, K, status);
     prof_end(st);
     return cudaGetLastError();
 }

@@ -38,7 +38,7 @@ __global__ void __launch_bounds__(kIdThreads) quant_identity_kernel(IdArgs p) {
 #pragma unroll
     for (int c = 0; c < kIdMaxChunks; ++c) {
         const int ch = tid + c * kIdThreads;
-        if (ch < nchunks) {
+        if (ch < nchunks && GBQ_IN_RANGE(p.status, row * p.ld_in + 8 * ch, 8, p.M * p.ld_in)) {
             const uint4 w = __ldg(src + ch);
             const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -130,6 +130,7 @@ __global__ void __launch_bounds__(kIdThreads) quant_identity_kernel(IdArgs p) {
     for (int c = 0; c < kIdMaxChunks; ++c) {
         const int ch = tid + c * kIdThreads;
         if (ch >= nchunks) continue;
+        if (!GBQ_IN_RANGE(p.status, row * p.K + 8 * ch, 8, p.M * p.K)) continue;
         if constexpr (OUT == OUT_S8) {
             reinterpret_cast<uint2 *>(reinterpret_cast<int8_t *>(p.out) + row * p.K)[ch] =
                 make_uint2(words[c][0], words[c][1]);
@@ -192,6 +193,10 @@ __global__ void __launch_bounds__(kIdsThreads, 2) quant_identity_stream_kernel(I
         abort_flag = 0;
         fence_mbar_init();
         for (; issued < n_local && issued < stages; ++issued) {
+            if (!GBQ_IN_RANGE(p.status, row_of(issued) * p.ld_in, row_bytes / 2, p.M * p.ld_in)) {
+                mbar_arrive_expect_tx(&full[issued], 0);  // debug builds: skipped, the stage completes empty
+                continue;
+            }
             mbar_arrive_expect_tx(&full[issued], row_bytes);
             bulk_g2s(ids_smem + (size_t)issued * row_bytes, in + row_of(issued) * p.ld_in, row_bytes, &full[issued]);
         }
@@ -296,7 +301,8 @@ __global__ void __launch_bounds__(kIdsThreads, 2) quant_identity_stream_kernel(I
                             w1 |= pair << (16 * (h - 2));
                     }
                 }
-                if constexpr (OUT == OUT_S8) {
+                if (!GBQ_IN_RANGE(p.status, row * p.K + 8 * ch, 8, p.M * p.K)) {
+                } else if constexpr (OUT == OUT_S8) {
                     reinterpret_cast<uint2 *>(reinterpret_cast<int8_t *>(p.out) + row * p.K)[ch] = make_uint2(w0, w1);
                 } else {
                     reinterpret_cast<uint4 *>(reinterpret_cast<__half *>(p.out) + row * p.K)[ch] =
@@ -313,8 +319,12 @@ __global__ void __launch_bounds__(kIdsThreads, 2) quant_identity_stream_kernel(I
         }
         __syncthreads();  // the stage is read, the block partials are complete
         if (tid == 0 && issued < n_local) {  // row i + stages into the stage just read
-            mbar_arrive_expect_tx(&full[stage], row_bytes);
-            bulk_g2s(ids_smem + (size_t)stage * row_bytes, in + row_of(issued) * p.ld_in, row_bytes, &full[stage]);
+            if (GBQ_IN_RANGE(p.status, row_of(issued) * p.ld_in, row_bytes / 2, p.M * p.ld_in)) {
+                mbar_arrive_expect_tx(&full[stage], row_bytes);
+                bulk_g2s(ids_smem + (size_t)stage * row_bytes, in + row_of(issued) * p.ld_in, row_bytes, &full[stage]);
+            } else {
+                mbar_arrive_expect_tx(&full[stage], 0);  // debug builds: skipped, the stage completes empty
+            }
             ++issued;
         }
         if (p.out_l1 && tid < nb) {

@@ -113,8 +113,12 @@ template <int IN>
 __device__ __forceinline__ void fast_issue(const RotArgs &p, int64_t row, uint8_t *dst, uint64_t *bar) {
     constexpr int NIN = in_count(IN);
     const uint32_t rb = p.row_in_bytes;
-    mbar_arrive_expect_tx(bar, NIN * rb);
     const int64_t off = row * p.ld_in * in_elem_bytes(IN);
+    if (!GBQ_IN_RANGE(p.status, off, rb, p.M * p.ld_in * in_elem_bytes(IN))) {
+        mbar_arrive_expect_tx(bar, 0);  // debug builds: the copy is skipped, the stage completes empty
+        return;
+    }
+    mbar_arrive_expect_tx(bar, NIN * rb);
     bulk_g2s(dst, reinterpret_cast<const uint8_t *>(p.in0) + off, rb, bar);
     if (NIN == 2) bulk_g2s(dst + rb, reinterpret_cast<const uint8_t *>(p.in1) + off, rb, bar);
 }
@@ -224,6 +228,7 @@ __global__ void __launch_bounds__(128) rot64_kernel(const __grid_constant__ Fast
             v);
         const int r = tau >> 2, jq = tau & 3;
         const int64_t o0 = row * 4096 + (2 * r) * 64 + 16 * jq;  // element offset of row 2r's chunk
+        const bool out_ok = GBQ_IN_RANGE(p.status, o0, 64 + 16, p.M * p.K);
         if constexpr (OUT == OUT_BF16) {
             float x0[16], x1[16];
 #pragma unroll
@@ -231,16 +236,20 @@ __global__ void __launch_bounds__(128) rot64_kernel(const __grid_constant__ Fast
                 x0[c] = v[c].x;
                 x1[c] = v[c].y;
             }
-            store_chunk_bf16(p.out, o0, x0);
-            store_chunk_bf16(p.out, o0 + 64, x1);
+            if (out_ok) {
+                store_chunk_bf16(p.out, o0, x0);
+                store_chunk_bf16(p.out, o0 + 64, x1);
+            }
         } else {
             const float amax = block_amax(pairs_amax(v), wmax, 4);
             const float s = __fdiv_rn(amax, 127.0f);
             if (tau == 0) p.out_scale[row] = s;
             uint32_t words[2][4];
             quant_codes<16>(v, s, words);
-            store_chunk_codes<OUT>(p.out, o0, words[0]);
-            store_chunk_codes<OUT>(p.out, o0 + 64, words[1]);
+            if (out_ok) {
+                store_chunk_codes<OUT>(p.out, o0, words[0]);
+                store_chunk_codes<OUT>(p.out, o0 + 64, words[1]);
+            }
             if (p.out_l1) warp_sums_store(codes_l1(words), p.out_l1 + row * 4);  // K = 4096: 4 blocks
         }
     }
@@ -343,6 +352,7 @@ __global__ void __launch_bounds__(512, 2) rot128_kernel(const __grid_constant__ 
             for (int c = 0; c < 16; ++c) v[c] = __fmul2_rn(v[c], half2);  // the two H2 levels: (1/sqrt2)^2
         }
         const int64_t o0 = row * 16384 + i * 128 + 16 * jq;  // element offset of the j6 = 0 chunk
+        const bool out_ok = GBQ_IN_RANGE(p.status, o0, 64 + 16, p.M * p.K);
         if constexpr (OUT == OUT_BF16) {
             float x0[16], x1[16];
 #pragma unroll
@@ -352,8 +362,10 @@ __global__ void __launch_bounds__(512, 2) rot128_kernel(const __grid_constant__ 
             }
             __syncthreads();  // pass-C reads done before the next row's copy lands in the tile
             if (tau == 0 && row + gridDim.x < p.M) fast_issue<IN>(p, row + gridDim.x, smem, &full[0]);
-            store_chunk_bf16(p.out, o0, x0);
-            store_chunk_bf16(p.out, o0 + 64, x1);
+            if (out_ok) {
+                store_chunk_bf16(p.out, o0, x0);
+                store_chunk_bf16(p.out, o0 + 64, x1);
+            }
         } else {
             const float amax = block_amax(pairs_amax(v), wmax, 16);  // its barrier also ends the pass-C reads
             if (tau == 0 && row + gridDim.x < p.M) fast_issue<IN>(p, row + gridDim.x, smem, &full[0]);
@@ -361,8 +373,10 @@ __global__ void __launch_bounds__(512, 2) rot128_kernel(const __grid_constant__ 
             if (tau == 0) p.out_scale[row] = s;
             uint32_t words[2][4];
             quant_codes<16>(v, s, words);
-            store_chunk_codes<OUT>(p.out, o0, words[0]);
-            store_chunk_codes<OUT>(p.out, o0 + 64, words[1]);
+            if (out_ok) {
+                store_chunk_codes<OUT>(p.out, o0, words[0]);
+                store_chunk_codes<OUT>(p.out, o0 + 64, words[1]);
+            }
             if (p.out_l1) warp_sums_store(codes_l1(words), p.out_l1 + row * 16);  // K = 16384: 16 blocks
         }
     }

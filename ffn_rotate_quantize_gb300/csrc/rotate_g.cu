@@ -59,6 +59,7 @@ struct GenArgs {
     float post;                  // factor after the last level: 1, 1/2 or fl(sqrt(1/2))
     uint32_t rowmax_off;         // byte offsets in dynamic shared memory
     uint32_t rowscale_off;
+    unsigned int *status;        // device status word (debug builds: bounds checks)
 };
 
 __device__ __forceinline__ int tix(int e) { return e + (e >> 5); }  // padded tile index
@@ -265,7 +266,12 @@ __global__ void __launch_bounds__(kGenThreads) rotg_kernel(const __grid_constant
                 const int u = u0 + j * kGenThreads;
                 if (u < E8) {
                     const int e = u * 8, row = e / K;
-                    gen_load8<IN>(p, r0 + row, e - row * K, x[j]);
+                    if (GBQ_IN_RANGE(p.status, r0 + row, 1, p.M) && GBQ_IN_RANGE(p.status, e - row * K, 8, K)) {
+                        gen_load8<IN>(p, r0 + row, e - row * K, x[j]);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) x[j][k] = 0.0f;
+                    }
                 }
             }
 #pragma unroll
@@ -306,7 +312,7 @@ __global__ void __launch_bounds__(kGenThreads) rotg_kernel(const __grid_constant
             for (int i = tid; i < nr; i += kGenThreads) {
                 const float s = __fdiv_rn(__uint_as_float(rowmax[i]), 127.0f);
                 rowscale[i] = s;
-                p.out_scale[r0 + i] = s;
+                if (GBQ_IN_RANGE(p.status, r0 + i, 1, p.M)) p.out_scale[r0 + i] = s;
             }
             __syncthreads();
         }
@@ -319,6 +325,7 @@ __global__ void __launch_bounds__(kGenThreads) rotg_kernel(const __grid_constant
 #pragma unroll
             for (int k = 0; k < 8; ++k) v[k] = make_float2(t[k], t[k + 8]);
             const int64_t off = (r0 + row) * (int64_t)K + (e - row * K);
+            if (!(GBQ_IN_RANGE(p.status, r0 + row, 1, p.M) && GBQ_IN_RANGE(p.status, e - row * K, 16, K))) continue;
             if constexpr (OUT == OUT_BF16) {
                 uint32_t w[8];
 #pragma unroll
@@ -424,6 +431,7 @@ cudaError_t launch_rotg(int in_kind, int out_kind, const RotArgs &a, int la, int
     g.ld_in = a.ld_in;
     g.out = a.out;
     g.out_scale = a.out_scale;
+    g.status = a.status;
     g.M = a.M;
     g.K = (int)a.K;
     int R = kGenTargetElems / g.K;

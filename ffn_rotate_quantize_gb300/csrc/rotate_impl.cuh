@@ -551,6 +551,12 @@ __global__ void __launch_bounds__(RotqMaxThreads<LOGN>::value) rotq_kernel(const
         const int64_t r0 = u * rpt;
         const int nr = (int)min((int64_t)rpt, p.M - r0);
         uint8_t *dst = stage0 + (size_t)st * p.stage_bytes;
+        const int64_t eb = in_elem_bytes(IN);
+        if (!GBQ_IN_RANGE(p.status, r0 * p.ld_in * eb, (int64_t)(nr - 1) * p.ld_in * eb + in_row_bytes,
+                          p.M * p.ld_in * eb)) {
+            mbar_arrive_expect_tx(&full[st], 0);  // debug builds: the copies are skipped, the stage completes empty
+            return;
+        }
         mbar_arrive_expect_tx(&full[st], (uint32_t)nr * NIN * in_row_bytes);
         for (int r = 0; r < nr; ++r) {
             const int64_t off = (r0 + r) * p.ld_in * in_elem_bytes(IN);
@@ -673,6 +679,7 @@ __global__ void __launch_bounds__(RotqMaxThreads<LOGN>::value) rotq_kernel(const
             const int nr = (int)min((int64_t)rpt, p.M - r0);
             const uint32_t ob = (uint32_t)(p.K * OESZ);
             for (int r = 0; r < nr; ++r)
+                if (GBQ_IN_RANGE(p.status, (r0 + r) * (int64_t)ob, ob, p.M * (int64_t)ob))
                 bulk_s2g(reinterpret_cast<uint8_t *>(p.out) + (r0 + r) * (int64_t)ob,
                          reinterpret_cast<const uint8_t *>(tiles) + (size_t)r * p.G * Geo::TILE * sizeof(float2), ob);
             tma_store_commit();

@@ -67,6 +67,8 @@ typedef struct gbq_rot {
 
 /* Device-status bits reported by gbq_device_status(). */
 #define GBQ_DEV_WAIT_TIMEOUT 0x1u /* an mbarrier wait hit its iteration limit */
+#define GBQ_DEV_BOUNDS 0x2u       /* debug build only (GBQ_DEBUG_BOUNDS): a kernel computed a global   */
+                                  /* memory access outside its tensor; the access was skipped       */
 
 /* ---- library / device ------------------------------------------------ */
 
