@@ -339,14 +339,103 @@ __device__ __forceinline__ void gemv_load_row(uint4 (&w)[kDxChunks], const int8_
     for (int k = 0; k < kDxChunks; ++k) w[k] = __ldcs(src + lane + 32 * k);
 }
 
+// One H4/2 level on register digit D (register bits 2D, 2D + 1) of 16 values: the operations of
+// h4_level, so the values equal the square kernels' bit for bit.
+template <int D>
+__device__ __forceinline__ void h4_regs16(float (&v)[16]) {
+#pragma unroll
+    for (int base = 0; base < 16; ++base) {
+        if ((base >> (2 * D)) & 3) continue;
+        const int b1 = base | (1 << (2 * D)), b2 = base | (2 << (2 * D)), b3 = base | (3 << (2 * D));
+        const float x0 = v[base], x1 = v[b1], x2 = v[b2], x3 = v[b3];
+        const float h = __fmul_rn(__fadd_rn(__fadd_rn(x0, x1), __fadd_rn(x2, x3)), 0.5f);
+        v[base] = __fmaf_rn(x3, -1.0f, h);
+        v[b1] = __fmaf_rn(x2, -1.0f, h);
+        v[b2] = __fmaf_rn(x1, -1.0f, h);
+        v[b3] = __fmaf_rn(x0, -1.0f, h);
+    }
+}
+
+constexpr int kDxPitch = 80;                         // floats per row of the 64-row exchange tile
+constexpr uint32_t kDxTileBytes = 64 * kDxPitch * 4;  // 20 KB
+
+// Rotate + quantize one 4096-long token row (bf16, staged at xb) with all 256 threads of the CTA:
+// X[i][j] (element 64 i + j) becomes V = H64 X H64 / 64 in the level order of the n = 64 kernels
+// (i01, i23, i45, j45, j01, j23) with their operations, so the codes are gbq_quantize_act's bit for
+// bit.  Each thread holds 16 values in three layouts (register bits / lane bits / warp bits):
+//   1: (i0..i3) / (j0..j4) / (j5, i4, i5)   levels i01, i23     from the staged x
+//   2: (i4, i5, j4, j5) / (j0..j3, i0) / (i1, i2, i3)   levels i45, j45   via the tile T
+//   3: (j0..j3) / (i4, i5, j4, j5, i0) / (i1, i2, i3)   levels j01, j23   via warp shuffles
+// Layout 3 leaves 16 consecutive values per thread: one 16-byte store of codes.  T is 64 rows of
+// kDxPitch floats (both tile patterns are free of bank conflicts).  Two CTA barriers.
+__device__ __forceinline__ void gemv_rot64_all(const uint8_t *xb, float *T, float *wmax, int8_t *xq_row,
+                                               float *xs_out, int tid) {
+    const int w = tid >> 5, l = tid & 31;
+    float v[16];
+    {
+        const uint16_t *x16 = reinterpret_cast<const uint16_t *>(xb);
+        const int j = l + 32 * (w & 1), i0 = 16 * (w >> 1);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) v[r] = bf16_to_float(x16[64 * (i0 + r) + j]);
+        h4_regs16<0>(v);
+        h4_regs16<1>(v);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) T[(i0 + r) * kDxPitch + j] = v[r];
+    }
+    __syncthreads();
+    {
+        const int jl = l & 15, ib = (l >> 4) + 2 * w;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) v[r] = T[(ib + 16 * (r & 3)) * kDxPitch + jl + 16 * (r >> 2)];
+        h4_regs16<0>(v);
+        h4_regs16<1>(v);
+    }
+    // register bit k <-> lane bit k, k = 0..3
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const bool up = (l >> k) & 1;
+#pragma unroll
+        for (int r0 = 0; r0 < 16; ++r0) {
+            if ((r0 >> k) & 1) continue;
+            const int r1 = r0 | (1 << k);
+            const float got = __shfl_xor_sync(0xffffffffu, up ? v[r0] : v[r1], 1 << k);
+            if (up)
+                v[r0] = got;
+            else
+                v[r1] = got;
+        }
+    }
+    h4_regs16<0>(v);
+    h4_regs16<1>(v);
+    float m = 0.0f;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) m = fmaxf(m, fabsf(v[r]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (l == 0) wmax[w] = m;
+    __syncthreads();  // also: every layout-2 read of T is done
+    float amax = wmax[0];
+#pragma unroll
+    for (int k = 1; k < kGvThreads / 32; ++k) amax = fmaxf(amax, wmax[k]);
+    const float s = __fdiv_rn(amax, 127.0f);
+    if (tid == 0) *xs_out = s;
+    float2 pv[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) pv[k] = make_float2(v[k], v[k + 8]);
+    uint32_t words[2][2];
+    quant_codes<8>(pv, s, words);
+    const int e0 = 16 * ((l >> 2) & 3) + 64 * ((l >> 4) + 2 * w + 16 * (l & 3));
+    *reinterpret_cast<uint4 *>(xq_row + e0) = make_uint4(words[0][0], words[0][1], words[1][0], words[1][1]);
+}
+
 template <int RPW>
 __global__ void __launch_bounds__(kGvThreads, 2) gemv_direct_kernel(GemvArgs p) {
     extern __shared__ __align__(128) uint8_t smem[];
     int8_t *xq = reinterpret_cast<int8_t *>(smem + p.x_off);
     float2 *T = reinterpret_cast<float2 *>(smem + p.t_off);
     float *xs_s = reinterpret_cast<float *>(smem + p.misc_off);
-    float *wmax = xs_s + kGvMaxM;
-    uint64_t *xfull = reinterpret_cast<uint64_t *>(wmax + kGvMaxM);
+    float *wmax = xs_s + kGvMaxM;                                             // one slot per warp
+    uint64_t *xfull = reinterpret_cast<uint64_t *>(wmax + kGvThreads / 32);  // byte 48 of misc
     int *abort_flag = reinterpret_cast<int *>(xfull + 1);
     uint64_t *wfull = xfull + 2;
 
@@ -395,30 +484,11 @@ __global__ void __launch_bounds__(kGvThreads, 2) gemv_direct_kernel(GemvArgs p) 
     if (has0) gemv_load_row(wa, p.w8, r0 + warp, lane);
     if (has1) gemv_load_row(wb, p.w8, r0 + warp + 8, lane);
 
-    // ---- rotate + quantize x: the three-pass n = 64 row transform on threads 0..127 ----
-    if (tid < 128) {
-        auto bar = [] { named_bar_sync(1, 128); };
-        RotArgs ra{};
-        const bool ok = named_bar_and(1, 128, xok);
-        for (int m = 0; m < p.M && ok; ++m) {
-            const uint8_t *xb = smem + p.xb_off + (size_t)m * kDxK * 2;
-            float2 v[16];
-            rot64_row<IN_BF16>(ra, xb, xb, 0.0f, T, tid, bar, [] {}, v);
-            float mx = pairs_amax(v);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            if (lane == 0) wmax[warp] = mx;
-            bar();
-            const float amax = fmaxf(fmaxf(wmax[0], wmax[1]), fmaxf(wmax[2], wmax[3]));
-            const float s = __fdiv_rn(amax, 127.0f);
-            if (tid == 0) xs_s[m] = s;
-            uint32_t words[2][4];
-            quant_codes<16>(v, s, words);
-            const int r = tid >> 2, jq = tid & 3;
-            store_codes<OUT_S8, 4>(xq, (int64_t)m * kDxK + 128 * r + 16 * jq, words[0]);
-            store_codes<OUT_S8, 4>(xq, (int64_t)m * kDxK + 128 * r + 64 + 16 * jq, words[1]);
-            bar();  // the tile and the amax slots are free for the next token
-        }
+    // ---- rotate + quantize x: every thread, one token at a time ----
+    if (__syncthreads_and(xok)) {
+        float *Tf = reinterpret_cast<float *>(T);
+        for (int m = 0; m < p.M; ++m)
+            gemv_rot64_all(smem + p.xb_off + (size_t)m * kDxK * 2, Tf, wmax, xq + (int64_t)m * kDxK, xs_s + m, tid);
     }
     __syncthreads();
     // Copies in flight when a wait gave up land (bounded) before the CTA leaves: x (if its wait gave
@@ -521,7 +591,7 @@ int launch_gemv_direct(const GemvArgs &base, int num_sms, cudaStream_t st) {
     const int64_t grid = (a.N + rpc - 1) / rpc;
     a.x_off = 0;
     a.t_off = (uint32_t)(((size_t)a.M * kDxK + 127) & ~(size_t)127);
-    a.misc_off = a.t_off + ((fast_tile_bytes(6) + 127) & ~127u);
+    a.misc_off = a.t_off + ((kDxTileBytes + 127) & ~127u);
     a.xb_off = a.misc_off + 128;
     size_t smem = a.xb_off + (size_t)a.M * kDxK * 2;
     // Stage the slice's rows 16.. in shared memory when two CTAs still fit per SM.
