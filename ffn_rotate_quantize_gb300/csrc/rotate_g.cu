@@ -218,7 +218,17 @@ __device__ __forceinline__ void gen_pass(float *T, int E, int p1, int p2, const 
                 float m = 0.0f;
 #pragma unroll
                 for (int r = 0; r < NV; ++r) m = fmaxf(m, fabsf(v[r]));
-                atomicMax(&rowmax[base / p.K], __float_as_uint(m));
+                // One atomic per warp when the warp's items lie in one row (wide rows), else one per item.
+                const int row = base / p.K;
+                const unsigned act = __activemask();
+                const int row0 = __shfl_sync(act, row, __ffs(act) - 1);
+                if (act == 0xffffffffu && __all_sync(act, row == row0)) {
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                    if ((threadIdx.x & 31) == 0) atomicMax(&rowmax[row], __float_as_uint(m));
+                } else {
+                    atomicMax(&rowmax[row], __float_as_uint(m));
+                }
             }
         }
 #pragma unroll
@@ -240,7 +250,7 @@ __device__ __forceinline__ void gen_pass_dispatch(int w1, int w2, float *T, int 
 }
 
 template <int IN, int OUT>
-__global__ void __launch_bounds__(kGenThreads) rotg_kernel(const __grid_constant__ GenArgs p) {
+__global__ void __launch_bounds__(kGenThreads, 3) rotg_kernel(const __grid_constant__ GenArgs p) {
     extern __shared__ __align__(128) uint8_t smem[];
     float *T = reinterpret_cast<float *>(smem);
     unsigned int *rowmax = reinterpret_cast<unsigned int *>(smem + p.rowmax_off);
@@ -257,12 +267,12 @@ __global__ void __launch_bounds__(kGenThreads) rotg_kernel(const __grid_constant
         if constexpr (OUT != OUT_BF16)
             for (int i = tid; i < nr; i += kGenThreads) rowmax[i] = 0u;
 
-        // ---- phase 0: global -> fp32 tile, four 8-value loads per thread in flight
+        // ---- phase 0: global -> fp32 tile, two 8-value loads per thread in flight
         const int E8 = E >> 3;
-        for (int u0 = tid; u0 < E8; u0 += 4 * kGenThreads) {
-            float x[4][8];
+        for (int u0 = tid; u0 < E8; u0 += 2 * kGenThreads) {
+            float x[2][8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 2; ++j) {
                 const int u = u0 + j * kGenThreads;
                 if (u < E8) {
                     const int e = u * 8, row = e / K;
@@ -275,7 +285,7 @@ __global__ void __launch_bounds__(kGenThreads) rotg_kernel(const __grid_constant
                 }
             }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 2; ++j) {
                 const int u = u0 + j * kGenThreads;
                 if (u < E8) {
                     float *t = T + tix(u * 8);  // eight values inside one 32-value block
@@ -305,7 +315,16 @@ __global__ void __launch_bounds__(kGenThreads) rotg_kernel(const __grid_constant
                     float m = 0.0f;
 #pragma unroll
                     for (int k = 0; k < 16; ++k) m = fmaxf(m, fabsf(t[k]));
-                    atomicMax(&rowmax[(u * 16) / K], __float_as_uint(m));
+                    const int row = (u * 16) / K;
+                    const unsigned act = __activemask();
+                    const int row0 = __shfl_sync(act, row, __ffs(act) - 1);
+                    if (act == 0xffffffffu && __all_sync(act, row == row0)) {
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                        if ((threadIdx.x & 31) == 0) atomicMax(&rowmax[row], __float_as_uint(m));
+                    } else {
+                        atomicMax(&rowmax[row], __float_as_uint(m));
+                    }
                 }
                 __syncthreads();
             }
