@@ -89,13 +89,13 @@ struct RotqMaxThreads {
 __device__ __forceinline__ float bf16_to_float(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
 
 // SiLU(g) * u in fp32: g / (1 + exp(-g)) * u with CUDA's accurate expf (a few ulp at most from the
-// correctly rounded exponential) and IEEE division, the operations of the plain definition, so a
-// code can move only where the value sits at a rounding boundary.  For g < -88 the exponential
-// overflows to inf and the quotient is -0 (as g e^g).
+// correctly rounded exponential; not the special-function unit's __expf) and the division through the
+// reciprocal (__fdividef, within 2 ulp of the IEEE quotient), so a code can move only where the value sits
+// at a rounding boundary.  For g < -88 the exponential overflows to inf and the quotient is -0 (as g e^g).
 __device__ __forceinline__ float silu_mul(float g, float u) {
     const float e = expf(-g);
     const float d = __fadd_rn(1.0f, e);
-    return __fmul_rn(__fdiv_rn(g, d), u);
+    return __fmul_rn(__fdividef(g, d), u);
 }
 
 // Dequant epilogue value rounded to bf16 and widened back (the gate/up outputs).
