@@ -51,7 +51,8 @@ DECODE_BYTES = 4096 * 4096 + 4096 * 4 + 4096 * 2 + 4096 * 2  # W8 + s + x + y
 DEQW_BYTES = 16384 * 4096 * 3 + 16384 * 4  # int8 read + bf16 write + scales
 WORKLOAD = ("prefill INT8 linear x[1024,4096] @ W8[14336,4096]^T + bias, R=H64(x)H64/64; "
             "step also runs decode GEMV [1x4096x4096], SwiGLU FFN [1024,4096,16384], "
-            "backward dx [4096,16384,4096], rotated-bf16 comparator [1024,4096,14336]")
+            "backward dx [4096,16384,4096], rotated-bf16 comparator [1024,4096,14336], activation "
+            "rotate+quantize [4096,16384] as H128(x)H128 and H64(x)H256")
 
 
 def load_peaks():
