@@ -243,6 +243,61 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(GemvArgs p) {
 }
 
 // ---------------------------------------------------------------------------
+// Decode GEMV over tokens already rotated and quantized (the codes and row scales the rotation kernels
+// wrote into the workspace): for every descriptor the in-kernel rotations above do not cover.  Launched
+// with programmatic stream serialization right after the quantizer: the first weight stages are
+// bulk-copied at entry, while the quantizer may still run (it writes only the codes and scales); the
+// codes and scales are read after griddepcontrol.wait; then the dot phase of gemv_kernel.
+__global__ void __launch_bounds__(kGvThreads, 1) gemv_codes_kernel(GemvArgs p, const int8_t *codes,
+                                                                   const float *scales) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t *stages = smem;
+    int8_t *xq = reinterpret_cast<int8_t *>(smem + p.x_off);
+    float *xs_s = reinterpret_cast<float *>(smem + p.misc_off);
+    uint64_t *full = reinterpret_cast<uint64_t *>(xs_s + 2 * kGvMaxM);
+    int *abort_flag = reinterpret_cast<int *>(full + kGvStages);
+    uint64_t *xfull = full + kGvStages + 1;
+
+    const int tid = threadIdx.x;
+    const int64_t r0 = (int64_t)blockIdx.x * p.rows_per_cta;
+    const int nrows = (int)(min(p.N, r0 + p.rows_per_cta) - r0);
+    // Debug builds: the CTA's weight slice (every weight copy below) lies inside W8.
+    if (!GBQ_IN_RANGE(p.status, r0 * p.K, (int64_t)nrows * p.K, p.N * p.K)) return;
+    const int nchunks = (nrows + p.rows_per_stage - 1) / p.rows_per_stage;
+    if (tid == 0) {
+        for (int s2 = 0; s2 < kGvStages; ++s2) mbar_init(&full[s2], 1);
+        mbar_init(xfull, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        for (int c = 0; c < nchunks && c < kGvStages; ++c) {
+            const int rows = min(p.rows_per_stage, nrows - c * p.rows_per_stage);
+            const uint32_t bytes = (uint32_t)rows * (uint32_t)p.K;
+            mbar_arrive_expect_tx(&full[c], bytes);
+            bulk_g2s(stages + (size_t)c * p.stage_bytes, p.w8 + (r0 + (int64_t)c * p.rows_per_stage) * p.K, bytes,
+                     &full[c]);
+        }
+    }
+    pdl_wait();  // the codes and scales come from the kernel before
+    if (tid == 0) {
+        mbar_arrive_expect_tx(xfull, (uint32_t)(p.M * p.K));
+        bulk_g2s(xq, codes, (uint32_t)(p.M * p.K), xfull);
+    }
+    if (tid < p.M) xs_s[tid] = scales[tid];
+    __syncthreads();  // barriers initialised, scales in place
+    const bool xok = mbar_wait(xfull, 0, p.status, abort_flag);
+    if (__syncthreads_and(xok)) gemv_dot_phase(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks);
+    if (tid == 0 && *(volatile int *)abort_flag) {
+        // A wait gave up: let the copies issued at entry land (bounded) before the CTA leaves.
+        for (int c = 0; c <= min(nchunks, kGvStages); ++c) {
+            uint64_t *b = c < min(nchunks, kGvStages) ? &full[c] : xfull;
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(b, 0) && globaltimer() - t0 < kWaitLimitNs) {
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Register-streaming variant for K = 4096, n = 64, one group, and at most 32
 // weight rows per CTA (4 per warp), launched with programmatic stream
 // serialization so that consecutive decode calls overlap:
@@ -675,6 +730,66 @@ int launch_gemv_t(const GemvArgs &base, int num_sms, cudaStream_t st) {
 }
 
 }  // namespace
+
+bool gemv_codes_fits(int64_t M, int64_t K) {
+    if (M < 1 || M > kGvMaxM || K < 16 || K % 16 != 0) return false;
+    const size_t fixed = (((size_t)M * K + 127) & ~(size_t)127) + 128;
+    return fixed < kGvSmem && (kGvSmem - fixed) / kGvStages >= (size_t)K + 127;  // one row per stage at least
+}
+
+int launch_gemv_codes(const int8_t *codes, const float *scales, const int8_t *w8, const float *w_scale,
+                      const void *bias, void *y, int64_t M, int64_t N, int64_t K, int num_sms, cudaStream_t st,
+                      unsigned int *status) {
+    if (!gemv_codes_fits(M, K) || N < 1) return GBQ_ENOTSUP;
+    if (((uintptr_t)codes | (uintptr_t)w8) & 15) return GBQ_ENOTSUP;
+    GemvArgs a{};
+    a.w8 = w8;
+    a.ws = w_scale;
+    a.bias = reinterpret_cast<const __nv_bfloat16 *>(bias);
+    a.y = reinterpret_cast<__nv_bfloat16 *>(y);
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.G = 1;
+    a.status = status;
+    const size_t x_bytes = (size_t)M * K;
+    const size_t misc = 2 * kGvMaxM * 4 + (kGvStages + 2) * 8 + 16;  // scales, barriers, abort, codes barrier
+    const size_t fixed = ((x_bytes + 127) & ~(size_t)127) + 128;
+    const int64_t rpc = (N + num_sms - 1) / num_sms;
+    const int64_t grid = (N + rpc - 1) / rpc;
+    // A stage is rows_per_stage weight rows rounded up to 128 bytes (K is a multiple of 16 only).
+    const int64_t rps_cap = (int64_t)((kGvSmem - fixed) / kGvStages - 127) / K;
+    const int64_t rps_fit = (rpc + kGvStages - 1) / kGvStages;
+    const int64_t rps = rps_fit <= rps_cap ? rps_fit : rps_cap;
+    a.rows_per_cta = (int)rpc;
+    a.rows_per_stage = (int)rps;
+    a.stage_bytes = (uint32_t)(((size_t)rps * K + 127) & ~(size_t)127);
+    a.x_off = (uint32_t)((size_t)kGvStages * a.stage_bytes);
+    a.misc_off = a.x_off + (uint32_t)((x_bytes + 127) & ~(size_t)127);
+    const size_t smem = a.misc_off + misc;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(gemv_codes_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGvSmem) !=
+            cudaSuccess)
+            return gbq_fail(GBQ_ECUDA, "gemv: cannot set shared memory size");
+        attr = true;
+    }
+    cudaLaunchAttribute lattr[1];
+    lattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    lattr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = st;
+    cfg.attrs = lattr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kGvThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    prof_begin(3, st);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_codes_kernel, a, codes, scales);
+    prof_end(st);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return e == cudaSuccess ? GBQ_OK : gbq_fail(GBQ_ECUDA, cudaGetErrorString(e));
+}
 
 int launch_gemv(const void *x, const int8_t *w8, const float *w_scale, const void *bias, void *y, int64_t M, int64_t N,
                 int64_t K, int logn, int groups, int num_sms, cudaStream_t st, unsigned int *status) {
