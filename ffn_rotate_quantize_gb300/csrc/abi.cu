@@ -618,16 +618,14 @@ int gbq_linear(const void *x, const int8_t *w8, const float *w_scale, const void
     if (rc) return rc;
     INIT(d);
     cudaStream_t st = (cudaStream_t)stream;
-    if (M <= 4) {
-        // Decode: the GEMV with the rotation inside for the square shapes it covers; for every other
-        // descriptor the rotation kernels quantize x into the workspace and a GEMV streams the weight
-        // over those codes (the same codes, scales and epilogue as the GEMM route below).
-        if (rs.logn > 0) {
-            rc = launch_gemv(x, w8, w_scale, bias, y, M, N, K, rs.logn, rs.groups, d->sms, st, d->status);
-            if (rc != GBQ_ENOTSUP) return rc;
-        }
+    // Decode and small batches: for M <= 4 the GEMV with the rotation inside for the square shapes it
+    // covers; otherwise, up to 16 tokens, the rotation kernels quantize x into the workspace and a GEMV
+    // streams the weight over those codes (the same codes, scales and epilogue as the GEMM route below).
+    if (M <= 4 && rs.logn > 0) {
+        rc = launch_gemv(x, w8, w_scale, bias, y, M, N, K, rs.logn, rs.groups, d->sms, st, d->status);
+        if (rc != GBQ_ENOTSUP) return rc;
     }
-    if (M <= 4 && gemv_codes_fits(M, K)) {
+    if (gemv_codes_fits(M, N, K, d->sms)) {
         Ws wc{(uint8_t *)workspace, ws_bytes};
         int8_t *codes = (int8_t *)wc.take((size_t)M * K);
         float *xs_c = (float *)wc.take((size_t)M * 4);
@@ -638,7 +636,7 @@ int gbq_linear(const void *x, const int8_t *w8, const float *w_scale, const void
         a.out_scale = xs_c;
         a.M = M;
         a.K = K;
-        rc = run_rotq("gbq_linear (decode codes)", rs, IN_BF16, OUT_S8, a, st);
+        rc = run_rotq("gbq_linear (GEMV codes)", rs, IN_BF16, OUT_S8, a, st);
         if (rc) return rc;
         return launch_gemv_codes(codes, xs_c, w8, w_scale, bias, y, M, N, K, d->sms, st, d->status);
     }

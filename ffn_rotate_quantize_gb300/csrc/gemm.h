@@ -67,9 +67,9 @@ int launch_bf16_gemm_tn(const void *x, const void *w, const void *bias, void *y,
 int launch_gemv(const void *x, const int8_t *w8, const float *w_scale, const void *bias, void *y, int64_t M,
                 int64_t N, int64_t K, int logn, int groups, int num_sms, cudaStream_t st, unsigned int *status);
 
-// Decode GEMV (M <= 4) over tokens already quantized: codes int8 [M][K] and row scales fp32 [M] (e.g. in the
+// GEMV (M <= 16) over tokens already quantized: codes int8 [M][K] and row scales fp32 [M] (e.g. in the
 // workspace), y[m][n] = dequant(sum_k codes[m][k] w8[n][k]).  GBQ_ENOTSUP (nothing launched) when it does not fit.
-bool gemv_codes_fits(int64_t M, int64_t K);
+bool gemv_codes_fits(int64_t M, int64_t N, int64_t K, int num_sms);
 int launch_gemv_codes(const int8_t *codes, const float *scales, const int8_t *w8, const float *w_scale,
                       const void *bias, void *y, int64_t M, int64_t N, int64_t K, int num_sms, cudaStream_t st,
                       unsigned int *status);

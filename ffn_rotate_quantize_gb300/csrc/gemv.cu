@@ -10,9 +10,12 @@
 // arithmetic.  While the bytes are in flight, the CTA rotates and quantizes x
 // with the same core (and the same fp32 operation order) as the standalone
 // rotate+quantize kernel, so its codes are bit-identical to gbq_quantize_act.
-// Then warps take weight rows, do 16-byte shared loads and int8 dp4a dot
-// products against the quantized x, reduce across lanes and apply the dequant
-// epilogue (fp32(acc) * x_scale, fmaf with the row scale and bias, bf16).
+// Then each warp takes its share of the K columns of every staged weight row,
+// does 16-byte shared loads and int8 dp4a dot products against the quantized x,
+// the partial sums are reduced across lanes and warps, and the dequant epilogue
+// runs (fp32(acc) * x_scale, fmaf with the row scale and bias, bf16).
+#include <algorithm>
+
 #include "gemm.h"
 #include "rotate_fast.cuh"
 
@@ -38,16 +41,66 @@ struct GemvArgs {
     uint32_t x_off, t_off, misc_off;
     uint32_t xb_off;        // bf16 staging of the M token rows (three-pass n = 64 path), else 0
     uint32_t wrow_off;      // register-streaming kernel: staging of slice rows 16.. (0: rows 16.. via registers)
+    uint32_t ep_off;        // ring kernels: epilogue operands of the slice (gv_ep_bytes)
     unsigned int *status;
 };
 
+constexpr int kGvWarps = kGvThreads / 32;
+constexpr int kGcMaxM = 16;  // tokens of the codes GEMV (the kernels that rotate in-kernel take kGvMaxM)
+
+// Tokens padded to a power of two; the dot phase keeps 32 / MP rows of a stage in flight per lane.
+__host__ __device__ constexpr int gv_pad_m(int64_t M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
+// The ring kernels' misc block (token scales, amax slots, stage barriers, abort flag, token barrier)
+// fits in the 128 bytes before the epilogue operands.
+static_assert(2 * kGvMaxM * 4 + (kGvStages + 2) * 8 + 16 <= 128, "misc block exceeds 128 bytes");
+
+// Shared memory of the ring kernels' epilogue operands: w_scale and bias (as fp32) of the CTA's rows,
+// then the warps' partial sums of one stage (32 per warp).
+__host__ __device__ constexpr size_t gv_ep_bytes(int64_t rows_per_cta) {
+    return ((size_t)rows_per_cta * 8 + kGvWarps * 32 * 4 + 127) & ~(size_t)127;
+}
+
+// The slice's w_scale and bias into shared memory (read before the dot products need them; the first
+// stage wait's __syncthreads publishes them).
+__device__ __forceinline__ void gv_load_epilogue(const GemvArgs &p, float *ep, int64_t r0, int nrows) {
+    for (int t = threadIdx.x; t < nrows; t += kGvThreads) {
+        ep[t] = __ldg(p.ws + r0 + t);
+        ep[p.rows_per_cta + t] = p.bias ? __bfloat162float(p.bias[r0 + t]) : 0.0f;
+    }
+}
+
+// 16-byte load from shared memory at a shared-window address (a .shared access, whatever the
+// compiler can prove about the generic pointer it came from).
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
 // Dot products of the staged weight slice against the quantized tokens xq (row
-// stride K) and the dequant epilogue; every thread of the CTA takes part.
-__device__ __forceinline__ void gemv_dot_phase(const GemvArgs &p, uint8_t *stages, const int8_t *xq,
-                                               const float *xs_s, uint64_t *full, int *abort_flag, int64_t r0,
-                                               int nrows, int nchunks) {
+// stride K) and the dequant epilogue; every thread of the CTA takes part.  Warp w
+// owns the same 1/8 of the K columns (16-byte groups) in every stage: per group it
+// reads the tokens' codes once and the group of each of the stage's rows (at most
+// 32 / MP rows, MP = the token count padded to a power of two), so each weight
+// byte is read from shared memory once, with independent dp4a chains per row and
+// token.  A transposing shuffle reduction leaves lane l of every warp with the
+// warp's sum for row l / MP and token l % MP; the eight warps' partial sums are
+// added after the stage's barrier (exact integers: the order does not matter).
+// w_scale and bias come from shared memory (gv_load_epilogue).
+template <int MP, int RB>  // tokens and rows per stage, each padded to a power of two (>= p.M, rows_per_stage)
+__device__ __forceinline__ void gemv_dot_phase_t(const GemvArgs &p, uint8_t *stages, const int8_t *xq,
+                                                 const float *xs_s, uint64_t *full, int *abort_flag, int64_t r0,
+                                                 int nrows, int nchunks, float *ep) {
+    constexpr int NV = MP * RB;  // partial sums per lane, a power of two <= 32
+    static_assert(NV >= 2 && NV <= 32, "2..32 partial sums per lane");
+    constexpr int LANES_PER_V = 32 / NV;  // lanes that end up holding one value's total
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
+    const float *ep_ws = ep;
+    const float *ep_b = ep + p.rows_per_cta;
+    int *part = reinterpret_cast<int *>(ep + 2 * p.rows_per_cta);  // [kGvWarps][32]
     auto issue = [&](int c) {
         const int rows = min(p.rows_per_stage, nrows - c * p.rows_per_stage);
         const uint32_t bytes = (uint32_t)rows * (uint32_t)p.K;
@@ -56,47 +109,110 @@ __device__ __forceinline__ void gemv_dot_phase(const GemvArgs &p, uint8_t *stage
         bulk_g2s(stages + (size_t)(c % kGvStages) * p.stage_bytes, p.w8 + (r0 + (int64_t)c * p.rows_per_stage) * p.K,
                  bytes, bar);
     };
-    // ---- stream the weight slice: dp4a dot products ----
     const int kq = (int)(p.K / 16);
+    const int cpw = (kq + kGvWarps - 1) / kGvWarps;  // 16-byte groups per warp
+    const int i0 = warp * cpw + lane, i1 = min(kq, (warp + 1) * cpw);
+    const uint32_t xq_s = smem_u32(xq), kb = (uint32_t)p.K;
     for (int c = 0; c < nchunks; ++c) {
         const bool ok = mbar_wait(&full[c % kGvStages], (uint32_t)((c / kGvStages) & 1), p.status, abort_flag);
         if (!__syncthreads_and(ok)) break;  // every thread leaves together
         const int rows = min(p.rows_per_stage, nrows - c * p.rows_per_stage);
-        const uint8_t *st = stages + (size_t)(c % kGvStages) * p.stage_bytes;
-        for (int j = warp; j < rows; j += kGvThreads / 32) {
-            const uint4 *wr = reinterpret_cast<const uint4 *>(st + (size_t)j * p.K);
-            int acc[kGvMaxM] = {0, 0, 0, 0};
-            for (int i = lane; i < kq; i += 32) {
-                const uint4 w = wr[i];
+        const uint32_t st_s = smem_u32(stages + (size_t)(c % kGvStages) * p.stage_bytes);
+        int acc[NV];  // [row j][token m] at j * MP + m
 #pragma unroll
-                for (int m = 0; m < kGvMaxM; ++m) {
-                    if (m < p.M) {
-                        const uint4 xv = reinterpret_cast<const uint4 *>(xq + (int64_t)m * p.K)[i];
-                        acc[m] = __dp4a((int)w.x, (int)xv.x, acc[m]);
-                        acc[m] = __dp4a((int)w.y, (int)xv.y, acc[m]);
-                        acc[m] = __dp4a((int)w.z, (int)xv.z, acc[m]);
-                        acc[m] = __dp4a((int)w.w, (int)xv.w, acc[m]);
+        for (int q = 0; q < NV; ++q) acc[q] = 0;
+        for (int i = i0; i < i1; i += 32) {
+            uint4 xv[MP];
+#pragma unroll
+            for (int m = 0; m < MP; ++m)
+                xv[m] = m < p.M ? lds128(xq_s + (uint32_t)m * kb + 16u * (uint32_t)i) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int j = 0; j < RB; ++j) {
+                if (j < rows) {
+                    const uint4 w = lds128(st_s + (uint32_t)j * kb + 16u * (uint32_t)i);
+#pragma unroll
+                    for (int m = 0; m < MP; ++m) {
+                        if (m < p.M) {
+                            int a = acc[j * MP + m];
+                            a = __dp4a((int)w.x, (int)xv[m].x, a);
+                            a = __dp4a((int)w.y, (int)xv[m].y, a);
+                            a = __dp4a((int)w.z, (int)xv[m].z, a);
+                            a = __dp4a((int)w.w, (int)xv[m].w, a);
+                            acc[j * MP + m] = a;
+                        }
                     }
                 }
             }
+        }
+        // Transposing reduction over the lanes: at each level (lane bits 4, 3, ...) a lane keeps the half
+        // of its values selected by its lane bit and adds the partner's copy of that half; once one value
+        // is left, plain butterflies over the remaining lane bits.  Lane l ends with the total of value
+        // l / LANES_PER_V.
 #pragma unroll
-            for (int m = 0; m < kGvMaxM; ++m)
+        for (int o = 16, n = NV; n > 1; o >>= 1, n >>= 1) {
+            const bool up = (lane & o) != 0;
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], o);
-            const int64_t n = r0 + (int64_t)c * p.rows_per_stage + j;
-            if (lane < p.M) {
-                int a = acc[0];
-#pragma unroll
-                for (int m = 1; m < kGvMaxM; ++m)
-                    if (lane == m) a = acc[m];
-                const float b = p.bias ? __bfloat162float(p.bias[n]) : 0.0f;
-                const float tv = __fmul_rn(__int2float_rn(a), xs_s[lane]);
-                if (GBQ_IN_RANGE(p.status, (int64_t)lane * p.N + n, 1, p.M * p.N))
-                    p.y[(int64_t)lane * p.N + n] = __float2bfloat16_rn(__fmaf_rn(tv, __ldg(p.ws + n), b));
+            for (int q = 0; q < n / 2; ++q) {
+                const int send = up ? acc[q] : acc[q + n / 2];
+                const int keep = up ? acc[q + n / 2] : acc[q];
+                acc[q] = keep + __shfl_xor_sync(0xffffffffu, send, o);
             }
         }
+#pragma unroll
+        for (int o = LANES_PER_V / 2; o >= 1; o >>= 1) acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], o);
+        if (lane % LANES_PER_V == 0) part[warp * 32 + lane / LANES_PER_V] = acc[0];
         __syncthreads();
+        if (tid < NV) {
+            const int j = tid / MP, m = tid % MP;
+            if (j < rows && m < p.M) {
+                int a = 0;
+#pragma unroll
+                for (int w = 0; w < kGvWarps; ++w) a += part[w * 32 + tid];
+                const int jr = c * p.rows_per_stage + j;  // row within the slice
+                const int64_t n = r0 + jr;
+                const float tv = __fmul_rn(__int2float_rn(a), xs_s[m]);
+                if (GBQ_IN_RANGE(p.status, (int64_t)m * p.N + n, 1, p.M * p.N))
+                    p.y[(int64_t)m * p.N + n] = __float2bfloat16_rn(__fmaf_rn(tv, ep_ws[jr], ep_b[jr]));
+            }
+        }
         if (tid == 0 && c + kGvStages < nchunks) issue(c + kGvStages);
+    }
+}
+
+// The dot phase for the launch's token count and rows per stage (MAXM: the most tokens the kernel takes).
+template <int MP>
+__device__ __forceinline__ void gemv_dot_phase_m(const GemvArgs &p, uint8_t *stages, const int8_t *xq,
+                                                 const float *xs_s, uint64_t *full, int *abort_flag, int64_t r0,
+                                                 int nrows, int nchunks, float *ep) {
+    const int rb = p.rows_per_stage;  // <= 32 / MP (launcher)
+    if (rb <= 2 || MP * 4 > 32)
+        gemv_dot_phase_t<MP, (MP * 2 <= 32 ? 2 : 1)>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
+    else if (rb <= 4 || MP * 8 > 32)
+        gemv_dot_phase_t<MP, (MP * 4 <= 32 ? 4 : 1)>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
+    else if (rb <= 8 || MP * 16 > 32)
+        gemv_dot_phase_t<MP, (MP * 8 <= 32 ? 8 : 1)>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
+    else if (rb <= 16 || MP * 32 > 32)
+        gemv_dot_phase_t<MP, (MP * 16 <= 32 ? 16 : 1)>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
+    else
+        gemv_dot_phase_t<MP, 32 / MP>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
+}
+
+template <int MAXM>
+__device__ __forceinline__ void gemv_dot_phase(const GemvArgs &p, uint8_t *stages, const int8_t *xq,
+                                               const float *xs_s, uint64_t *full, int *abort_flag, int64_t r0,
+                                               int nrows, int nchunks, float *ep) {
+    switch (gv_pad_m(p.M)) {
+        case 1: gemv_dot_phase_m<1>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep); break;
+        case 2: gemv_dot_phase_m<2>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep); break;
+        case 4: gemv_dot_phase_m<4>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep); break;
+        default:
+            if constexpr (MAXM > 4) {
+                if (gv_pad_m(p.M) == 8)
+                    gemv_dot_phase_m<8>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
+                else
+                    gemv_dot_phase_m<16>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
+            }
+            break;
     }
 }
 
@@ -164,6 +280,8 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(GemvArgs p) {
     } else if (tid == 0) {
         for (int c = 0; c < nchunks && c < kGvStages; ++c) issue(c);
     }
+    float *ep = reinterpret_cast<float *>(smem + p.ep_off);
+    gv_load_epilogue(p, ep, r0, nrows);
 
     if constexpr (LOGN == 6) {
         if (p.G == 1) {
@@ -195,7 +313,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(GemvArgs p) {
                 }
             }
             __syncthreads();
-            gemv_dot_phase(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks);
+            gemv_dot_phase<kGvMaxM>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
             if (tid == 0 && *(volatile int *)abort_flag) {
                 // A wait gave up: let the copies issued at entry land (bounded) before the CTA leaves.
                 for (int c = 0; c <= min(nchunks, kGvStages); ++c) {
@@ -239,7 +357,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(GemvArgs p) {
         __syncthreads();
     }
 
-    gemv_dot_phase(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks);
+    gemv_dot_phase<kGvMaxM>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
 }
 
 // ---------------------------------------------------------------------------
@@ -253,10 +371,12 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_codes_kernel(GemvArgs p, c
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *stages = smem;
     int8_t *xq = reinterpret_cast<int8_t *>(smem + p.x_off);
+    // misc block: token scales [kGcMaxM], stage barriers, codes barrier, abort flag (108 bytes)
+    static_assert(kGcMaxM * 4 + (kGvStages + 1) * 8 + 4 <= 128, "misc block exceeds 128 bytes");
     float *xs_s = reinterpret_cast<float *>(smem + p.misc_off);
-    uint64_t *full = reinterpret_cast<uint64_t *>(xs_s + 2 * kGvMaxM);
-    int *abort_flag = reinterpret_cast<int *>(full + kGvStages);
-    uint64_t *xfull = full + kGvStages + 1;
+    uint64_t *full = reinterpret_cast<uint64_t *>(xs_s + kGcMaxM);
+    uint64_t *xfull = full + kGvStages;
+    int *abort_flag = reinterpret_cast<int *>(xfull + 1);
 
     const int tid = threadIdx.x;
     const int64_t r0 = (int64_t)blockIdx.x * p.rows_per_cta;
@@ -277,6 +397,8 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_codes_kernel(GemvArgs p, c
                      &full[c]);
         }
     }
+    float *ep = reinterpret_cast<float *>(smem + p.ep_off);
+    gv_load_epilogue(p, ep, r0, nrows);  // w_scale and bias: not written by the quantizer
     pdl_wait();  // the codes and scales come from the kernel before
     if (tid == 0) {
         mbar_arrive_expect_tx(xfull, (uint32_t)(p.M * p.K));
@@ -285,7 +407,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_codes_kernel(GemvArgs p, c
     if (tid < p.M) xs_s[tid] = scales[tid];
     __syncthreads();  // barriers initialised, scales in place
     const bool xok = mbar_wait(xfull, 0, p.status, abort_flag);
-    if (__syncthreads_and(xok)) gemv_dot_phase(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks);
+    if (__syncthreads_and(xok)) gemv_dot_phase<kGcMaxM>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
     if (tid == 0 && *(volatile int *)abort_flag) {
         // A wait gave up: let the copies issued at entry land (bounded) before the CTA leaves.
         for (int c = 0; c <= min(nchunks, kGvStages); ++c) {
@@ -692,17 +814,17 @@ int launch_gemv_t(const GemvArgs &base, int num_sms, cudaStream_t st) {
     const size_t x_bytes = (size_t)a.M * a.K;
     size_t t_bytes = (size_t)a.G * RotGeom<LOGN>::TILE * sizeof(float2);
     if (LOGN == 6 && a.G == 1 && t_bytes < fast_tile_bytes(6)) t_bytes = fast_tile_bytes(6);  // three-pass tile
-    const size_t misc = 2 * kGvMaxM * 4 + (kGvStages + 2) * 8 + 16;  // scales, amax, barriers, abort, x barrier
     const size_t xb_bytes = (LOGN == 6 && a.G == 1) ? (size_t)a.M * a.K * 2 + 128 : 0;  // bf16 token staging
-    const size_t fixed = ((x_bytes + 127) & ~(size_t)127) + ((t_bytes + 127) & ~(size_t)127) + 128 + xb_bytes;
-    if (fixed + (size_t)kGvStages * a.K > kGvSmem) return GBQ_ENOTSUP;
     int64_t rpc = (a.N + num_sms - 1) / num_sms;
     const int64_t grid = (a.N + rpc - 1) / rpc;
+    const size_t fixed = ((x_bytes + 127) & ~(size_t)127) + ((t_bytes + 127) & ~(size_t)127) + 128 + xb_bytes +
+                         gv_ep_bytes(rpc);
+    if (fixed + (size_t)kGvStages * a.K > kGvSmem) return GBQ_ENOTSUP;
     const int64_t rps_cap = (int64_t)((kGvSmem - fixed) / kGvStages) / a.K;
     // Rows per stage: the whole slice over the ring when it fits (no more shared memory than needed),
     // else as many as fit.
     const int64_t rps_fit = (rpc + kGvStages - 1) / kGvStages;
-    const int64_t rps = rps_fit <= rps_cap ? rps_fit : rps_cap;
+    const int64_t rps = std::min<int64_t>(std::min(rps_fit, rps_cap), 32 / gv_pad_m(a.M));
     a.rows_per_cta = (int)rpc;
     a.rows_per_stage = (int)rps;
     a.stage_bytes = (uint32_t)(((size_t)rps * a.K + 127) & ~(size_t)127);
@@ -710,7 +832,8 @@ int launch_gemv_t(const GemvArgs &base, int num_sms, cudaStream_t st) {
     a.t_off = a.x_off + (uint32_t)((x_bytes + 127) & ~(size_t)127);
     a.misc_off = a.t_off + (uint32_t)((t_bytes + 127) & ~(size_t)127);
     a.xb_off = 0;
-    size_t smem = a.misc_off + misc;
+    a.ep_off = a.misc_off + 128;  // misc <= 128 bytes
+    size_t smem = a.ep_off + gv_ep_bytes(rpc);
     if (LOGN == 6 && a.G == 1) {
         a.xb_off = (uint32_t)((smem + 127) & ~(size_t)127);
         smem = a.xb_off + (size_t)a.M * a.K * 2;
@@ -731,16 +854,23 @@ int launch_gemv_t(const GemvArgs &base, int num_sms, cudaStream_t st) {
 
 }  // namespace
 
-bool gemv_codes_fits(int64_t M, int64_t K) {
-    if (M < 1 || M > kGvMaxM || K < 16 || K % 16 != 0) return false;
-    const size_t fixed = (((size_t)M * K + 127) & ~(size_t)127) + 128;
+// Shared memory of gemv_codes_kernel besides the weight ring: the codes, the scales and barriers, the
+// epilogue operands.
+size_t gemv_codes_fixed(int64_t M, int64_t N, int64_t K, int num_sms) {
+    const int64_t rpc = (N + num_sms - 1) / num_sms;
+    return (((size_t)M * K + 127) & ~(size_t)127) + 128 + gv_ep_bytes(rpc);
+}
+
+bool gemv_codes_fits(int64_t M, int64_t N, int64_t K, int num_sms) {
+    if (M < 1 || M > kGcMaxM || K < 16 || K % 16 != 0 || N < 1 || num_sms < 1) return false;
+    const size_t fixed = gemv_codes_fixed(M, N, K, num_sms);
     return fixed < kGvSmem && (kGvSmem - fixed) / kGvStages >= (size_t)K + 127;  // one row per stage at least
 }
 
 int launch_gemv_codes(const int8_t *codes, const float *scales, const int8_t *w8, const float *w_scale,
                       const void *bias, void *y, int64_t M, int64_t N, int64_t K, int num_sms, cudaStream_t st,
                       unsigned int *status) {
-    if (!gemv_codes_fits(M, K) || N < 1) return GBQ_ENOTSUP;
+    if (!gemv_codes_fits(M, N, K, num_sms)) return GBQ_ENOTSUP;
     if (((uintptr_t)codes | (uintptr_t)w8) & 15) return GBQ_ENOTSUP;
     GemvArgs a{};
     a.w8 = w8;
@@ -753,20 +883,20 @@ int launch_gemv_codes(const int8_t *codes, const float *scales, const int8_t *w8
     a.G = 1;
     a.status = status;
     const size_t x_bytes = (size_t)M * K;
-    const size_t misc = 2 * kGvMaxM * 4 + (kGvStages + 2) * 8 + 16;  // scales, barriers, abort, codes barrier
-    const size_t fixed = ((x_bytes + 127) & ~(size_t)127) + 128;
+    const size_t fixed = gemv_codes_fixed(M, N, K, num_sms);
     const int64_t rpc = (N + num_sms - 1) / num_sms;
     const int64_t grid = (N + rpc - 1) / rpc;
     // A stage is rows_per_stage weight rows rounded up to 128 bytes (K is a multiple of 16 only).
     const int64_t rps_cap = (int64_t)((kGvSmem - fixed) / kGvStages - 127) / K;
     const int64_t rps_fit = (rpc + kGvStages - 1) / kGvStages;
-    const int64_t rps = rps_fit <= rps_cap ? rps_fit : rps_cap;
+    const int64_t rps = std::min<int64_t>(std::min(rps_fit, rps_cap), 32 / gv_pad_m(M));
     a.rows_per_cta = (int)rpc;
     a.rows_per_stage = (int)rps;
     a.stage_bytes = (uint32_t)(((size_t)rps * K + 127) & ~(size_t)127);
     a.x_off = (uint32_t)((size_t)kGvStages * a.stage_bytes);
     a.misc_off = a.x_off + (uint32_t)((x_bytes + 127) & ~(size_t)127);
-    const size_t smem = a.misc_off + misc;
+    a.ep_off = a.misc_off + 128;  // scales, barriers, abort flag, codes barrier: < 128 bytes
+    const size_t smem = a.ep_off + gv_ep_bytes(rpc);
     static bool attr = false;
     if (!attr) {
         if (cudaFuncSetAttribute(gemv_codes_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGvSmem) !=

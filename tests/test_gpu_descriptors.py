@@ -125,15 +125,19 @@ def test_prepare_weight_any_descriptor(ops, rot):
     assert_int8_parity(w8.cpu().numpy(), w8r, (v / wsr[:, None]).astype(np.float32))
 
 
-# M <= 4 runs the decode GEMV over codes from the rotation kernels (the square in-kernel rotations do
-# not cover these descriptors), larger M the GEMM; both give the same bits as dequant(linear_acc).
-# (16, 16, 128) is square but has too many groups for the in-kernel rotation of the decode GEMV.
+# M <= 16 runs the GEMV over codes from the rotation kernels (for M <= 4 the square in-kernel rotations
+# do not cover these descriptors), larger M the GEMM; both give the same bits as dequant(linear_acc).
+# (16, 16, 128) is square but has too many groups for the in-kernel rotation of the decode GEMV; the
+# square (64, 64, 1) at M = 5, 8 and 16 takes the codes GEMV as a small batch.
 @pytest.mark.parametrize("M,K,N,rot", [(130, 2048, 392, (32, 64, 1)), (1, 2048, 512, (64, 32, 1)),
                                        (64, 8192, 256, (64, 128, 1)), (3, 8192, 300, (128, 64, 1)),
                                        (40, 1024, 200, (8, 8, 16)), (2, 2048, 1000, (32, 64, 1)),
                                        (4, 8192, 777, (64, 128, 1)), (4, 1024, 200, (8, 8, 16)),
                                        (1, 2048, 300, (1, 1, 2048)), (3, 1536, 152, (32, 16, 3)),
-                                       (1, 32768, 160, (16, 16, 128)), (4, 16384, 4096, (128, 128, 1))])
+                                       (1, 32768, 160, (16, 16, 128)), (4, 16384, 4096, (128, 128, 1)),
+                                       (5, 4096, 1000, (64, 64, 1)), (8, 4096, 4096, (64, 64, 1)),
+                                       (16, 4096, 700, (64, 64, 1)), (11, 8192, 300, (64, 128, 1)),
+                                       (16, 2048, 2000, (32, 64, 1)), (7, 1024, 200, (8, 8, 16))])
 def test_linear_any_descriptor(ops, M, K, N, rot):
     c = I.linear_case(M, K, N, n_outliers=max(1, K // 100), outlier_scale=30.0, bias_std=0.01, seed=M + K + N)
     w8, ws = O.prepare_weight(c["w"], rot)
