@@ -936,11 +936,14 @@ int launch_gemv(const void *x, const int8_t *w8, const float *w_scale, const voi
     a.G = groups;
     a.status = status;
     switch (logn) {
-        case 4: return launch_gemv_t<4>(a, num_sms, st);
-        case 5: return launch_gemv_t<5>(a, num_sms, st);
+        // The ring kernel rotates every token in each CTA: past two tokens or K = 4096 the rotation
+        // kernels plus gemv_codes_kernel are faster (measured: K = 8192 as 64x64x2, one token, 27 vs
+        // 24 us; K = 4096 as 32x32x4, four tokens, 17.8 vs 15.1 us), so those return GBQ_ENOTSUP.
+        case 4: return M <= 2 && K <= 4096 ? launch_gemv_t<4>(a, num_sms, st) : GBQ_ENOTSUP;
+        case 5: return M <= 2 && K <= 4096 ? launch_gemv_t<5>(a, num_sms, st) : GBQ_ENOTSUP;
         case 6: {
             const int rc = launch_gemv_direct(a, num_sms, st);
-            return rc == GBQ_ENOTSUP ? launch_gemv_t<6>(a, num_sms, st) : rc;
+            return rc == GBQ_ENOTSUP && M <= 2 && K <= 4096 ? launch_gemv_t<6>(a, num_sms, st) : rc;
         }
         default: return GBQ_ENOTSUP;
     }

@@ -141,7 +141,11 @@ DECODE_CASES = [(1, 4096, 4096, (64, 64, 1), False), (2, 1024, 520, (32, 32, 1),
                 # (N = 4100: 27 rows per CTA, the last CTA 23); four tokens at 32 rows per CTA, where the staging
                 # does not fit two CTAs per SM and rows 2, 3 of every warp come through registers
                 (2, 4096, 3000, (64, 64, 1), True), (3, 4096, 4100, (64, 64, 1), False),
-                (4, 4096, 4864, (64, 64, 1), True), (1, 4096, 4864, (64, 64, 1), True)]
+                (4, 4096, 4864, (64, 64, 1), True), (1, 4096, 4864, (64, 64, 1), True),
+                # the ring kernel with the rotation inside (one or two tokens, K <= 4096): n = 16, n = 16 in
+                # sixteen groups, n = 64 past the register-streaming kernel's 32 rows per CTA
+                (1, 256, 1000, (16, 16, 1), True), (2, 4096, 300, (16, 16, 16), False),
+                (1, 4096, 6000, (64, 64, 1), True)]
 
 
 @pytest.mark.parametrize("M,K,N,rot,with_bias", DECODE_CASES)
