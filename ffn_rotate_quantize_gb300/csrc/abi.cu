@@ -638,7 +638,7 @@ int gbq_linear(const void *x, const int8_t *w8, const float *w_scale, const void
         a.K = K;
         rc = run_rotq("gbq_linear (GEMV codes)", rs, IN_BF16, OUT_S8, a, st);
         if (rc) return rc;
-        return launch_gemv_codes(codes, xs_c, w8, w_scale, bias, y, M, N, K, d->sms, st, d->status);
+        return launch_gemv_codes(codes, xs_c, w8, w_scale, bias, y, N, M, N, K, d->sms, st, d->status);
     }
     Ws w{(uint8_t *)workspace, ws_bytes};
     void *qf = w.take((size_t)M * K * 2);
@@ -675,6 +675,41 @@ int gbq_ffn_fused(const void *x, const int8_t *wg8, const float *s_gate, const i
     if (rc) return rc;
     INIT(dv);
     cudaStream_t st = (cudaStream_t)stream;
+    if (gemv_codes_fits(M, H, d, dv->sms) && gemv_codes_fits(M, d, H, dv->sms)) {
+        // Decode and small batches: the same four steps with int8 codes and weight-streaming GEMVs in
+        // place of the GEMMs (the same codes, scales and epilogues, so the same bits).
+        Ws wc{(uint8_t *)workspace, ws_bytes};
+        int8_t *cx = (int8_t *)wc.take((size_t)M * d * 2);  // the slots of the GEMM route below
+        float *cxs = (float *)wc.take((size_t)M * 4);
+        uint8_t *cgu = (uint8_t *)wc.take((size_t)M * 2 * H * 2);
+        int8_t *ch = (int8_t *)wc.take((size_t)M * H * 2);
+        float *chs = (float *)wc.take((size_t)M * 4);
+        RotArgs a{};
+        a.in0 = x;
+        a.ld_in = d;
+        a.out = cx;
+        a.out_scale = cxs;
+        a.M = M;
+        a.K = d;
+        rc = run_rotq("gbq_ffn_fused (x codes)", rsd, IN_BF16, OUT_S8, a, st);
+        if (rc) return rc;
+        // g | u in bf16, row stride 2H (no bias)
+        rc = launch_gemv_codes(cx, cxs, wg8, s_gate, nullptr, cgu, 2 * H, M, H, d, dv->sms, st, dv->status);
+        if (rc) return rc;
+        rc = launch_gemv_codes(cx, cxs, wu8, s_up, nullptr, cgu + H * 2, 2 * H, M, H, d, dv->sms, st, dv->status);
+        if (rc) return rc;
+        RotArgs ah{};
+        ah.in0 = cgu;
+        ah.in1 = cgu + H * 2;
+        ah.ld_in = 2 * H;
+        ah.out = ch;
+        ah.out_scale = chs;
+        ah.M = M;
+        ah.K = H;
+        rc = run_rotq("gbq_ffn_fused (h codes)", rsh, IN_GLU_BF16, OUT_S8, ah, st);
+        if (rc) return rc;
+        return launch_gemv_codes(ch, chs, wd8, s_down, nullptr, y, d, M, d, H, dv->sms, st, dv->status);
+    }
     Ws w{(uint8_t *)workspace, ws_bytes};
     void *qx = w.take((size_t)M * d * 2);
     float *xs = (float *)w.take((size_t)M * 4);

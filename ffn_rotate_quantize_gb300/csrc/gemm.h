@@ -68,11 +68,13 @@ int launch_gemv(const void *x, const int8_t *w8, const float *w_scale, const voi
                 int64_t N, int64_t K, int logn, int groups, int num_sms, cudaStream_t st, unsigned int *status);
 
 // GEMV (M <= 16) over tokens already quantized: codes int8 [M][K] and row scales fp32 [M] (e.g. in the
-// workspace), y[m][n] = dequant(sum_k codes[m][k] w8[n][k]).  GBQ_ENOTSUP (nothing launched) when it does not fit.
+// workspace), y[m * ld_y + n] = dequant(sum_k codes[m][k] w8[n][k]).  Launched with programmatic stream
+// serialization: it reads the codes and scales only after the preceding kernel completed, w8, w_scale and
+// bias before.  GBQ_ENOTSUP (nothing launched) when it does not fit.
 bool gemv_codes_fits(int64_t M, int64_t N, int64_t K, int num_sms);
 int launch_gemv_codes(const int8_t *codes, const float *scales, const int8_t *w8, const float *w_scale,
-                      const void *bias, void *y, int64_t M, int64_t N, int64_t K, int num_sms, cudaStream_t st,
-                      unsigned int *status);
+                      const void *bias, void *y, int64_t ld_y, int64_t M, int64_t N, int64_t K, int num_sms,
+                      cudaStream_t st, unsigned int *status);
 
 // Elementwise helpers.
 cudaError_t launch_dequant(const int32_t *acc, int64_t ld_acc, const float *xs, const float *ws, const void *bias,

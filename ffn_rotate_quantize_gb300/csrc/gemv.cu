@@ -34,6 +34,7 @@ struct GemvArgs {
     const __nv_bfloat16 *bias;
     __nv_bfloat16 *y;
     int64_t M, N, K;
+    int64_t ld_y;           // elements between token rows of y (ring kernels)
     int G;
     int rows_per_cta;
     int rows_per_stage;
@@ -171,8 +172,8 @@ __device__ __forceinline__ void gemv_dot_phase_t(const GemvArgs &p, uint8_t *sta
                 const int jr = c * p.rows_per_stage + j;  // row within the slice
                 const int64_t n = r0 + jr;
                 const float tv = __fmul_rn(__int2float_rn(a), xs_s[m]);
-                if (GBQ_IN_RANGE(p.status, (int64_t)m * p.N + n, 1, p.M * p.N))
-                    p.y[(int64_t)m * p.N + n] = __float2bfloat16_rn(__fmaf_rn(tv, ep_ws[jr], ep_b[jr]));
+                if (GBQ_IN_RANGE(p.status, (int64_t)m * p.ld_y + n, 1, (p.M - 1) * p.ld_y + p.N))
+                    p.y[(int64_t)m * p.ld_y + n] = __float2bfloat16_rn(__fmaf_rn(tv, ep_ws[jr], ep_b[jr]));
             }
         }
         if (tid == 0 && c + kGvStages < nchunks) issue(c + kGvStages);
@@ -868,9 +869,9 @@ bool gemv_codes_fits(int64_t M, int64_t N, int64_t K, int num_sms) {
 }
 
 int launch_gemv_codes(const int8_t *codes, const float *scales, const int8_t *w8, const float *w_scale,
-                      const void *bias, void *y, int64_t M, int64_t N, int64_t K, int num_sms, cudaStream_t st,
-                      unsigned int *status) {
-    if (!gemv_codes_fits(M, N, K, num_sms)) return GBQ_ENOTSUP;
+                      const void *bias, void *y, int64_t ld_y, int64_t M, int64_t N, int64_t K, int num_sms,
+                      cudaStream_t st, unsigned int *status) {
+    if (!gemv_codes_fits(M, N, K, num_sms) || ld_y < N) return GBQ_ENOTSUP;
     if (((uintptr_t)codes | (uintptr_t)w8) & 15) return GBQ_ENOTSUP;
     GemvArgs a{};
     a.w8 = w8;
@@ -880,6 +881,7 @@ int launch_gemv_codes(const int8_t *codes, const float *scales, const int8_t *w8
     a.M = M;
     a.N = N;
     a.K = K;
+    a.ld_y = ld_y;
     a.G = 1;
     a.status = status;
     const size_t x_bytes = (size_t)M * K;
@@ -933,6 +935,7 @@ int launch_gemv(const void *x, const int8_t *w8, const float *w_scale, const voi
     a.M = M;
     a.N = N;
     a.K = K;
+    a.ld_y = N;
     a.G = groups;
     a.status = status;
     switch (logn) {

@@ -158,7 +158,11 @@ def test_linear_any_descriptor(ops, M, K, N, rot):
 
 @pytest.mark.parametrize("M,dm,H,rd,rh", [(64, 2048, 8192, (32, 64, 1), (64, 128, 1)),
                                           (40, 1024, 2048, (1, 1, 1024), (1, 1, 2048)),
-                                          (33, 512, 1024, (16, 32, 1), (8, 8, 16))])
+                                          (33, 512, 1024, (16, 32, 1), (8, 8, 16)),
+                                          # the GEMV route (M <= 16)
+                                          (1, 2048, 8192, (32, 64, 1), (64, 128, 1)),
+                                          (4, 1024, 2048, (1, 1, 1024), (1, 1, 2048)),
+                                          (3, 512, 1024, (16, 32, 1), (8, 8, 16))])
 def test_ffn_any_descriptor(ops, M, dm, H, rd, rh):
     c = I.ffn_case(M, dm, H, seed=M + dm + H)
     wg8, sg = O.prepare_weight(c["wg"], rd)

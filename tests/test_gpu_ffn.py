@@ -29,8 +29,10 @@ def d(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
 
+# M <= 16 (while the codes fit in shared memory) runs the GEMV route, larger M the GEMMs.
 FFN_CASES = [(200, 1024, 4096, (32, 32, 1), (64, 64, 1)), (16, 256, 1024, (16, 16, 1), (32, 32, 1)),
-             (130, 256, 16384, (16, 16, 1), (128, 128, 1))]
+             (130, 256, 16384, (16, 16, 1), (128, 128, 1)), (1, 1024, 4096, (32, 32, 1), (64, 64, 1)),
+             (5, 1024, 16384, (32, 32, 1), (128, 128, 1))]
 
 
 @pytest.mark.parametrize("M,dm,H,rd,rh", FFN_CASES)
