@@ -401,6 +401,44 @@ def run_ours(args):
                "eager": {"ms": round(gv_ms, 4), "achieved": round(ach, 1), "frac": round(ach / peaks["hbm"], 4),
                          "note": "the same chain launched from Python, one event pair (host launch rate bound)"}}
 
+    small = None
+    if "decode_gemv" in opfn and not args.only:
+        # Few-token calls served by weight-streaming GEMVs (graph-replayed chains of dependent layers whose
+        # weights together exceed L2): the SwiGLU FFN at one token (d = 4096, H = 16384; four layers with
+        # their own weights, 804 MB) and the 4096 x 4096 linear at eight tokens (the 16 decode weight copies).
+        gen = torch.Generator(device=dev).manual_seed(7)
+        dF, HF = FFN["d"], FFN["H"]
+        layers = []
+        for _ in range(4):
+            lw = []
+            for (n_, k_, r_) in ((HF, dF, FFN["rot_d"]), (HF, dF, FFN["rot_d"]), (dF, HF, FFN["rot_h"])):
+                wb = (torch.randn((n_, k_), generator=gen, device=dev) * 0.02).to(torch.bfloat16)
+                lw.extend(G.prepare_weight(wb, r_))
+                del wb
+            layers.append(lw)
+        ws_f1 = torch.empty(G.workspace_size(G.OP_FFN, 1, 0, dF, HF), dtype=torch.uint8, device=dev)
+        xf = [(torch.randn((1, dF), generator=gen, device=dev)).to(torch.bfloat16) for _ in range(9)]
+        ffn1 = lambda i: G.ffn_fused(xf[i], *layers[i % 4], FFN["rot_d"], FFN["rot_h"], ws_f1, out=xf[i + 1])
+        ffn_ms = graph_batch_ms(torch, flush, ffn1, reps=8)
+        ffn_bytes = 3 * HF * dF + 2 * 4 * HF + 4 * dF + 2 * dF * 2
+        ws_m8 = torch.empty(G.workspace_size(G.OP_LINEAR, 8, DECODE["N"], DECODE["K"]), dtype=torch.uint8,
+                            device=dev)
+        x8 = [(torch.randn((8, DECODE["K"]), generator=gen, device=dev)).to(torch.bfloat16) for _ in range(33)]
+        lin8 = lambda i: G.linear(x8[i], w82c[i % len(w82c)], s2, None, DECODE["rot"], ws_m8, out=x8[i + 1])
+        lin8_ms = graph_batch_ms(torch, flush, lin8, reps=32)
+        lin8_bytes = DECODE["N"] * DECODE["K"] + 4 * DECODE["N"] + 2 * 8 * (DECODE["K"] + DECODE["N"])
+        small = {
+            "ffn_decode_1x4096x16384": {
+                "ms": round(ffn_ms, 4), "achieved": round(ffn_bytes / (ffn_ms * 1e-3) * 1e-9, 1), "unit": "GB/s",
+                "frac": round(ffn_bytes / (ffn_ms * 1e-3) * 1e-9 / peaks["hbm"], 4),
+                "route": "x codes -> gate GEMV, up GEMV -> SiLU-GLU + H128(x)H128 codes -> down GEMV"},
+            "linear_8x4096x4096": {
+                "ms": round(lin8_ms, 4), "achieved": round(lin8_bytes / (lin8_ms * 1e-3) * 1e-9, 1),
+                "unit": "GB/s", "frac": round(lin8_bytes / (lin8_ms * 1e-3) * 1e-9 / peaks["hbm"], 4),
+                "route": "rotation kernel -> codes GEMV"},
+            "mode": "CUDA-graph replay of dependent layers (call i's x is call i-1's y), one event pair"}
+        del layers
+
     out = {
         "metric": METRIC, "value": None if value is None else round(value, 2), "unit": "TOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 3), "higher_is_better": True, "scaling": "weak",
@@ -410,7 +448,7 @@ def run_ours(args):
                          "dirty lines); roofline kernels: back-to-back "
                          "launches cycling inputs larger than L2 (4 prefill / 16 decode weight copies)",
                    "parallelism": f"replicas x{world}"},
-        "roofline": roof, "decode_roofline": dec, "rows": rows, "gpu_launches": launches,
+        "roofline": roof, "decode_roofline": dec, "small_batch": small, "rows": rows, "gpu_launches": launches,
         "int8_speedup_vs_rotated_bf16": (round(rows["linear_bf16_rotated"]["ms"] / rows["linear"]["ms"], 3)
                                          if "linear_bf16_rotated" in rows and "linear" in rows else None),
         "kernel_ms_census_step": {k: round(v[1], 3) for k, v in zip(("rotate", "i8gemm", "bf16gemm", "gemv",
