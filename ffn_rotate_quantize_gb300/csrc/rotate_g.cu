@@ -249,6 +249,34 @@ __device__ __forceinline__ void gen_pass_dispatch(int w1, int w2, float *T, int 
     }
 }
 
+// Bytes of one input element (per input tensor) and whether a second tensor (in1) is read.
+template <int IN>
+constexpr int gen_in_bytes() {
+    return (IN == IN_BF16 || IN == IN_GLU_BF16) ? 2 : (IN == IN_S8_ROWSCALE ? 1 : 4);
+}
+template <int IN>
+constexpr bool gen_two_inputs() {
+    return IN == IN_GLU_BF16 || IN == IN_ACC_GLU;
+}
+
+// L2 prefetch hint for the input rows [r0, r0 + nr): one bulk prefetch per row and input tensor, issued
+// by threads 0..nr-1 (a row is K elements, a multiple of 16 bytes, at a 16-byte aligned address).
+template <int IN>
+__device__ __forceinline__ void gen_prefetch_rows(const GenArgs &p, int64_t r0, int nr) {
+    constexpr int EB = gen_in_bytes<IN>();
+    for (int i = threadIdx.x; i < nr; i += kGenThreads) {
+        const int64_t off = (r0 + i) * p.ld_in * EB;
+        const uint32_t bytes = (uint32_t)p.K * EB;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<const uint8_t *>(p.in0) + off),
+                     "r"(bytes)
+                     : "memory");
+        if constexpr (gen_two_inputs<IN>())
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<const uint8_t *>(p.in1) + off),
+                         "r"(bytes)
+                         : "memory");
+    }
+}
+
 template <int IN, int OUT>
 __global__ void __launch_bounds__(kGenThreads, 3) rotg_kernel(const __grid_constant__ GenArgs p) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -266,6 +294,10 @@ __global__ void __launch_bounds__(kGenThreads, 3) rotg_kernel(const __grid_const
         const int E = nr * K;
         if constexpr (OUT != OUT_BF16)
             for (int i = tid; i < nr; i += kGenThreads) rowmax[i] = 0u;
+        {  // the CTA's next chunk streams into L2 while this one is transformed
+            const int64_t cn = c + gridDim.x;
+            if (cn < nchunks) gen_prefetch_rows<IN>(p, cn * p.R, (int)min((int64_t)p.R, p.M - cn * p.R));
+        }
 
         // ---- phase 0: global -> fp32 tile, two 8-value loads per thread in flight
         const int E8 = E >> 3;

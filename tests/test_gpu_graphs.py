@@ -112,7 +112,9 @@ def test_linear_dx_int8_two_stream_split_graph(ops):
     assert_bf16_parity(bf16_np(dx), O.linear_dx_int8(c["dy"], w8, s, rot))
 
 
-@pytest.mark.parametrize("M,K,rot", [(1, 4096, (64, 64, 1)), (3, 4096, (64, 64, 1)), (2, 1024, (32, 32, 1))])
+# The last three run the rotation kernels + codes GEMV (programmatic dependent launch after the quantizer).
+@pytest.mark.parametrize("M,K,rot", [(1, 4096, (64, 64, 1)), (3, 4096, (64, 64, 1)), (2, 1024, (32, 32, 1)),
+                                     (8, 4096, (64, 64, 1)), (1, 2048, (32, 64, 1)), (4, 8192, (64, 64, 2))])
 def test_decode_chain_back_to_back(ops, M, K, rot):
     """Stacked decode layers, each reading the previous layer's output as its x, launched back to
     back (the GEMV waits for the kernel before it while the next call's weight prefetch runs beside
