@@ -1,4 +1,6 @@
 // misc.cu -- memory-bound elementwise kernels of libgbq and workspace sizing.
+#include <algorithm>
+
 #include "common.cuh"
 #include "gemm.h"
 
@@ -6,45 +8,84 @@ namespace gbq {
 namespace {
 
 // y[m, n] = bf16(fmaf(fp32(acc[m, n]) * xs[m], ws[n], bias[n]))  (the page's dequant epilogue,
-// "API": out = acc * x_scale[m] * w_scale[n] + bias[n]); 4 columns per thread when aligned.
+// "API": out = acc * x_scale[m] * w_scale[n] + bias[n]).  Blocks tile (column groups) x (rows): a thread
+// owns 8 consecutive columns and strides over rows, two rows per step (four 16-byte accumulator loads in
+// flight, two 16-byte stores) when the rows and pointers are 16-byte aligned (vec), else element by
+// element.
+__device__ __forceinline__ float dq_one(int32_t a, float x, float w, float b) {
+    return __fmaf_rn(__fmul_rn(__int2float_rn(a), x), w, b);
+}
+
 __global__ void dequant_kernel(const int32_t *__restrict__ acc, int64_t ld_acc, const float *__restrict__ xs,
                                const float *__restrict__ ws, const __nv_bfloat16 *__restrict__ bias,
-                               __nv_bfloat16 *__restrict__ y, int64_t ld_y, int64_t M, int64_t N, int vec4,
+                               __nv_bfloat16 *__restrict__ y, int64_t ld_y, int64_t M, int64_t N, int vec,
                                unsigned int *status) {
-    const int64_t per_row = vec4 ? N / 4 : N;
-    const int64_t total = M * per_row;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t m = i / per_row;
-        const int64_t c = i - m * per_row;
-        if (!(GBQ_IN_RANGE(status, m, 1, M) && GBQ_IN_RANGE(status, vec4 ? 4 * c : c, vec4 ? 4 : 1, N))) continue;
-        const float x = __ldg(xs + m);
-        if (vec4) {
-            const int64_t n = 4 * c;
-            const int4 a = __ldg(reinterpret_cast<const int4 *>(acc + m * ld_acc + n));
-            const float4 w = __ldg(reinterpret_cast<const float4 *>(ws + n));
-            float b[4] = {0.f, 0.f, 0.f, 0.f};
-            if (bias) {
-                const uint2 bb = __ldg(reinterpret_cast<const uint2 *>(bias + n));
-                b[0] = __uint_as_float(bb.x << 16);
-                b[1] = __uint_as_float(bb.x & 0xFFFF0000u);
-                b[2] = __uint_as_float(bb.y << 16);
-                b[3] = __uint_as_float(bb.y & 0xFFFF0000u);
+    const int64_t n0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
+    if (n0 >= N) return;
+    const int cols = (int)min((int64_t)8, N - n0);
+    // Column operands, loaded once for all the thread's rows.
+    float w[8], b[8];
+    if (vec && cols == 8) {
+        const float4 w0 = __ldg(reinterpret_cast<const float4 *>(ws + n0));
+        const float4 w1 = __ldg(reinterpret_cast<const float4 *>(ws + n0) + 1);
+        w[0] = w0.x; w[1] = w0.y; w[2] = w0.z; w[3] = w0.w;
+        w[4] = w1.x; w[5] = w1.y; w[6] = w1.z; w[7] = w1.w;
+        if (bias) {
+            const uint4 bb = __ldg(reinterpret_cast<const uint4 *>(bias + n0));
+            const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                b[2 * k] = __uint_as_float(bw[k] << 16);
+                b[2 * k + 1] = __uint_as_float(bw[k] & 0xFFFF0000u);
             }
-            const float r0 = __fmaf_rn(__fmul_rn(__int2float_rn(a.x), x), w.x, b[0]);
-            const float r1 = __fmaf_rn(__fmul_rn(__int2float_rn(a.y), x), w.y, b[1]);
-            const float r2 = __fmaf_rn(__fmul_rn(__int2float_rn(a.z), x), w.z, b[2]);
-            const float r3 = __fmaf_rn(__fmul_rn(__int2float_rn(a.w), x), w.w, b[3]);
-            __nv_bfloat162 lo = __floats2bfloat162_rn(r0, r1), hi = __floats2bfloat162_rn(r2, r3);
-            uint2 o;
-            o.x = *reinterpret_cast<uint32_t *>(&lo);
-            o.y = *reinterpret_cast<uint32_t *>(&hi);
-            *reinterpret_cast<uint2 *>(y + m * ld_y + n) = o;
         } else {
-            const int64_t n = c;
-            const float b = bias ? __bfloat162float(bias[n]) : 0.0f;
-            const float r = __fmaf_rn(__fmul_rn(__int2float_rn(acc[m * ld_acc + n]), x), __ldg(ws + n), b);
-            y[m * ld_y + n] = __float2bfloat16_rn(r);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) b[k] = 0.0f;
         }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            w[k] = k < cols ? __ldg(ws + n0 + k) : 0.0f;
+            b[k] = (k < cols && bias) ? __bfloat162float(bias[n0 + k]) : 0.0f;
+        }
+    }
+    if (vec && cols == 8) {
+        // Two rows per step: four 16-byte loads in flight per thread.
+        for (int64_t m = blockIdx.y; m < M; m += 2 * (int64_t)gridDim.y) {
+            const int64_t m2 = m + gridDim.y;
+            const bool two = m2 < M;
+            if (!(GBQ_IN_RANGE(status, m, 1, M) && GBQ_IN_RANGE(status, n0, 8, N))) continue;
+            const int4 *ar = reinterpret_cast<const int4 *>(acc + m * ld_acc + n0);
+            const int4 *ar2 = reinterpret_cast<const int4 *>(acc + (two ? m2 : m) * ld_acc + n0);
+            const int4 a0 = __ldcs(ar), a1 = __ldcs(ar + 1);
+            const int4 c0 = __ldcs(ar2), c1 = __ldcs(ar2 + 1);
+            const float x = __ldg(xs + m), x2 = __ldg(xs + (two ? m2 : m));
+            const int a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const int c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+            uint32_t o[4], o2[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                __nv_bfloat162 h = __floats2bfloat162_rn(dq_one(a[2 * k], x, w[2 * k], b[2 * k]),
+                                                         dq_one(a[2 * k + 1], x, w[2 * k + 1], b[2 * k + 1]));
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(dq_one(c[2 * k], x2, w[2 * k], b[2 * k]),
+                                                          dq_one(c[2 * k + 1], x2, w[2 * k + 1], b[2 * k + 1]));
+                o[k] = *reinterpret_cast<uint32_t *>(&h);
+                o2[k] = *reinterpret_cast<uint32_t *>(&h2);
+            }
+            *reinterpret_cast<uint4 *>(y + m * ld_y + n0) = make_uint4(o[0], o[1], o[2], o[3]);
+            if (two && GBQ_IN_RANGE(status, m2, 1, M))
+                *reinterpret_cast<uint4 *>(y + m2 * ld_y + n0) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+        }
+        return;
+    }
+    for (int64_t m = blockIdx.y; m < M; m += gridDim.y) {
+        if (!(GBQ_IN_RANGE(status, m, 1, M) && GBQ_IN_RANGE(status, n0, cols, N))) continue;
+        const float x = __ldg(xs + m);
+        const int32_t *ar = acc + m * ld_acc + n0;
+        __nv_bfloat16 *yr = y + m * ld_y + n0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (k < cols) yr[k] = __float2bfloat16_rn(dq_one(ar[k], x, w[k], b[k]));
     }
 }
 
@@ -102,15 +143,23 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 cudaError_t launch_dequant(const int32_t *acc, int64_t ld_acc, const float *xs, const float *ws, const void *bias,
                            void *y, int64_t ld_y, int64_t M, int64_t N, cudaStream_t st, unsigned int *status) {
-    const int vec4 = (N % 4 == 0 && ld_acc % 4 == 0 && ld_y % 4 == 0 && ((uintptr_t)acc & 15) == 0 &&
-                      ((uintptr_t)y & 7) == 0 && ((uintptr_t)ws & 15) == 0 && ((uintptr_t)bias & 7) == 0)
-                         ? 1
-                         : 0;
-    const int64_t work = M * (vec4 ? N / 4 : N);
+    if (M == 0 || N == 0) return cudaSuccess;
+    // 16-byte accesses: accumulator rows (4-byte elements) and output / bias rows (2-byte elements)
+    // start on 16-byte boundaries.
+    const int vec = (ld_acc % 4 == 0 && ld_y % 8 == 0 && ((uintptr_t)acc & 15) == 0 && ((uintptr_t)y & 15) == 0 &&
+                     ((uintptr_t)ws & 15) == 0 && ((uintptr_t)bias & 15) == 0)
+                        ? 1
+                        : 0;
+    constexpr int kThreads = 128;
+    const int64_t col_groups = (N + 7) / 8;
+    const unsigned gx = (unsigned)((col_groups + kThreads - 1) / kThreads);
+    // One wave of 16 resident 128-thread blocks per SM; each thread then strides over rows (its column
+    // operands loaded once).
+    const int64_t want_rows = ((int64_t)152 * 16 + gx - 1) / gx;
+    const unsigned gy = (unsigned)std::min<int64_t>(std::min<int64_t>(M, 65535), std::max<int64_t>(want_rows, 1));
     prof_begin(4, st);
-    dequant_kernel<<<grid_for(work, 256), 256, 0, st>>>(acc, ld_acc, xs, ws,
-                                                         reinterpret_cast<const __nv_bfloat16 *>(bias),
-                                                         reinterpret_cast<__nv_bfloat16 *>(y), ld_y, M, N, vec4, status);
+    dequant_kernel<<<dim3(gx, gy), kThreads, 0, st>>>(acc, ld_acc, xs, ws, reinterpret_cast<const __nv_bfloat16 *>(bias),
+                                                      reinterpret_cast<__nv_bfloat16 *>(y), ld_y, M, N, vec, status);
     prof_end(st);
     return cudaGetLastError();
 }

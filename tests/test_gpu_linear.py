@@ -252,8 +252,9 @@ def test_linear_acc_chunk_plans_exact(ops):
 
 @pytest.mark.parametrize("M,N,with_bias", [(70000, 16, True), (33, 100, True), (5, 2051, False), (300, 14336, True)])
 def test_dequant_shapes(ops, M, N, with_bias):
-    """The 8-column kernel (including rows striding past the 65535 grid rows) and the 4- and 1-column
-    kernels (N not a multiple of 8) compute the oracle's fp32 operations: identical bits."""
+    """The 8-column path (including rows striding past the grid's rows), ragged last column groups and the
+    element-by-element path (N not a multiple of 8, so rows are not 16-byte aligned) compute the oracle's
+    fp32 operations: identical bits."""
     rng = np.random.default_rng(M + N)
     acc = rng.integers(-2 ** 27, 2 ** 27, (M, N)).astype(np.int32)
     xs = (rng.random(M) * 1e-4).astype(np.float32)
