@@ -675,7 +675,7 @@ int gbq_ffn_fused(const void *x, const int8_t *wg8, const float *s_gate, const i
     if (rc) return rc;
     INIT(dv);
     cudaStream_t st = (cudaStream_t)stream;
-    if (gemv_codes_fits(M, H, d, dv->sms) && gemv_codes_fits(M, d, H, dv->sms)) {
+    if (gemv_codes_fits(M, 2 * H, d, dv->sms) && gemv_codes_fits(M, d, H, dv->sms)) {
         // Decode and small batches: the same four steps with int8 codes and weight-streaming GEMVs in
         // place of the GEMMs (the same codes, scales and epilogues, so the same bits).
         Ws wc{(uint8_t *)workspace, ws_bytes};
@@ -693,10 +693,9 @@ int gbq_ffn_fused(const void *x, const int8_t *wg8, const float *s_gate, const i
         a.K = d;
         rc = run_rotq("gbq_ffn_fused (x codes)", rsd, IN_BF16, OUT_S8, a, st);
         if (rc) return rc;
-        // g | u in bf16, row stride 2H (no bias)
-        rc = launch_gemv_codes(cx, cxs, wg8, s_gate, nullptr, cgu, 2 * H, M, H, d, dv->sms, st, dv->status);
-        if (rc) return rc;
-        rc = launch_gemv_codes(cx, cxs, wu8, s_up, nullptr, cgu + H * 2, 2 * H, M, H, d, dv->sms, st, dv->status);
+        // g | u in bf16, row stride 2H (no bias): one GEMV over the virtual weight [W_gate; W_up]
+        rc = launch_gemv_codes2(cx, cxs, wg8, s_gate, wu8, s_up, H, nullptr, cgu, 2 * H, M, 2 * H, d, dv->sms, st,
+                                dv->status);
         if (rc) return rc;
         RotArgs ah{};
         ah.in0 = cgu;

@@ -75,6 +75,12 @@ bool gemv_codes_fits(int64_t M, int64_t N, int64_t K, int num_sms);
 int launch_gemv_codes(const int8_t *codes, const float *scales, const int8_t *w8, const float *w_scale,
                       const void *bias, void *y, int64_t ld_y, int64_t M, int64_t N, int64_t K, int num_sms,
                       cudaStream_t st, unsigned int *status);
+// The same over the virtual weight [w8; w8b]: rows [0, n_split) from w8 / w_scale, rows [n_split, N) from
+// w8b / w_scale_b (row n - n_split), so y[m][n] covers both (e.g. the FFN's gate | up in one launch).
+int launch_gemv_codes2(const int8_t *codes, const float *scales, const int8_t *w8, const float *w_scale,
+                       const int8_t *w8b, const float *w_scale_b, int64_t n_split, const void *bias, void *y,
+                       int64_t ld_y, int64_t M, int64_t N, int64_t K, int num_sms, cudaStream_t st,
+                       unsigned int *status);
 
 // Elementwise helpers.
 cudaError_t launch_dequant(const int32_t *acc, int64_t ld_acc, const float *xs, const float *ws, const void *bias,

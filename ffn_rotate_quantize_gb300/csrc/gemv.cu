@@ -31,6 +31,11 @@ struct GemvArgs {
     const void *x;
     const int8_t *w8;
     const float *ws;
+    // Ring kernels: rows [n_split, N) of the weight come from w8b / wsb (row n - n_split); n_split = N
+    // for one weight tensor.
+    const int8_t *w8b;
+    const float *wsb;
+    int64_t n_split;
     const __nv_bfloat16 *bias;
     __nv_bfloat16 *y;
     int64_t M, N, K;
@@ -65,9 +70,19 @@ __host__ __device__ constexpr size_t gv_ep_bytes(int64_t rows_per_cta) {
 // stage wait's __syncthreads publishes them).
 __device__ __forceinline__ void gv_load_epilogue(const GemvArgs &p, float *ep, int64_t r0, int nrows) {
     for (int t = threadIdx.x; t < nrows; t += kGvThreads) {
-        ep[t] = __ldg(p.ws + r0 + t);
-        ep[p.rows_per_cta + t] = p.bias ? __bfloat162float(p.bias[r0 + t]) : 0.0f;
+        const int64_t n = r0 + t;
+        ep[t] = n < p.n_split ? __ldg(p.ws + n) : __ldg(p.wsb + (n - p.n_split));
+        ep[p.rows_per_cta + t] = p.bias ? __bfloat162float(p.bias[n]) : 0.0f;
     }
+}
+
+// Bulk copy of weight rows [r, r + rows) into dst (contiguous, K bytes a row), completing on bar; the
+// rows may straddle the split between the two weight tensors.
+__device__ __forceinline__ void gv_copy_rows(const GemvArgs &p, uint8_t *dst, int64_t r, int rows, uint64_t *bar) {
+    const int64_t lo = r < p.n_split ? min((int64_t)rows, p.n_split - r) : 0;  // rows from w8
+    if (lo > 0) bulk_g2s(dst, p.w8 + r * p.K, (uint32_t)(lo * p.K), bar);
+    if (lo < rows)
+        bulk_g2s(dst + lo * p.K, p.w8b + (r + lo - p.n_split) * p.K, (uint32_t)((rows - lo) * p.K), bar);
 }
 
 // 16-byte load from shared memory at a shared-window address (a .shared access, whatever the
@@ -107,8 +122,8 @@ __device__ __forceinline__ void gemv_dot_phase_t(const GemvArgs &p, uint8_t *sta
         const uint32_t bytes = (uint32_t)rows * (uint32_t)p.K;
         uint64_t *bar = &full[c % kGvStages];
         mbar_arrive_expect_tx(bar, bytes);
-        bulk_g2s(stages + (size_t)(c % kGvStages) * p.stage_bytes, p.w8 + (r0 + (int64_t)c * p.rows_per_stage) * p.K,
-                 bytes, bar);
+        gv_copy_rows(p, stages + (size_t)(c % kGvStages) * p.stage_bytes, r0 + (int64_t)c * p.rows_per_stage, rows,
+                     bar);
     };
     const int kq = (int)(p.K / 16);
     const int cpw = (kq + kGvWarps - 1) / kGvWarps;  // 16-byte groups per warp
@@ -252,8 +267,8 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(GemvArgs p) {
         const uint32_t bytes = (uint32_t)rows * (uint32_t)p.K;
         uint64_t *bar = &full[c % kGvStages];
         mbar_arrive_expect_tx(bar, bytes);
-        bulk_g2s(stages + (size_t)(c % kGvStages) * p.stage_bytes, p.w8 + (r0 + (int64_t)c * p.rows_per_stage) * p.K,
-                 bytes, bar);
+        gv_copy_rows(p, stages + (size_t)(c % kGvStages) * p.stage_bytes, r0 + (int64_t)c * p.rows_per_stage, rows,
+                     bar);
     };
     const bool fast_x = (LOGN == 6 && p.G == 1);
     uint64_t *xfull = full + kGvStages + 1;  // after the abort flag's slot
@@ -275,8 +290,8 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(GemvArgs p) {
             for (int c = 0; c < nchunks && c < kGvStages; ++c) {
                 const int rows = min(p.rows_per_stage, nrows - c * p.rows_per_stage);
                 for (int j = warp; j < rows; j += kGvThreads / 32)
-                    bulk_g2s(stages + (size_t)c * p.stage_bytes + (size_t)j * p.K,
-                             p.w8 + (r0 + (int64_t)c * p.rows_per_stage + j) * p.K, (uint32_t)p.K, &full[c]);
+                    gv_copy_rows(p, stages + (size_t)c * p.stage_bytes + (size_t)j * p.K,
+                                 r0 + (int64_t)c * p.rows_per_stage + j, 1, &full[c]);
             }
     } else if (tid == 0) {
         for (int c = 0; c < nchunks && c < kGvStages; ++c) issue(c);
@@ -394,8 +409,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_codes_kernel(GemvArgs p, c
             const int rows = min(p.rows_per_stage, nrows - c * p.rows_per_stage);
             const uint32_t bytes = (uint32_t)rows * (uint32_t)p.K;
             mbar_arrive_expect_tx(&full[c], bytes);
-            bulk_g2s(stages + (size_t)c * p.stage_bytes, p.w8 + (r0 + (int64_t)c * p.rows_per_stage) * p.K, bytes,
-                     &full[c]);
+            gv_copy_rows(p, stages + (size_t)c * p.stage_bytes, r0 + (int64_t)c * p.rows_per_stage, rows, &full[c]);
         }
     }
     float *ep = reinterpret_cast<float *>(smem + p.ep_off);
@@ -868,14 +882,18 @@ bool gemv_codes_fits(int64_t M, int64_t N, int64_t K, int num_sms) {
     return fixed < kGvSmem && (kGvSmem - fixed) / kGvStages >= (size_t)K + 127;  // one row per stage at least
 }
 
-int launch_gemv_codes(const int8_t *codes, const float *scales, const int8_t *w8, const float *w_scale,
-                      const void *bias, void *y, int64_t ld_y, int64_t M, int64_t N, int64_t K, int num_sms,
-                      cudaStream_t st, unsigned int *status) {
-    if (!gemv_codes_fits(M, N, K, num_sms) || ld_y < N) return GBQ_ENOTSUP;
-    if (((uintptr_t)codes | (uintptr_t)w8) & 15) return GBQ_ENOTSUP;
+int launch_gemv_codes2(const int8_t *codes, const float *scales, const int8_t *w8, const float *w_scale,
+                       const int8_t *w8b, const float *w_scale_b, int64_t n_split, const void *bias, void *y,
+                       int64_t ld_y, int64_t M, int64_t N, int64_t K, int num_sms, cudaStream_t st,
+                       unsigned int *status) {
+    if (!gemv_codes_fits(M, N, K, num_sms) || ld_y < N || n_split < 0 || n_split > N) return GBQ_ENOTSUP;
+    if (((uintptr_t)codes | (uintptr_t)w8 | (uintptr_t)w8b) & 15) return GBQ_ENOTSUP;
     GemvArgs a{};
     a.w8 = w8;
     a.ws = w_scale;
+    a.w8b = w8b;
+    a.wsb = w_scale_b;
+    a.n_split = n_split;
     a.bias = reinterpret_cast<const __nv_bfloat16 *>(bias);
     a.y = reinterpret_cast<__nv_bfloat16 *>(y);
     a.M = M;
@@ -923,6 +941,13 @@ int launch_gemv_codes(const int8_t *codes, const float *scales, const int8_t *w8
     return e == cudaSuccess ? GBQ_OK : gbq_fail(GBQ_ECUDA, cudaGetErrorString(e));
 }
 
+int launch_gemv_codes(const int8_t *codes, const float *scales, const int8_t *w8, const float *w_scale,
+                      const void *bias, void *y, int64_t ld_y, int64_t M, int64_t N, int64_t K, int num_sms,
+                      cudaStream_t st, unsigned int *status) {
+    return launch_gemv_codes2(codes, scales, w8, w_scale, w8, w_scale, N, bias, y, ld_y, M, N, K, num_sms, st,
+                              status);
+}
+
 int launch_gemv(const void *x, const int8_t *w8, const float *w_scale, const void *bias, void *y, int64_t M, int64_t N,
                 int64_t K, int logn, int groups, int num_sms, cudaStream_t st, unsigned int *status) {
     if (M < 1 || M > kGvMaxM || K % 128 != 0) return GBQ_ENOTSUP;
@@ -936,6 +961,9 @@ int launch_gemv(const void *x, const int8_t *w8, const float *w_scale, const voi
     a.N = N;
     a.K = K;
     a.ld_y = N;
+    a.w8b = w8;
+    a.wsb = w_scale;
+    a.n_split = N;
     a.G = groups;
     a.status = status;
     switch (logn) {
