@@ -222,7 +222,7 @@ def run_ours(args):
             xr3 = torch.empty_like(x3)
             ops.append(("linear_bf16_rotated", lambda i: (G.rotate_bf16(x3, PREFILL["rot"], out=xr3),
                                                           G.linear_bf16(xr3, wr3, b3, out=y3b))))
-    if want("decode_gemv"):
+    if want("decode_gemv", "small_batch"):
         c2 = I.linear_case(DECODE["M"], DECODE["K"], DECODE["N"], n_outliers=I.outlier_count(DECODE["K"]),
                            outlier_scale=30.0, bias_std=None, seed=0)
         x2 = bf(c2["x"])
@@ -232,8 +232,9 @@ def run_ours(args):
         ws_dec = torch.empty(max(G.workspace_size(G.OP_LINEAR, 1, DECODE["N"], DECODE["K"]), 256),
                              dtype=torch.uint8, device=dev)
         y2 = torch.empty((1, DECODE["N"]), dtype=torch.bfloat16, device=dev)
-        ops.append(("decode_gemv", lambda i: G.linear(x2, w82c[i % len(w82c)], s2, None, DECODE["rot"], ws_dec,
-                                                      out=y2)))
+        if want("decode_gemv"):
+            ops.append(("decode_gemv", lambda i: G.linear(x2, w82c[i % len(w82c)], s2, None, DECODE["rot"],
+                                                          ws_dec, out=y2)))
         # A chain of dependent decode layers (N = K): call i reads call i-1's output as its x.
         chain = [x2] + [torch.empty((1, DECODE["N"]), dtype=torch.bfloat16, device=dev) for _ in range(32)]
         decode_chain = lambda i: G.linear(chain[i % 32], w82c[i % len(w82c)], s2, None, DECODE["rot"], ws_dec,
@@ -402,7 +403,7 @@ def run_ours(args):
                          "note": "the same chain launched from Python, one event pair (host launch rate bound)"}}
 
     small = None
-    if "decode_gemv" in opfn and not args.only:
+    if want("small_batch"):
         # Few-token calls served by weight-streaming GEMVs (graph-replayed chains of dependent layers whose
         # weights together exceed L2): the SwiGLU FFN at one token (d = 4096, H = 16384; four layers with
         # their own weights, 804 MB) and the 4096 x 4096 linear at eight tokens (the 16 decode weight copies).
