@@ -142,20 +142,26 @@ __device__ __forceinline__ void gemv_dot_phase_t(const GemvArgs &p, uint8_t *sta
 #pragma unroll
             for (int m = 0; m < MP; ++m)
                 xv[m] = m < p.M ? lds128(xq_s + (uint32_t)m * kb + 16u * (uint32_t)i) : make_uint4(0, 0, 0, 0);
+            // Rows in groups of up to eight: the group's loads first (independent, in flight together),
+            // then its dot products; rows past the stage's end read as zero and add nothing.
+            constexpr int GR = RB < 8 ? RB : 8;
 #pragma unroll
-            for (int j = 0; j < RB; ++j) {
-                if (j < rows) {
-                    const uint4 w = lds128(st_s + (uint32_t)j * kb + 16u * (uint32_t)i);
+            for (int jg = 0; jg < RB; jg += GR) {
+                uint4 w[GR];
+#pragma unroll
+                for (int jj = 0; jj < GR; ++jj)
+                    w[jj] = jg + jj < rows ? lds128(st_s + (uint32_t)(jg + jj) * kb + 16u * (uint32_t)i)
+                                           : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int jj = 0; jj < GR; ++jj) {
 #pragma unroll
                     for (int m = 0; m < MP; ++m) {
-                        if (m < p.M) {
-                            int a = acc[j * MP + m];
-                            a = __dp4a((int)w.x, (int)xv[m].x, a);
-                            a = __dp4a((int)w.y, (int)xv[m].y, a);
-                            a = __dp4a((int)w.z, (int)xv[m].z, a);
-                            a = __dp4a((int)w.w, (int)xv[m].w, a);
-                            acc[j * MP + m] = a;
-                        }
+                        int a = acc[(jg + jj) * MP + m];
+                        a = __dp4a((int)w[jj].x, (int)xv[m].x, a);
+                        a = __dp4a((int)w[jj].y, (int)xv[m].y, a);
+                        a = __dp4a((int)w[jj].z, (int)xv[m].z, a);
+                        a = __dp4a((int)w[jj].w, (int)xv[m].w, a);
+                        acc[(jg + jj) * MP + m] = a;
                     }
                 }
             }
