@@ -8,8 +8,8 @@ once on a small case, checking a property that holds without any reference imple
     codes are +-127 and its scale fl(fl(1/sqrt K)/127) (n = 16, 64 and 128 factors);
   * exactness: the int8 contraction equals an int64 matrix product; the identity-rotation dequant_weight
     equals one fp32 multiply rounded to bf16;
-  * bit identities between routes: linear == dequant(linear_acc) (prefill and the M = 1 decode GEMV),
-    linear_noalloc == linear, the fused FFN == its chain of public calls;
+  * bit identities between routes: linear == dequant(linear_acc) (the GEMM, the decode GEMV and the codes
+    GEMV), linear_noalloc == linear, the fused FFN (GEMV and GEMM routes) == its chain of public calls;
   * loose bounds: R R = I through the rotate-only path, dequant_weight(prepare_weight(W)) within 2% of W,
     linear_dx against an fp32 product, the int8 dx route within 5% of the bf16 one;
   * a clean device status word afterwards.
@@ -98,31 +98,37 @@ def _layer(G, dev, M, K, N, rot, seed):
 
 
 def check_linear_routes(G, dev):
-    rot = (64, 64, 1)
-    for M in (64, 1):  # the GEMM route and the decode GEMV
-        x, w8, s, bias = _layer(G, dev, M, 4096, 512, rot, seed=M)
+    # the GEMM route, the decode GEMV with the rotation inside, the codes GEMV (a small batch, and one
+    # token with a non-square descriptor)
+    for M, K, rot in ((64, 4096, (64, 64, 1)), (1, 4096, (64, 64, 1)), (8, 4096, (64, 64, 1)),
+                      (1, 2048, (32, 64, 1))):
+        x, w8, s, bias = _layer(G, dev, M, K, 512, rot, seed=M + K)
         y = G.linear(x, w8, s, bias, rot)
         acc, xs = G.linear_acc(x, w8, rot)
         if not _same_bits(y, G.dequant(acc, xs, s, bias)):
-            return False, f"M={M}: linear != dequant(linear_acc)"
+            return False, f"M={M} {rot}: linear != dequant(linear_acc)"
         if not _same_bits(y, G.linear_noalloc(x, w8, s, bias, rot)):
-            return False, f"M={M}: linear_noalloc != linear"
-    return True, "linear == dequant(linear_acc) == linear_noalloc, bit for bit, at M = 64 and M = 1"
+            return False, f"M={M} {rot}: linear_noalloc != linear"
+    return True, ("linear == dequant(linear_acc) == linear_noalloc, bit for bit: GEMM (M = 64), decode GEMV "
+                  "(M = 1), codes GEMV (M = 8; M = 1 with 32 x 64)")
 
 
 def check_ffn_chain(G, dev):
-    M, d, H, rd, rh = 16, 256, 1024, (16, 16, 1), (32, 32, 1)
-    g = np.random.default_rng(3)
-    x = _bf16(g.standard_normal((M, d)), dev)
-    wg8, sg = G.prepare_weight(_bf16(g.standard_normal((H, d)) * 0.02, dev), rd)
-    wu8, su = G.prepare_weight(_bf16(g.standard_normal((H, d)) * 0.02, dev), rd)
-    wd8, sd = G.prepare_weight(_bf16(g.standard_normal((d, H)) * 0.02, dev), rh)
-    y = G.ffn_fused(x, wg8, sg, wu8, su, wd8, sd, rd, rh)
-    accg, xs = G.linear_acc(x, wg8, rd)
-    accu, _ = G.linear_acc(x, wu8, rd)
-    qh, hs = G.dequant_act_quantize(accg, accu, xs, sg, su, rh)
-    y_chain = G.dequant(G.int8_gemm(qh, wd8), hs, sd)
-    return _same_bits(y, y_chain), f"ffn_fused == chain of public calls, {M}x{d}x{H}"
+    d, H, rd, rh = 256, 1024, (16, 16, 1), (32, 32, 1)
+    for M in (16, 64):  # the GEMV route (few tokens) and the GEMM route
+        g = np.random.default_rng(3 + M)
+        x = _bf16(g.standard_normal((M, d)), dev)
+        wg8, sg = G.prepare_weight(_bf16(g.standard_normal((H, d)) * 0.02, dev), rd)
+        wu8, su = G.prepare_weight(_bf16(g.standard_normal((H, d)) * 0.02, dev), rd)
+        wd8, sd = G.prepare_weight(_bf16(g.standard_normal((d, H)) * 0.02, dev), rh)
+        y = G.ffn_fused(x, wg8, sg, wu8, su, wd8, sd, rd, rh)
+        accg, xs = G.linear_acc(x, wg8, rd)
+        accu, _ = G.linear_acc(x, wu8, rd)
+        qh, hs = G.dequant_act_quantize(accg, accu, xs, sg, su, rh)
+        y_chain = G.dequant(G.int8_gemm(qh, wd8), hs, sd)
+        if not _same_bits(y, y_chain):
+            return False, f"M={M}: ffn_fused != chain of public calls"
+    return True, f"ffn_fused == chain of public calls (GEMM-only), {d}x{H}, M = 16 (GEMVs) and 64 (GEMMs)"
 
 
 def check_rotation_involution(G, dev):
