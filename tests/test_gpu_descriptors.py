@@ -137,7 +137,11 @@ def test_prepare_weight_any_descriptor(ops, rot):
                                        (1, 32768, 160, (16, 16, 128)), (4, 16384, 4096, (128, 128, 1)),
                                        (5, 4096, 1000, (64, 64, 1)), (8, 4096, 4096, (64, 64, 1)),
                                        (16, 4096, 700, (64, 64, 1)), (11, 8192, 300, (64, 128, 1)),
-                                       (16, 2048, 2000, (32, 64, 1)), (7, 1024, 200, (8, 8, 16))])
+                                       (16, 2048, 2000, (32, 64, 1)), (7, 1024, 200, (8, 8, 16)),
+                                       # edges of the codes GEMV: fewer weight rows than warps or SMs, one
+                                       # row per ring stage at K = 32768, and past its shared-memory limit
+                                       (16, 64, 1, (8, 8, 1)), (3, 64, 5, (2, 32, 1)),
+                                       (2, 32768, 100, (128, 256, 1)), (4, 32768, 100, (128, 256, 1))])
 def test_linear_any_descriptor(ops, M, K, N, rot):
     c = I.linear_case(M, K, N, n_outliers=max(1, K // 100), outlier_scale=30.0, bias_std=0.01, seed=M + K + N)
     w8, ws = O.prepare_weight(c["w"], rot)
