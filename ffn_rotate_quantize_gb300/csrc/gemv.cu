@@ -86,12 +86,14 @@ __device__ __forceinline__ void gv_copy_rows(const GemvArgs &p, uint8_t *dst, in
 }
 
 // 16-byte load from shared memory at a shared-window address (a .shared access, whatever the
-// compiler can prove about the generic pointer it came from).
+// compiler can prove about the generic pointer it came from).  The memory clobber keeps it after the
+// barriers and plain stores that publish what it reads.
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr));
+                 : "r"(addr)
+                 : "memory");
     return v;
 }
 
