@@ -39,6 +39,17 @@ def _req(t, dtype, name):
         raise ValueError(f"{name}: expected a contiguous CUDA {dtype} tensor, got {t.dtype} on {t.device}")
 
 
+def _out(out, shape, dtype, device, name="out"):
+    """A new output tensor, or the caller's after checking that it has exactly the expected shape and type
+    (the C ABI takes raw pointers and writes shape-many elements)."""
+    if out is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    _req(out, dtype, name)
+    if tuple(out.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(out.shape)}")
+    return out
+
+
 def init() -> str:
     check(lib().gbq_init())
     return lib().gbq_device_name().decode()
@@ -125,7 +136,7 @@ def rotate_bf16(x: torch.Tensor, r, stream=None, out=None):
     """bf16 [M,K] -> bf16(R x)."""
     _req(x, torch.bfloat16, "x")
     M, K = x.shape
-    y = torch.empty_like(x) if out is None else out
+    y = _out(out, x.shape, torch.bfloat16, x.device)
     check(lib().gbq_rotate_bf16(_ptr(x), _ptr(y), M, K, _rot(r), _stream(stream)))
     return y
 
@@ -136,7 +147,7 @@ def linear_bf16(x: torch.Tensor, w: torch.Tensor, bias=None, out=None, stream=No
     _req(w, torch.bfloat16, "w")
     M, K = x.shape
     N = w.shape[0]
-    y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device) if out is None else out
+    y = _out(out, (M, N), torch.bfloat16, x.device)
     check(lib().gbq_linear_bf16(_ptr(x), _ptr(w), _ptr(bias), _ptr(y), M, N, K,
                                 _stream(stream)))
     return y
@@ -174,7 +185,7 @@ def dequant(acc: torch.Tensor, x_scale, w_scale, bias=None, out=None, stream=Non
     if acc.dtype != torch.int32 or acc.stride(1) != 1:
         raise ValueError("acc must be int32 with unit column stride")
     M, N = acc.shape
-    y = torch.empty((M, N), dtype=torch.bfloat16, device=acc.device) if out is None else out
+    y = _out(out, (M, N), torch.bfloat16, acc.device)
     check(lib().gbq_dequant(_ptr(acc), acc.stride(0), _ptr(x_scale), _ptr(w_scale), _ptr(bias), _ptr(y),
                             y.stride(0), M, N, _stream(stream)))
     return y
@@ -186,7 +197,7 @@ def linear(x: torch.Tensor, w8: torch.Tensor, w_scale, bias, r, workspace=None, 
     _req(w8, torch.int8, "w8")
     M, K = x.shape
     N = w8.shape[0]
-    y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device) if out is None else out
+    y = _out(out, (M, N), torch.bfloat16, x.device)
     ws, n = _workspace(OP_LINEAR, M, N, K, 0, x.device, workspace)
     check(lib().gbq_linear(_ptr(x), _ptr(w8), _ptr(w_scale), _ptr(bias), _ptr(y), M, N, K, _rot(r), _ptr(ws), n,
                            _stream(stream)))
@@ -199,7 +210,7 @@ def linear_noalloc(x: torch.Tensor, w8: torch.Tensor, w_scale, bias, r, out=None
     _req(w8, torch.int8, "w8")
     M, K = x.shape
     N = w8.shape[0]
-    y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device) if out is None else out
+    y = _out(out, (M, N), torch.bfloat16, x.device)
     check(lib().gbq_linear_noalloc(_ptr(x), _ptr(w8), _ptr(w_scale), _ptr(bias), _ptr(y), M, N, K, _rot(r),
                                    _stream(stream)))
     return y
@@ -211,7 +222,7 @@ def ffn_fused(x, wg8, s_gate, wu8, s_up, wd8, s_down, rot_d, rot_h, workspace=No
     _req(x, torch.bfloat16, "x")
     M, d = x.shape
     H = wg8.shape[0]
-    y = torch.empty((M, d), dtype=torch.bfloat16, device=x.device) if out is None else out
+    y = _out(out, (M, d), torch.bfloat16, x.device)
     ws, n = _workspace(OP_FFN, M, 0, d, H, x.device, workspace)
     check(lib().gbq_ffn_fused(_ptr(x), _ptr(wg8), _ptr(s_gate), _ptr(wu8), _ptr(s_up), _ptr(wd8), _ptr(s_down),
                               _ptr(y), M, d, H, _rot(rot_d), _rot(rot_h), _ptr(ws), n, _stream(stream)))
@@ -234,7 +245,7 @@ def linear_dx(dy: torch.Tensor, w: torch.Tensor, out=None, stream=None):
     _req(w, torch.bfloat16, "w")
     M, N = dy.shape
     K = w.shape[1]
-    dx = torch.empty((M, K), dtype=torch.bfloat16, device=dy.device) if out is None else out
+    dx = _out(out, (M, K), torch.bfloat16, dy.device)
     check(lib().gbq_linear_dx(_ptr(dy), _ptr(w), _ptr(dx), M, N, K, _stream(stream)))
     return dx
 
@@ -245,7 +256,7 @@ def linear_dx_int8(dy: torch.Tensor, w8: torch.Tensor, w_scale, r, workspace=Non
     _req(w8, torch.int8, "w8")
     M, N = dy.shape
     K = w8.shape[1]
-    dx = torch.empty((M, K), dtype=torch.bfloat16, device=dy.device) if out is None else out
+    dx = _out(out, (M, K), torch.bfloat16, dy.device)
     ws, n = _workspace(OP_LINEAR_DX_INT8, M, N, K, 0, dy.device, workspace)
     check(lib().gbq_linear_dx_int8(_ptr(dy), _ptr(w8), _ptr(w_scale), _ptr(dx), M, N, K, _rot(r), _ptr(ws), n,
                                    _stream(stream)))

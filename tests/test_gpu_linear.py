@@ -262,3 +262,17 @@ def test_dequant_shapes(ops, M, N, with_bias):
     bias = I.bf16_bits(rng.standard_normal(N).astype(np.float32) * 0.01) if with_bias else None
     y = ops.dequant(d(acc), d(xs), d(ws), bf16_dev(bias) if with_bias else None)
     assert np.array_equal(bf16_np(y), O.dequant(acc.astype(np.int64), xs, ws, bias))
+
+
+def test_binding_rejects_wrong_output_shape(ops):
+    """The binding checks a caller's output tensor before the C call writes M x N elements through it."""
+    x = torch.zeros((2, 256), dtype=torch.bfloat16, device="cuda")
+    w8 = torch.zeros((64, 256), dtype=torch.int8, device="cuda")
+    s = torch.ones((64,), dtype=torch.float32, device="cuda")
+    with pytest.raises(ValueError):
+        ops.linear(x, w8, s, None, (16, 16, 1), out=torch.empty((2, 32), dtype=torch.bfloat16, device="cuda"))
+    with pytest.raises(ValueError):
+        ops.linear(x, w8, s, None, (16, 16, 1), out=torch.empty((2, 64), dtype=torch.float32, device="cuda"))
+    y = ops.linear(x, w8, s, None, (16, 16, 1), out=torch.empty((2, 64), dtype=torch.bfloat16, device="cuda"))
+    torch.cuda.synchronize()
+    assert y.shape == (2, 64) and bool((y.float() == 0).all())
