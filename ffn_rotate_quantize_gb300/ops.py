@@ -39,6 +39,23 @@ def _req(t, dtype, name):
         raise ValueError(f"{name}: expected a contiguous CUDA {dtype} tensor, got {t.dtype} on {t.device}")
 
 
+def _vec(t, n, dtype, name, optional=False):
+    """A per-row / per-column vector argument: a contiguous CUDA tensor of n elements of dtype."""
+    if t is None and optional:
+        return
+    if t is None:
+        raise ValueError(f"{name}: required")
+    _req(t, dtype, name)
+    if t.numel() != n:
+        raise ValueError(f"{name}: expected {n} elements, got {t.numel()}")
+
+
+def _mat(t, shape, dtype, name):
+    _req(t, dtype, name)
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
 def _out(out, shape, dtype, device, name="out"):
     """A new output tensor, or the caller's after checking that it has exactly the expected shape and type
     (the C ABI takes raw pointers and writes shape-many elements)."""
@@ -82,10 +99,14 @@ def workspace_size(op: int, M: int, N: int = 0, K: int = 0, H: int = 0) -> int:
 
 
 def _workspace(op, M, N, K, H, device, workspace=None):
-    n = workspace_size(op, M, N, K, H)
+    """(workspace, its size in bytes): a new one of the size the library asks for, or the caller's, whose
+    actual size is passed on (the library rejects one that is too small)."""
     if workspace is None:
-        workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=device)
-    return workspace, n
+        n = workspace_size(op, M, N, K, H)
+        return torch.empty(max(n, 1), dtype=torch.uint8, device=device), n
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace: expected a contiguous CUDA tensor")
+    return workspace, workspace.numel() * workspace.element_size()
 
 
 # ------------------------------------------------------------------ rotate + quantize
@@ -112,8 +133,8 @@ def prepare_weight(w: torch.Tensor, r, stream=None):
 def quantize_act_glu(g: torch.Tensor, u: torch.Tensor, r, stream=None):
     """(bf16 g, bf16 u) [M,H] -> quantize(R (silu(g) * u))."""
     _req(g, torch.bfloat16, "g")
-    _req(u, torch.bfloat16, "u")
     M, H = g.shape
+    _mat(u, (M, H), torch.bfloat16, "u")
     q = torch.empty((M, H), dtype=torch.int8, device=g.device)
     s = torch.empty((M,), dtype=torch.float32, device=g.device)
     check(lib().gbq_quantize_act_glu(_ptr(g), _ptr(u), _ptr(q), _ptr(s), M, H, _rot(r), _stream(stream)))
@@ -123,8 +144,11 @@ def quantize_act_glu(g: torch.Tensor, u: torch.Tensor, r, stream=None):
 def dequant_act_quantize(acc_g, acc_u, x_scale, s_gate, s_up, r, stream=None):
     """int32 gate/up accumulators -> quantize(R (silu(dequant(acc_g)) * dequant(acc_u)))."""
     _req(acc_g, torch.int32, "acc_g")
-    _req(acc_u, torch.int32, "acc_u")
     M, H = acc_g.shape
+    _mat(acc_u, (M, H), torch.int32, "acc_u")
+    _vec(x_scale, M, torch.float32, "x_scale")
+    _vec(s_gate, H, torch.float32, "s_gate")
+    _vec(s_up, H, torch.float32, "s_up")
     q = torch.empty((M, H), dtype=torch.int8, device=acc_g.device)
     s = torch.empty((M,), dtype=torch.float32, device=acc_g.device)
     check(lib().gbq_dequant_act_quantize(_ptr(acc_g), _ptr(acc_u), H, _ptr(x_scale), _ptr(s_gate), _ptr(s_up),
@@ -144,9 +168,10 @@ def rotate_bf16(x: torch.Tensor, r, stream=None, out=None):
 def linear_bf16(x: torch.Tensor, w: torch.Tensor, bias=None, out=None, stream=None):
     """bf16 x [M,K] @ bf16 w[N,K]^T + bias [N] -> bf16 y [M,N] (the rotate-only path's linear)."""
     _req(x, torch.bfloat16, "x")
-    _req(w, torch.bfloat16, "w")
     M, K = x.shape
     N = w.shape[0]
+    _mat(w, (N, K), torch.bfloat16, "w")
+    _vec(bias, N, torch.bfloat16, "bias", optional=True)
     y = _out(out, (M, N), torch.bfloat16, x.device)
     check(lib().gbq_linear_bf16(_ptr(x), _ptr(w), _ptr(bias), _ptr(y), M, N, K,
                                 _stream(stream)))
@@ -157,9 +182,9 @@ def linear_bf16(x: torch.Tensor, w: torch.Tensor, bias=None, out=None, stream=No
 def int8_gemm(q: torch.Tensor, w8: torch.Tensor, workspace=None, stream=None):
     """int8 [M,K] x int8 [N,K] -> int32 [M,N], exact."""
     _req(q, torch.int8, "q")
-    _req(w8, torch.int8, "w8")
     M, K = q.shape
     N = w8.shape[0]
+    _mat(w8, (N, K), torch.int8, "w8")
     acc = torch.empty((M, N), dtype=torch.int32, device=q.device)
     ws, n = _workspace(OP_INT8_GEMM, M, N, K, 0, q.device, workspace)
     check(lib().gbq_int8_gemm(_ptr(q), _ptr(w8), _ptr(acc), N, M, N, K, _ptr(ws), n, _stream(stream)))
@@ -169,9 +194,9 @@ def int8_gemm(q: torch.Tensor, w8: torch.Tensor, workspace=None, stream=None):
 def linear_acc(x: torch.Tensor, w8: torch.Tensor, r, workspace=None, stream=None):
     """bf16 x [M,K] -> (int32 acc [M,N], fp32 x_scale [M])."""
     _req(x, torch.bfloat16, "x")
-    _req(w8, torch.int8, "w8")
     M, K = x.shape
     N = w8.shape[0]
+    _mat(w8, (N, K), torch.int8, "w8")
     acc = torch.empty((M, N), dtype=torch.int32, device=x.device)
     xs = torch.empty((M,), dtype=torch.float32, device=x.device)
     ws, n = _workspace(OP_LINEAR, M, N, K, 0, x.device, workspace)
@@ -185,6 +210,9 @@ def dequant(acc: torch.Tensor, x_scale, w_scale, bias=None, out=None, stream=Non
     if acc.dtype != torch.int32 or acc.stride(1) != 1:
         raise ValueError("acc must be int32 with unit column stride")
     M, N = acc.shape
+    _vec(x_scale, M, torch.float32, "x_scale")
+    _vec(w_scale, N, torch.float32, "w_scale")
+    _vec(bias, N, torch.bfloat16, "bias", optional=True)
     y = _out(out, (M, N), torch.bfloat16, acc.device)
     check(lib().gbq_dequant(_ptr(acc), acc.stride(0), _ptr(x_scale), _ptr(w_scale), _ptr(bias), _ptr(y),
                             y.stride(0), M, N, _stream(stream)))
@@ -194,9 +222,11 @@ def dequant(acc: torch.Tensor, x_scale, w_scale, bias=None, out=None, stream=Non
 def linear(x: torch.Tensor, w8: torch.Tensor, w_scale, bias, r, workspace=None, out=None, stream=None):
     """bf16 x [M,K] -> bf16 y [M,N] = dequant(linear_acc(x))."""
     _req(x, torch.bfloat16, "x")
-    _req(w8, torch.int8, "w8")
     M, K = x.shape
     N = w8.shape[0]
+    _mat(w8, (N, K), torch.int8, "w8")
+    _vec(w_scale, N, torch.float32, "w_scale")
+    _vec(bias, N, torch.bfloat16, "bias", optional=True)
     y = _out(out, (M, N), torch.bfloat16, x.device)
     ws, n = _workspace(OP_LINEAR, M, N, K, 0, x.device, workspace)
     check(lib().gbq_linear(_ptr(x), _ptr(w8), _ptr(w_scale), _ptr(bias), _ptr(y), M, N, K, _rot(r), _ptr(ws), n,
@@ -207,9 +237,11 @@ def linear(x: torch.Tensor, w8: torch.Tensor, w_scale, bias, r, workspace=None, 
 def linear_noalloc(x: torch.Tensor, w8: torch.Tensor, w_scale, bias, r, out=None, stream=None):
     """linear() without a workspace: the library's static device scratch is used (see include/gbq.h)."""
     _req(x, torch.bfloat16, "x")
-    _req(w8, torch.int8, "w8")
     M, K = x.shape
     N = w8.shape[0]
+    _mat(w8, (N, K), torch.int8, "w8")
+    _vec(w_scale, N, torch.float32, "w_scale")
+    _vec(bias, N, torch.bfloat16, "bias", optional=True)
     y = _out(out, (M, N), torch.bfloat16, x.device)
     check(lib().gbq_linear_noalloc(_ptr(x), _ptr(w8), _ptr(w_scale), _ptr(bias), _ptr(y), M, N, K, _rot(r),
                                    _stream(stream)))
@@ -222,6 +254,12 @@ def ffn_fused(x, wg8, s_gate, wu8, s_up, wd8, s_down, rot_d, rot_h, workspace=No
     _req(x, torch.bfloat16, "x")
     M, d = x.shape
     H = wg8.shape[0]
+    _mat(wg8, (H, d), torch.int8, "wg8")
+    _mat(wu8, (H, d), torch.int8, "wu8")
+    _mat(wd8, (d, H), torch.int8, "wd8")
+    _vec(s_gate, H, torch.float32, "s_gate")
+    _vec(s_up, H, torch.float32, "s_up")
+    _vec(s_down, d, torch.float32, "s_down")
     y = _out(out, (M, d), torch.bfloat16, x.device)
     ws, n = _workspace(OP_FFN, M, 0, d, H, x.device, workspace)
     check(lib().gbq_ffn_fused(_ptr(x), _ptr(wg8), _ptr(s_gate), _ptr(wu8), _ptr(s_up), _ptr(wd8), _ptr(s_down),
@@ -234,6 +272,7 @@ def dequant_weight(w8: torch.Tensor, w_scale, r, stream=None):
     """int8 W8 [N,K] + fp32 s [N] -> bf16 W [N,K], un-rotated."""
     _req(w8, torch.int8, "w8")
     N, K = w8.shape
+    _vec(w_scale, N, torch.float32, "w_scale")
     w = torch.empty((N, K), dtype=torch.bfloat16, device=w8.device)
     check(lib().gbq_dequant_weight(_ptr(w8), _ptr(w_scale), _ptr(w), N, K, _rot(r), _stream(stream)))
     return w
@@ -242,9 +281,9 @@ def dequant_weight(w8: torch.Tensor, w_scale, r, stream=None):
 def linear_dx(dy: torch.Tensor, w: torch.Tensor, out=None, stream=None):
     """bf16 dy [M,N] @ bf16 W [N,K] -> bf16 dx [M,K]."""
     _req(dy, torch.bfloat16, "dy")
-    _req(w, torch.bfloat16, "w")
     M, N = dy.shape
     K = w.shape[1]
+    _mat(w, (N, K), torch.bfloat16, "w")
     dx = _out(out, (M, K), torch.bfloat16, dy.device)
     check(lib().gbq_linear_dx(_ptr(dy), _ptr(w), _ptr(dx), M, N, K, _stream(stream)))
     return dx
@@ -253,9 +292,10 @@ def linear_dx(dy: torch.Tensor, w: torch.Tensor, out=None, stream=None):
 def linear_dx_int8(dy: torch.Tensor, w8: torch.Tensor, w_scale, r, workspace=None, out=None, stream=None):
     """dx through the int8 route: quantize dy*s, int8 GEMM against W8, rotate back."""
     _req(dy, torch.bfloat16, "dy")
-    _req(w8, torch.int8, "w8")
     M, N = dy.shape
     K = w8.shape[1]
+    _mat(w8, (N, K), torch.int8, "w8")
+    _vec(w_scale, N, torch.float32, "w_scale")
     dx = _out(out, (M, K), torch.bfloat16, dy.device)
     ws, n = _workspace(OP_LINEAR_DX_INT8, M, N, K, 0, dy.device, workspace)
     check(lib().gbq_linear_dx_int8(_ptr(dy), _ptr(w8), _ptr(w_scale), _ptr(dx), M, N, K, _rot(r), _ptr(ws), n,

@@ -276,3 +276,14 @@ def test_binding_rejects_wrong_output_shape(ops):
     y = ops.linear(x, w8, s, None, (16, 16, 1), out=torch.empty((2, 64), dtype=torch.bfloat16, device="cuda"))
     torch.cuda.synchronize()
     assert y.shape == (2, 64) and bool((y.float() == 0).all())
+    # inputs: a weight of the wrong width, a scale or bias vector of the wrong length
+    with pytest.raises(ValueError):
+        ops.linear(x, torch.zeros((64, 128), dtype=torch.int8, device="cuda"), s, None, (16, 16, 1))
+    with pytest.raises(ValueError):
+        ops.linear(x, w8, torch.ones((32,), dtype=torch.float32, device="cuda"), None, (16, 16, 1))
+    with pytest.raises(ValueError):
+        ops.linear(x, w8, s, torch.zeros((65,), dtype=torch.bfloat16, device="cuda"), (16, 16, 1))
+    # a caller's workspace is passed with its real size: one too small is refused by the library
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(Exception, match="workspace"):
+        ops.linear(x, w8, s, None, (16, 16, 1), workspace=small)
