@@ -74,10 +74,11 @@ def _linear_pair(ops, M, K, N, rot, seed, with_bias=True):
 
 def test_noalloc_large_call_then_smaller_calls(ops):
     """A call that fills most of the scratch, then smaller ones (whose scratch is a prefix of what the large
-    call wrote), then a non-square rotation: every result equals gbq_linear on a workspace, bit for bit, so
-    nothing left in the shared array by an earlier call reaches a later one."""
+    call wrote), then a non-square rotation, then the few-token GEMV over codes in the scratch: every result
+    equals gbq_linear on a workspace, bit for bit, so nothing left in the shared array by an earlier call
+    reaches a later one."""
     cases = [(1500, 4096, 256, (64, 64, 1)), (37, 4096, 300, (64, 64, 1)), (2, 4096, 520, (64, 64, 1)),
-             (129, 2048, 200, (32, 64, 1))]
+             (129, 2048, 200, (32, 64, 1)), (8, 4096, 300, (64, 64, 1)), (1, 2048, 200, (32, 64, 1))]
     for i, (M, K, N, rot) in enumerate(cases):
         y, y_ref = _linear_pair(ops, M, K, N, rot, seed=300 + i)
         assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16)), (M, K, N, rot)
