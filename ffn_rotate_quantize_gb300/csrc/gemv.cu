@@ -1,4 +1,4 @@
-// gemv.cu -- decode path (M <= 4): y = dequant(quantize(R x) @ W8^T), weight streaming.
+// gemv.cu -- decode and small-batch path (M <= 16): y = dequant(quantize(R x) @ W8^T), weight streaming.
 //
 // What it computes: the rotated-INT8 linear layer of the PyPI page
 // "xpu-kernels 0.2.0" ("Use from Python": linear), for a handful of tokens,
@@ -6,14 +6,22 @@
 //
 // Design: one CTA per SM, each owning a contiguous slice of weight rows.  At
 // entry one thread issues bulk copies (cp.async.bulk, mbarrier-tracked) of the
-// whole slice into a shared-memory ring, so the HBM stream starts before any
-// arithmetic.  While the bytes are in flight, the CTA rotates and quantizes x
-// with the same core (and the same fp32 operation order) as the standalone
-// rotate+quantize kernel, so its codes are bit-identical to gbq_quantize_act.
-// Then each warp takes its share of the K columns of every staged weight row,
-// does 16-byte shared loads and int8 dp4a dot products against the quantized x,
-// the partial sums are reduced across lanes and warps, and the dequant epilogue
-// runs (fp32(acc) * x_scale, fmaf with the row scale and bias, bf16).
+// slice into a shared-memory ring, so the HBM stream starts before any
+// arithmetic.  Three kernels share that structure:
+//   gemv_direct_kernel  n = 64, K = 4096, up to 4 tokens: the register-streaming
+//                       variant, consecutive calls overlapping (described below);
+//   gemv_kernel         other square shapes, one or two tokens: while the bytes
+//                       are in flight the CTA rotates and quantizes x with the
+//                       same core (and fp32 operation order) as the standalone
+//                       rotate+quantize kernel, so its codes are bit-identical to
+//                       gbq_quantize_act;
+//   gemv_codes_kernel   up to 16 tokens, any descriptor: the codes and scales
+//                       come from the rotation kernels (launched before it).
+// The ring kernels' dot phase: each warp takes its share of the K columns of
+// every staged weight row, does 16-byte shared loads and int8 dp4a dot products
+// against the quantized x, the partial sums are reduced across lanes and warps,
+// and the dequant epilogue runs (fp32(acc) * x_scale, fmaf with the row scale
+// and bias, bf16).
 #include <algorithm>
 
 #include "gemm.h"

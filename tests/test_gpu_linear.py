@@ -132,7 +132,8 @@ def test_dequant_standalone_and_slice(ops):
     assert np.array_equal(bf16_np(yn), O.dequant(acc.astype(np.int64), xs, ws, None))
 
 
-# M <= 4 runs the decode GEMV (weight streaming) inside gbq_linear; linear_acc stays on the GEMM.
+# M <= 4 runs a decode GEMV (weight streaming) inside gbq_linear (the rotation inside for the square shapes
+# it covers, else the codes GEMV); linear_acc stays on the GEMM.
 DECODE_CASES = [(1, 4096, 4096, (64, 64, 1), False), (2, 1024, 520, (32, 32, 1), True),
                 (4, 256, 1000, (16, 16, 1), True), (3, 4096, 300, (16, 16, 16), False), (1, 4096, 7, (64, 64, 1), True),
                 (4, 4096, 1500, (64, 64, 1), True), (3, 8192, 333, (64, 64, 2), False),
