@@ -619,13 +619,20 @@ int launch_i8gemm(const I8GemmProblem &q, cudaStream_t st) {
                                 (uint64_t)q.ld_w, kBM, kBK, CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc) return rc;
     }
-    // Output through TMA when its row stride allows (16-byte multiple).
+    // Output through TMA when its row stride allows (16-byte multiple) and it lies in device memory; an
+    // output in pinned host memory (written straight over the chip-to-chip link) takes plain stores.
     {
         const uint32_t esz = q.epi == EPI_DEQUANT_BF16 ? 2u : 4u;
         const CUtensorMapDataType dt = q.epi == EPI_DEQUANT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                        : q.epi == EPI_ACC_I32    ? CU_TENSOR_MAP_DATA_TYPE_INT32
                                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-        p.use_tma_out = ((q.ld_out * esz) % 16 == 0 && ((uintptr_t)q.out & 15) == 0) ? 1 : 0;
+        bool out_device = false;
+        cudaPointerAttributes pa{};
+        if (cudaPointerGetAttributes(&pa, q.out) == cudaSuccess)
+            out_device = pa.type == cudaMemoryTypeDevice || pa.type == cudaMemoryTypeManaged;
+        else
+            (void)cudaGetLastError();  // an unknown pointer: plain stores
+        p.use_tma_out = (out_device && (q.ld_out * esz) % 16 == 0 && ((uintptr_t)q.out & 15) == 0) ? 1 : 0;
         if (p.use_tma_out) {
             rc = encode_tmap_2d(&p.tm_out, dt, q.out, (uint64_t)q.N, (uint64_t)q.M, (uint64_t)q.ld_out * esz, 32,
                                 kOutBlock / (32 * esz), CU_TENSOR_MAP_SWIZZLE_NONE);

@@ -186,16 +186,19 @@ int gbq_dequant(const int32_t *acc, int64_t ld_acc, const float *x_scale,
  * GEMV (weight streaming): with the rotation inside for a = b = 64, one group
  * (M <= 4, N <= 4864) and for a = b in {16, 32, 64} with M <= 2, K <= 4096;
  * else over codes the rotation kernels write into the workspace first (any
- * descriptor, while M * K codes and four weight rows fit
- * in shared memory; at N = 4096: K <= 44672 at M = 1, 27904 at M = 4, 11168
- * at M = 16);
- * larger M or K runs the GEMM (same values).  Workspace: GBQ_OP_LINEAR.
+ * descriptor, while M * K codes and four weight rows fit in shared memory; at
+ * N = 4096: K <= 44672 at M = 1, 27904 at M = 4, 11168 at M = 16); larger M
+ * or K runs the GEMM (same values).  Workspace: GBQ_OP_LINEAR.
  * At K = 4096 (a = b = 64, one group) the decode kernel is launched with
  * programmatic stream serialization: it may start while the kernel before it on
  * the stream is still running, but reads none of its inputs (x, w8, w_scale,
  * bias) before that kernel has completed, so x may be that kernel's output;
  * consecutive decode calls overlap (the next one's weight is fetched into L2
  * meanwhile).  Results do not depend on the overlap.
+ * y may also be pinned host memory (cudaHostAlloc / cudaHostRegister): the
+ * kernels then write it directly over the chip-to-chip link with plain
+ * stores (no TMA).  On GB300 that is slower than a device y followed by a
+ * copy, so it serves convenience, not speed.
  */
 int gbq_linear(const void *x, const int8_t *w8, const float *w_scale, const void *bias,
                void *y, int64_t M, int64_t N, int64_t K, gbq_rot rot, void *workspace,

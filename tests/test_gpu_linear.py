@@ -288,3 +288,23 @@ def test_binding_rejects_wrong_output_shape(ops):
     small = torch.empty(16, dtype=torch.uint8, device="cuda")
     with pytest.raises(Exception, match="workspace"):
         ops.linear(x, w8, s, None, (16, 16, 1), workspace=small)
+
+
+@pytest.mark.parametrize("M", [1, 8, 300])
+def test_linear_into_pinned_host_memory(ops, M):
+    """y in pinned host memory: the GEMM (plain stores instead of TMA) and the GEMVs write it directly; the
+    result equals the device-resident one bit for bit."""
+    from ffn_rotate_quantize_gb300 import _lib as L
+    K, N, rot = 4096, 520, (64, 64, 1)
+    c = I.linear_case(M, K, N, n_outliers=41, outlier_scale=30.0, bias_std=0.01, seed=500 + M)
+    w8, ws = O.prepare_weight(c["w"], rot)
+    x, bias = bf16_dev(c["x"]), bf16_dev(c["bias"])
+    w8d, wsd = d(w8), d(ws)
+    y_dev = ops.linear(x, w8d, wsd, bias, rot)
+    y_host = torch.zeros((M, N), dtype=torch.bfloat16).pin_memory()
+    work = torch.empty(ops.workspace_size(ops.OP_LINEAR, M, N, K), dtype=torch.uint8, device="cuda")
+    L.check(L.lib().gbq_linear(x.data_ptr(), w8d.data_ptr(), wsd.data_ptr(), bias.data_ptr(), y_host.data_ptr(),
+                               M, N, K, ops._rot(rot), work.data_ptr(), work.numel(),
+                               torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    assert torch.equal(y_host.view(torch.int16), y_dev.cpu().view(torch.int16))
