@@ -62,7 +62,7 @@ int launch_bf16_gemm_nn(const void *dy, const void *w, void *dx, int64_t M, int6
 int launch_bf16_gemm_tn(const void *x, const void *w, const void *bias, void *y, int64_t M, int64_t N, int64_t K,
                         unsigned int *status, int num_sms, cudaStream_t st);
 
-// Decode GEMV with the rotation inside (M <= 4; square n = 16, 32, 64 shapes, see launch_gemv):
+// Decode GEMV with the rotation inside (M <= 2, K <= 4096; square n = 16, 32, 64 shapes, see launch_gemv):
 // y[m][n] = dequant(sum_k q[m][k] w8[n][k]) from x rotated and quantized in the kernel.
 // Returns GBQ_ENOTSUP (nothing launched) for shapes it does not cover.
 int launch_gemv(const void *x, const int8_t *w8, const float *w_scale, const void *bias, void *y, int64_t M,

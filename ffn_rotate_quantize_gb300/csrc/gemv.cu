@@ -8,7 +8,7 @@
 // entry one thread issues bulk copies (cp.async.bulk, mbarrier-tracked) of the
 // slice into a shared-memory ring, so the HBM stream starts before any
 // arithmetic.  Three kernels share that structure:
-//   gemv_direct_kernel  n = 64, K = 4096, up to 4 tokens: the register-streaming
+//   gemv_direct_kernel  n = 64, K = 4096, one or two tokens: the register-streaming
 //                       variant, consecutive calls overlapping (described below);
 //   gemv_kernel         other square shapes, one or two tokens: while the bytes
 //                       are in flight the CTA rotates and quantizes x with the
@@ -982,15 +982,17 @@ int launch_gemv(const void *x, const int8_t *w8, const float *w_scale, const voi
     a.n_split = N;
     a.G = groups;
     a.status = status;
+    // Both kernels rotate every token in each CTA, one token after the other: past two tokens or K = 4096
+    // the rotation kernels plus gemv_codes_kernel are faster (measured: K = 8192 as 64x64x2, one token, 27
+    // vs 24 us; K = 4096 as 32x32x4, four tokens, 17.8 vs 15.1 us; K = 4096 as 64x64, three / four tokens,
+    // 11.4 / 13.6 vs 9.8 / 9.9 us), so those return GBQ_ENOTSUP.
+    if (M > 2 || K > 4096) return GBQ_ENOTSUP;
     switch (logn) {
-        // The ring kernel rotates every token in each CTA: past two tokens or K = 4096 the rotation
-        // kernels plus gemv_codes_kernel are faster (measured: K = 8192 as 64x64x2, one token, 27 vs
-        // 24 us; K = 4096 as 32x32x4, four tokens, 17.8 vs 15.1 us), so those return GBQ_ENOTSUP.
-        case 4: return M <= 2 && K <= 4096 ? launch_gemv_t<4>(a, num_sms, st) : GBQ_ENOTSUP;
-        case 5: return M <= 2 && K <= 4096 ? launch_gemv_t<5>(a, num_sms, st) : GBQ_ENOTSUP;
+        case 4: return launch_gemv_t<4>(a, num_sms, st);
+        case 5: return launch_gemv_t<5>(a, num_sms, st);
         case 6: {
             const int rc = launch_gemv_direct(a, num_sms, st);
-            return rc == GBQ_ENOTSUP && M <= 2 && K <= 4096 ? launch_gemv_t<6>(a, num_sms, st) : rc;
+            return rc == GBQ_ENOTSUP ? launch_gemv_t<6>(a, num_sms, st) : rc;
         }
         default: return GBQ_ENOTSUP;
     }

@@ -137,12 +137,12 @@ def test_dequant_standalone_and_slice(ops):
 DECODE_CASES = [(1, 4096, 4096, (64, 64, 1), False), (2, 1024, 520, (32, 32, 1), True),
                 (4, 256, 1000, (16, 16, 1), True), (3, 4096, 300, (16, 16, 16), False), (1, 4096, 7, (64, 64, 1), True),
                 (4, 4096, 1500, (64, 64, 1), True), (3, 8192, 333, (64, 64, 2), False),
-                # K = 4096 register-streaming kernel: three rows per warp with slice rows 16.. staged in shared
-                # memory (N = 3000: 20 rows per CTA); three tokens with staging and a ragged last slice
-                # (N = 4100: 27 rows per CTA, the last CTA 23); four tokens at 32 rows per CTA, where the staging
-                # does not fit two CTAs per SM and rows 2, 3 of every warp come through registers
+                # K = 4096 register-streaming kernel (one or two tokens): three rows per warp with slice rows
+                # 16.. staged in shared memory (N = 3000: 20 rows per CTA); 32 rows per CTA; three and four
+                # tokens (the codes GEMV) with a ragged last slice (N = 4100: 27 rows per CTA, the last CTA 23)
                 (2, 4096, 3000, (64, 64, 1), True), (3, 4096, 4100, (64, 64, 1), False),
                 (4, 4096, 4864, (64, 64, 1), True), (1, 4096, 4864, (64, 64, 1), True),
+                (2, 4096, 4864, (64, 64, 1), False),
                 # the ring kernel with the rotation inside (one or two tokens, K <= 4096): n = 16, n = 16 in
                 # sixteen groups, n = 64 past the register-streaming kernel's 32 rows per CTA
                 (1, 256, 1000, (16, 16, 1), True), (2, 4096, 300, (16, 16, 16), False),
