@@ -618,11 +618,19 @@ int gbq_linear(const void *x, const int8_t *w8, const float *w_scale, const void
     if (rc) return rc;
     INIT(d);
     cudaStream_t st = (cudaStream_t)stream;
-    // Decode and small batches: for M <= 4 the GEMV with the rotation inside for the square shapes it
-    // covers; otherwise, up to 16 tokens, the rotation kernels quantize x into the workspace and a GEMV
-    // streams the weight over those codes (the same codes, scales and epilogue as the GEMM route below).
+    // Decode and small batches: for one or two tokens a GEMV with the rotation inside (the square kernels'
+    // for the shapes they cover, else the generic rotation's); otherwise, up to 16 tokens, the rotation
+    // kernels quantize x into the workspace and a GEMV streams the weight over those codes.  Every route
+    // has the same codes, scales and epilogue as the GEMM route below.
     if (M <= 4 && rs.logn > 0) {
         rc = launch_gemv(x, w8, w_scale, bias, y, M, N, K, rs.logn, rs.groups, d->sms, st, d->status);
+        if (rc != GBQ_ENOTSUP) return rc;
+    }
+    // The generic rotation inside: faster than the rotation kernels + codes GEMV while a CTA rotates at
+    // most 8192 values (measured: K = 2048 as 32x64, one token, 5.8 vs 6.9 us; K = 8192 as 64x128, 21.3 vs
+    // 22.3 us, two tokens 27.9 vs 23.9 us; K = 16384 as 128x128, 48.9 vs 46.0 us).
+    if (M * K <= 8192 && rs.logn != 0 && gemv_gen_fits(M, N, K, d->sms)) {
+        rc = launch_gemv_gen(x, w8, w_scale, bias, y, M, N, K, rs.la, rs.lb, d->sms, st, d->status);
         if (rc != GBQ_ENOTSUP) return rc;
     }
     if (gemv_codes_fits(M, N, K, d->sms)) {

@@ -68,6 +68,13 @@ int launch_bf16_gemm_tn(const void *x, const void *w, const void *bias, void *y,
 int launch_gemv(const void *x, const int8_t *w8, const float *w_scale, const void *bias, void *y, int64_t M,
                 int64_t N, int64_t K, int logn, int groups, int num_sms, cudaStream_t st, unsigned int *status);
 
+// Decode GEMV with the generic rotation inside (M <= 2; any descriptor of two or more levels, K <= 49152
+// while the tile, the codes and four weight rows fit): the tokens are rotated with the generic rotation's
+// level list in every CTA.  GBQ_ENOTSUP (nothing launched) when it does not fit.
+bool gemv_gen_fits(int64_t M, int64_t N, int64_t K, int num_sms);
+int launch_gemv_gen(const void *x, const int8_t *w8, const float *w_scale, const void *bias, void *y, int64_t M,
+                    int64_t N, int64_t K, int la, int lb, int num_sms, cudaStream_t st, unsigned int *status);
+
 // GEMV (M <= 16) over tokens already quantized: codes int8 [M][K] and row scales fp32 [M] (e.g. in the
 // workspace), y[m * ld_y + n] = dequant(sum_k codes[m][k] w8[n][k]).  Launched with programmatic stream
 // serialization: it reads the codes and scales only after the preceding kernel completed, w8, w_scale and

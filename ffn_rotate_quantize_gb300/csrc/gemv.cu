@@ -15,6 +15,8 @@
 //                       same core (and fp32 operation order) as the standalone
 //                       rotate+quantize kernel, so its codes are bit-identical to
 //                       gbq_quantize_act;
+//   gemv_gen_kernel     one or two tokens, any descriptor: as gemv_kernel, with
+//                       the generic rotation's passes (rotate_g.cuh) inside;
 //   gemv_codes_kernel   up to 16 tokens, any descriptor: the codes and scales
 //                       come from the rotation kernels (launched before it).
 // The ring kernels' dot phase: each warp takes its share of the K columns of
@@ -26,6 +28,7 @@
 
 #include "gemm.h"
 #include "rotate_fast.cuh"
+#include "rotate_g.cuh"
 
 namespace gbq {
 namespace {
@@ -61,6 +64,7 @@ struct GemvArgs {
 
 constexpr int kGvWarps = kGvThreads / 32;
 constexpr int kGcMaxM = 16;  // tokens of the codes GEMV (the kernels that rotate in-kernel take kGvMaxM)
+constexpr int kGvGenMaxM = 2;  // tokens of the GEMV with the generic rotation inside
 
 // Tokens padded to a power of two; the dot phase keeps 32 / MP rows of a stage in flight per lane.
 __host__ __device__ constexpr int gv_pad_m(int64_t M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
@@ -236,7 +240,9 @@ __device__ __forceinline__ void gemv_dot_phase(const GemvArgs &p, uint8_t *stage
     switch (gv_pad_m(p.M)) {
         case 1: gemv_dot_phase_m<1>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep); break;
         case 2: gemv_dot_phase_m<2>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep); break;
-        case 4: gemv_dot_phase_m<4>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep); break;
+        case 4:
+            if constexpr (MAXM >= 4) gemv_dot_phase_m<4>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
+            break;
         default:
             if constexpr (MAXM > 4) {
                 if (gv_pad_m(p.M) == 8)
@@ -883,6 +889,98 @@ int launch_gemv_t(const GemvArgs &base, int num_sms, cudaStream_t st) {
     return e == cudaSuccess ? GBQ_OK : gbq_fail(GBQ_ECUDA, cudaGetErrorString(e));
 }
 
+// ---------------------------------------------------------------------------
+// Decode GEMV for the descriptors the square in-kernel rotations do not take (a != b, odd total log2,
+// small factors, many groups, K above 4096), one or two tokens: every CTA rotates and quantizes the
+// tokens itself with the generic rotation's passes (rotate_g.cuh: rotg_kernel's level list and fp32
+// operations, so the same codes and scales) while its first weight stages stream in.  Launched with
+// programmatic stream serialization: the weight copies and the epilogue operands are issued before
+// griddepcontrol.wait, x is read after it, and the next launch may start at entry.
+__global__ void __launch_bounds__(kGvThreads, 2) gemv_gen_kernel(GemvArgs p, gen::GenArgs g) {
+    static_assert(kGvThreads == gen::kGenThreads, "the generic passes stride over the CTA's threads");
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t *stages = smem;
+    int8_t *xq = reinterpret_cast<int8_t *>(smem + p.x_off);
+    float *xs_s = reinterpret_cast<float *>(smem + p.misc_off);      // [kGvMaxM] token scales
+    unsigned *rowmax = reinterpret_cast<unsigned *>(xs_s + kGvMaxM);  // [kGvMaxM]
+    uint64_t *full = reinterpret_cast<uint64_t *>(rowmax + kGvMaxM);
+    int *abort_flag = reinterpret_cast<int *>(full + kGvStages);
+    float *T = reinterpret_cast<float *>(smem + p.t_off);
+    float *ep = reinterpret_cast<float *>(smem + p.ep_off);
+
+    const int tid = threadIdx.x;
+    const int64_t r0 = (int64_t)blockIdx.x * p.rows_per_cta;
+    const int nrows = (int)(min(p.N, r0 + p.rows_per_cta) - r0);
+    // Debug builds: the CTA's weight slice (every weight copy below) lies inside W8.
+    if (!GBQ_IN_RANGE(p.status, r0 * p.K, (int64_t)nrows * p.K, p.N * p.K)) return;
+    const int nchunks = (nrows + p.rows_per_stage - 1) / p.rows_per_stage;
+    if (tid == 0) {
+        for (int s2 = 0; s2 < kGvStages; ++s2) mbar_init(&full[s2], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        for (int c = 0; c < nchunks && c < kGvStages; ++c) {
+            const int rows = min(p.rows_per_stage, nrows - c * p.rows_per_stage);
+            mbar_arrive_expect_tx(&full[c], (uint32_t)rows * (uint32_t)p.K);
+            gv_copy_rows(p, stages + (size_t)c * p.stage_bytes, r0 + (int64_t)c * p.rows_per_stage, rows, &full[c]);
+        }
+    }
+    if (tid < kGvMaxM) rowmax[tid] = 0u;
+    gv_load_epilogue(p, ep, r0, nrows);  // w_scale and bias: not written by the kernel before
+    pdl_allow_dependents();              // the next call may start and issue its weight copies
+    pdl_wait();                          // x may come from the kernel before
+
+    // ---- rotate + quantize the tokens (rotg_kernel's phases on one chunk of M rows) ----
+    const int K = g.K;
+    const int E = (int)p.M * K;
+    for (int u = tid; u < (E >> 3); u += kGvThreads) {
+        const int e = u * 8, row = e / K;
+        float x[8];
+        if (GBQ_IN_RANGE(p.status, row, 1, p.M) && GBQ_IN_RANGE(p.status, e - row * K, 8, K)) {
+            gen::gen_load8<IN_BF16>(g, row, e - row * K, x);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) x[k] = 0.0f;
+        }
+        float *t = T + gen::tix(e);  // eight values inside one 32-value block
+#pragma unroll
+        for (int k = 0; k < 8; ++k) t[k] = x[k];
+    }
+    __syncthreads();  // the tile is complete; rowmax and the barriers are initialised
+    for (int l = 0; l < g.nlev; l += 2) {
+        const bool pair = l + 1 < g.nlev;
+        const int w1 = g.wid[l], w2 = pair ? g.wid[l + 1] : 0;
+        const int p1 = g.pos[l], p2 = pair ? g.pos[l + 1] : 0;
+        if (l + 2 >= g.nlev)
+            gen::gen_pass_dispatch<true, OUT_S8>(w1, w2, T, E, p1, p2, g, rowmax);
+        else
+            gen::gen_pass_dispatch<false, OUT_S8>(w1, w2, T, E, p1, p2, g, rowmax);
+        __syncthreads();
+    }
+    if (tid < p.M) xs_s[tid] = __fdiv_rn(__uint_as_float(rowmax[tid]), 127.0f);
+    __syncthreads();
+    for (int u = tid; u < (E >> 4); u += kGvThreads) {  // 16 contiguous codes per thread
+        const int e = u * 16, row = e / K;
+        const float *t = T + gen::tix(e);
+        float2 v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = make_float2(t[k], t[k + 8]);
+        uint32_t words[2][2];
+        quant_codes<8>(v, xs_s[row], words);
+        *reinterpret_cast<uint4 *>(xq + e) = make_uint4(words[0][0], words[0][1], words[1][0], words[1][1]);
+    }
+    __syncthreads();  // the codes are complete
+
+    gemv_dot_phase<kGvGenMaxM>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
+    if (tid == 0 && *(volatile int *)abort_flag) {
+        // A wait gave up: let the copies issued at entry land (bounded) before the CTA leaves.
+        for (int c = 0; c < min(nchunks, kGvStages); ++c) {
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(&full[c], 0) && globaltimer() - t0 < kWaitLimitNs) {
+            }
+        }
+    }
+}
+
 }  // namespace
 
 // Shared memory of gemv_codes_kernel besides the weight ring: the codes, the scales and barriers, the
@@ -962,6 +1060,86 @@ int launch_gemv_codes(const int8_t *codes, const float *scales, const int8_t *w8
                       cudaStream_t st, unsigned int *status) {
     return launch_gemv_codes2(codes, scales, w8, w_scale, w8, w_scale, N, bias, y, ld_y, M, N, K, num_sms, st,
                               status);
+}
+
+// Shared memory of gemv_gen_kernel besides the weight ring: the codes, the misc block, the epilogue
+// operands, the fp32 rotation tile of the M token rows (one pad float per 32).
+size_t gemv_gen_fixed(int64_t M, int64_t N, int64_t K, int num_sms) {
+    const int64_t rpc = (N + num_sms - 1) / num_sms;
+    const size_t E = (size_t)M * K;
+    return ((E + 127) & ~(size_t)127) + 128 + gv_ep_bytes(rpc) + (((E + E / 32) * 4 + 127) & ~(size_t)127);
+}
+
+bool gemv_gen_fits(int64_t M, int64_t N, int64_t K, int num_sms) {
+    if (M < 1 || M > kGvGenMaxM || K < 16 || K % 16 != 0 || K > kGenMaxK || N < 1 || num_sms < 1) return false;
+    const size_t fixed = gemv_gen_fixed(M, N, K, num_sms);
+    return fixed < kGvSmem && (kGvSmem - fixed) / kGvStages >= (size_t)K + 127;  // one row per stage at least
+}
+
+int launch_gemv_gen(const void *x, const int8_t *w8, const float *w_scale, const void *bias, void *y, int64_t M,
+                    int64_t N, int64_t K, int la, int lb, int num_sms, cudaStream_t st, unsigned int *status) {
+    if (!gemv_gen_fits(M, N, K, num_sms) || la + lb < 1) return GBQ_ENOTSUP;
+    if (((uintptr_t)x | (uintptr_t)w8) & 15) return GBQ_ENOTSUP;
+    GemvArgs a{};
+    a.x = x;
+    a.w8 = w8;
+    a.ws = w_scale;
+    a.w8b = w8;
+    a.wsb = w_scale;
+    a.n_split = N;
+    a.bias = reinterpret_cast<const __nv_bfloat16 *>(bias);
+    a.y = reinterpret_cast<__nv_bfloat16 *>(y);
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.ld_y = N;
+    a.G = 1;
+    a.status = status;
+    gen::GenArgs g{};
+    g.in0 = x;
+    g.ld_in = K;
+    g.M = M;
+    g.K = (int)K;
+    g.R = (int)M;
+    g.status = status;
+    gen::gen_levels(la, lb, g);
+    const size_t fixed = gemv_gen_fixed(M, N, K, num_sms);
+    const int64_t rpc = (N + num_sms - 1) / num_sms;
+    const int64_t grid = (N + rpc - 1) / rpc;
+    const int64_t rps_cap = (int64_t)((kGvSmem - fixed) / kGvStages - 127) / K;
+    const int64_t rps_fit = (rpc + kGvStages - 1) / kGvStages;
+    const int64_t rps = std::min<int64_t>(std::min(rps_fit, rps_cap), 32 / gv_pad_m(M));
+    a.rows_per_cta = (int)rpc;
+    a.rows_per_stage = (int)rps;
+    a.stage_bytes = (uint32_t)(((size_t)rps * K + 127) & ~(size_t)127);
+    a.x_off = (uint32_t)((size_t)kGvStages * a.stage_bytes);
+    a.misc_off = a.x_off + (uint32_t)(((size_t)M * K + 127) & ~(size_t)127);
+    a.ep_off = a.misc_off + 128;  // token scales, row maxima, stage barriers, abort flag: < 128 bytes
+    a.t_off = a.ep_off + (uint32_t)gv_ep_bytes(rpc);
+    const size_t E = (size_t)M * K;
+    const size_t smem = a.t_off + (((E + E / 32) * 4 + 127) & ~(size_t)127);
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(gemv_gen_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGvSmem) !=
+            cudaSuccess)
+            return gbq_fail(GBQ_ECUDA, "gemv: cannot set shared memory size");
+        attr = true;
+    }
+    cudaLaunchAttribute lattr[1];
+    lattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    lattr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = st;
+    cfg.attrs = lattr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kGvThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    prof_begin(3, st);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_gen_kernel, a, g);
+    prof_end(st);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return e == cudaSuccess ? GBQ_OK : gbq_fail(GBQ_ECUDA, cudaGetErrorString(e));
 }
 
 int launch_gemv(const void *x, const int8_t *w8, const float *w_scale, const void *bias, void *y, int64_t M, int64_t N,

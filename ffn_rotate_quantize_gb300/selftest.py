@@ -98,8 +98,8 @@ def _layer(G, dev, M, K, N, rot, seed):
 
 
 def check_linear_routes(G, dev):
-    # the GEMM route, the decode GEMV with the rotation inside, the codes GEMV (a small batch, and one
-    # token with a non-square descriptor)
+    # the GEMM route, the decode GEMV with the rotation inside, the codes GEMV (a small batch) and the GEMV
+    # with the generic rotation inside (one token with a non-square descriptor)
     for M, K, rot in ((64, 4096, (64, 64, 1)), (1, 4096, (64, 64, 1)), (8, 4096, (64, 64, 1)),
                       (1, 2048, (32, 64, 1))):
         x, w8, s, bias = _layer(G, dev, M, K, 512, rot, seed=M + K)
@@ -110,7 +110,7 @@ def check_linear_routes(G, dev):
         if not _same_bits(y, G.linear_noalloc(x, w8, s, bias, rot)):
             return False, f"M={M} {rot}: linear_noalloc != linear"
     return True, ("linear == dequant(linear_acc) == linear_noalloc, bit for bit: GEMM (M = 64), decode GEMV "
-                  "(M = 1), codes GEMV (M = 8; M = 1 with 32 x 64)")
+                  "(M = 1), codes GEMV (M = 8), GEMV with the generic rotation inside (M = 1 with 32 x 64)")
 
 
 def check_ffn_chain(G, dev):

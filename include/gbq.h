@@ -184,10 +184,11 @@ int gbq_dequant(const int32_t *acc, int64_t ld_acc, const float *x_scale,
  * [..,N]); rotate+quantize, int8 GEMM and the dequant epilogue fused in the
  * GEMM.  Bit-identical to gbq_dequant(gbq_linear_acc(x)).  M = 1..16 runs a
  * GEMV (weight streaming): with the rotation inside for M <= 2 and a = b in
- * {16, 32, 64}, K <= 4096; else over codes the rotation kernels write into
- * the workspace first (any descriptor, while M * K codes and four weight rows
- * fit in shared memory; at N = 4096: K <= 44672 at M = 1, 27904 at M = 4,
- * 11168 at M = 16); larger M or K runs the GEMM (same values).  Workspace:
+ * {16, 32, 64}, K <= 4096, and for every other descriptor (not the identity)
+ * while M * K <= 8192; else over codes the rotation kernels write into the
+ * workspace first (any descriptor, while M * K codes and four weight rows fit
+ * in shared memory; at N = 4096: K <= 44672 at M = 1, 27904 at M = 4, 11168
+ * at M = 16); larger M or K runs the GEMM (same values).  Workspace:
  * GBQ_OP_LINEAR.
  * At K = 4096 (a = b = 64, one group) the decode kernel is launched with
  * programmatic stream serialization: it may start while the kernel before it on

@@ -125,8 +125,9 @@ def test_prepare_weight_any_descriptor(ops, rot):
     assert_int8_parity(w8.cpu().numpy(), w8r, (v / wsr[:, None]).astype(np.float32))
 
 
-# M <= 16 runs the GEMV over codes from the rotation kernels (for M <= 4 the square in-kernel rotations
-# do not cover these descriptors), larger M the GEMM; both give the same bits as dequant(linear_acc).
+# M <= 16 runs a GEMV: with the generic rotation inside for M K <= 8192, else over codes from the rotation
+# kernels (the square in-kernel rotations do not cover these descriptors); larger M the GEMM.  Every route
+# gives the same bits as dequant(linear_acc).
 # (16, 16, 128) is square but has too many groups for the in-kernel rotation of the decode GEMV; the
 # square (64, 64, 1) at M = 5, 8 and 16 takes the codes GEMV as a small batch.
 @pytest.mark.parametrize("M,K,N,rot", [(130, 2048, 392, (32, 64, 1)), (1, 2048, 512, (64, 32, 1)),
@@ -141,7 +142,12 @@ def test_prepare_weight_any_descriptor(ops, rot):
                                        # edges of the codes GEMV: fewer weight rows than warps or SMs, one
                                        # row per ring stage at K = 32768, and past its shared-memory limit
                                        (16, 64, 1, (8, 8, 1)), (3, 64, 5, (2, 32, 1)),
-                                       (2, 32768, 100, (128, 256, 1)), (4, 32768, 100, (128, 256, 1))])
+                                       (2, 32768, 100, (128, 256, 1)), (4, 32768, 100, (128, 256, 1)),
+                                       # the GEMV with the generic rotation inside (M K <= 8192): grouped,
+                                       # two tokens, the largest K, factor 2, odd log2, a tiny row
+                                       (1, 1024, 200, (8, 8, 16)), (2, 4096, 300, (32, 128, 1)),
+                                       (1, 8192, 152, (64, 128, 1)), (1, 4096, 100, (2, 2048, 1)),
+                                       (1, 512, 7, (2, 256, 1)), (1, 64, 1, (8, 8, 1))])
 def test_linear_any_descriptor(ops, M, K, N, rot):
     c = I.linear_case(M, K, N, n_outliers=max(1, K // 100), outlier_scale=30.0, bias_std=0.01, seed=M + K + N)
     w8, ws = O.prepare_weight(c["w"], rot)
