@@ -249,3 +249,22 @@ def test_activation_quantizers_any_descriptor(ops, rot):
     qr, sr = O.quantize(v)
     assert_scale_parity(h1.cpu().numpy(), sr)
     assert_int8_parity(q1.cpu().numpy(), qr, (v / np.where(sr > 0, sr, 1)[:, None]).astype(np.float32))
+
+
+@pytest.mark.parametrize("rot", [(32, 64, 1), (64, 64, 1), (64, 128, 1), (128, 128, 1), (16, 16, 16), (1, 1, 4096),
+                                 (8, 8, 16)])
+def test_linear_routes_agree_across_token_counts(ops, rot):
+    """Every token count from 1 to 17 -- the GEMVs with the rotation inside (square and generic), the codes
+    GEMV and the GEMM -- gives linear == dequant(linear_acc) bit for bit, with bias, on one weight."""
+    K = rot[0] * rot[1] * rot[2]
+    N = 136
+    c = I.linear_case(17, K, N, n_outliers=max(1, K // 100), outlier_scale=30.0, bias_std=0.01, seed=K + rot[0])
+    w8, ws = O.prepare_weight(c["w"], rot)
+    w8d, wsd, bias = d(w8), d(ws), bf16_dev(c["bias"])
+    for M in (1, 2, 3, 4, 5, 8, 15, 16, 17):
+        x = bf16_dev(c["x"][:M])
+        y = ops.linear(x, w8d, wsd, bias, rot)
+        acc, xs = ops.linear_acc(x, w8d, rot)
+        y2 = ops.dequant(acc, xs, wsd, bias)
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), y2.view(torch.int16)), (rot, M)
