@@ -54,6 +54,7 @@ struct GemvArgs {
     int G;
     int rows_per_cta;
     int rows_per_stage;
+    int nstages;            // ring kernels: stages in use (3 or kGvStages)
     uint32_t stage_bytes;   // rows_per_stage * K, multiple of 128
     uint32_t x_off, t_off, misc_off;
     uint32_t xb_off;        // bf16 staging of the M token rows (three-pass n = 64 path), else 0
@@ -134,9 +135,9 @@ __device__ __forceinline__ void gemv_dot_phase_t(const GemvArgs &p, uint8_t *sta
     auto issue = [&](int c) {
         const int rows = min(p.rows_per_stage, nrows - c * p.rows_per_stage);
         const uint32_t bytes = (uint32_t)rows * (uint32_t)p.K;
-        uint64_t *bar = &full[c % kGvStages];
+        uint64_t *bar = &full[c % p.nstages];
         mbar_arrive_expect_tx(bar, bytes);
-        gv_copy_rows(p, stages + (size_t)(c % kGvStages) * p.stage_bytes, r0 + (int64_t)c * p.rows_per_stage, rows,
+        gv_copy_rows(p, stages + (size_t)(c % p.nstages) * p.stage_bytes, r0 + (int64_t)c * p.rows_per_stage, rows,
                      bar);
     };
     const int kq = (int)(p.K / 16);
@@ -144,10 +145,10 @@ __device__ __forceinline__ void gemv_dot_phase_t(const GemvArgs &p, uint8_t *sta
     const int i0 = warp * cpw + lane, i1 = min(kq, (warp + 1) * cpw);
     const uint32_t xq_s = smem_u32(xq), kb = (uint32_t)p.K;
     for (int c = 0; c < nchunks; ++c) {
-        const bool ok = mbar_wait(&full[c % kGvStages], (uint32_t)((c / kGvStages) & 1), p.status, abort_flag);
+        const bool ok = mbar_wait(&full[c % p.nstages], (uint32_t)((c / p.nstages) & 1), p.status, abort_flag);
         if (!__syncthreads_and(ok)) break;  // every thread leaves together
         const int rows = min(p.rows_per_stage, nrows - c * p.rows_per_stage);
-        const uint32_t st_s = smem_u32(stages + (size_t)(c % kGvStages) * p.stage_bytes);
+        const uint32_t st_s = smem_u32(stages + (size_t)(c % p.nstages) * p.stage_bytes);
         int acc[NV];  // [row j][token m] at j * MP + m
 #pragma unroll
         for (int q = 0; q < NV; ++q) acc[q] = 0;
@@ -211,7 +212,7 @@ __device__ __forceinline__ void gemv_dot_phase_t(const GemvArgs &p, uint8_t *sta
                     p.y[(int64_t)m * p.ld_y + n] = __float2bfloat16_rn(__fmaf_rn(tv, ep_ws[jr], ep_b[jr]));
             }
         }
-        if (tid == 0 && c + kGvStages < nchunks) issue(c + kGvStages);
+        if (tid == 0 && c + p.nstages < nchunks) issue(c + p.nstages);
     }
 }
 
@@ -287,9 +288,9 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(GemvArgs p) {
     auto issue = [&](int c) {
         const int rows = min(p.rows_per_stage, nrows - c * p.rows_per_stage);
         const uint32_t bytes = (uint32_t)rows * (uint32_t)p.K;
-        uint64_t *bar = &full[c % kGvStages];
+        uint64_t *bar = &full[c % p.nstages];
         mbar_arrive_expect_tx(bar, bytes);
-        gv_copy_rows(p, stages + (size_t)(c % kGvStages) * p.stage_bytes, r0 + (int64_t)c * p.rows_per_stage, rows,
+        gv_copy_rows(p, stages + (size_t)(c % p.nstages) * p.stage_bytes, r0 + (int64_t)c * p.rows_per_stage, rows,
                      bar);
     };
     const bool fast_x = (LOGN == 6 && p.G == 1);
@@ -302,21 +303,21 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(GemvArgs p) {
             fence_mbar_init();
             mbar_arrive_expect_tx(xfull, (uint32_t)(p.M * p.K * 2));
             bulk_g2s(smem + p.xb_off, p.x, (uint32_t)(p.M * p.K * 2), xfull);
-            for (int c = 0; c < nchunks && c < kGvStages; ++c) {
+            for (int c = 0; c < nchunks && c < p.nstages; ++c) {
                 const int rows = min(p.rows_per_stage, nrows - c * p.rows_per_stage);
                 mbar_arrive_expect_tx(&full[c], (uint32_t)rows * (uint32_t)p.K);
             }
         }
         __syncthreads();
         if (lane == 0)
-            for (int c = 0; c < nchunks && c < kGvStages; ++c) {
+            for (int c = 0; c < nchunks && c < p.nstages; ++c) {
                 const int rows = min(p.rows_per_stage, nrows - c * p.rows_per_stage);
                 for (int j = warp; j < rows; j += kGvThreads / 32)
                     gv_copy_rows(p, stages + (size_t)c * p.stage_bytes + (size_t)j * p.K,
                                  r0 + (int64_t)c * p.rows_per_stage + j, 1, &full[c]);
             }
     } else if (tid == 0) {
-        for (int c = 0; c < nchunks && c < kGvStages; ++c) issue(c);
+        for (int c = 0; c < nchunks && c < p.nstages; ++c) issue(c);
     }
     float *ep = reinterpret_cast<float *>(smem + p.ep_off);
     gv_load_epilogue(p, ep, r0, nrows);
@@ -354,8 +355,8 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(GemvArgs p) {
             gemv_dot_phase<kGvMaxM>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
             if (tid == 0 && *(volatile int *)abort_flag) {
                 // A wait gave up: let the copies issued at entry land (bounded) before the CTA leaves.
-                for (int c = 0; c <= min(nchunks, kGvStages); ++c) {
-                    uint64_t *b = c < min(nchunks, kGvStages) ? &full[c] : xfull;
+                for (int c = 0; c <= min(nchunks, p.nstages); ++c) {
+                    uint64_t *b = c < min(nchunks, p.nstages) ? &full[c] : xfull;
                     const uint64_t t0 = globaltimer();
                     while (!mbar_try_wait(b, 0) && globaltimer() - t0 < kWaitLimitNs) {
                     }
@@ -427,7 +428,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_codes_kernel(GemvArgs p, c
         mbar_init(xfull, 1);
         *abort_flag = 0;
         fence_mbar_init();
-        for (int c = 0; c < nchunks && c < kGvStages; ++c) {
+        for (int c = 0; c < nchunks && c < p.nstages; ++c) {
             const int rows = min(p.rows_per_stage, nrows - c * p.rows_per_stage);
             const uint32_t bytes = (uint32_t)rows * (uint32_t)p.K;
             mbar_arrive_expect_tx(&full[c], bytes);
@@ -447,8 +448,8 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_codes_kernel(GemvArgs p, c
     if (__syncthreads_and(xok)) gemv_dot_phase<kGcMaxM>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
     if (tid == 0 && *(volatile int *)abort_flag) {
         // A wait gave up: let the copies issued at entry land (bounded) before the CTA leaves.
-        for (int c = 0; c <= min(nchunks, kGvStages); ++c) {
-            uint64_t *b = c < min(nchunks, kGvStages) ? &full[c] : xfull;
+        for (int c = 0; c <= min(nchunks, p.nstages); ++c) {
+            uint64_t *b = c < min(nchunks, p.nstages) ? &full[c] : xfull;
             const uint64_t t0 = globaltimer();
             while (!mbar_try_wait(b, 0) && globaltimer() - t0 < kWaitLimitNs) {
             }
@@ -843,6 +844,31 @@ int launch_gemv_direct(const GemvArgs &base, int num_sms, cudaStream_t st) {
     return e == cudaSuccess ? GBQ_OK : gbq_fail(GBQ_ECUDA, cudaGetErrorString(e));
 }
 
+// Ring of a slice of rpc weight rows of K bytes beside `fixed` bytes of other shared memory: the number of
+// stages (kGvStages or 3) and rows per stage (at most 32 / MP for MP padded tokens), taking the plan with
+// fewer chunks -- each chunk costs ~1.8 K cycles of reduction, barriers and waits beside its dot products
+// (per-stage timestamps), so few large stages beat many small ones once both keep >= 3 stages in flight.
+// Sets nstages, rows_per_cta, rows_per_stage and stage_bytes; false when not one row fits per stage.
+bool gv_plan_ring(GemvArgs &a, int64_t rpc, int64_t K, size_t fixed, int mp) {
+    if (fixed >= kGvSmem) return false;
+    int64_t best_chunks = 0;
+    for (int S = kGvStages; S >= 3; --S) {
+        const int64_t per = (int64_t)((kGvSmem - fixed) / S) - 127;  // a stage is rounded up to 128 bytes
+        const int64_t cap = per > 0 ? per / K : 0;
+        if (cap < 1) continue;
+        const int64_t rps = std::min<int64_t>(std::min<int64_t>((rpc + S - 1) / S, cap), 32 / mp);
+        const int64_t chunks = (rpc + rps - 1) / rps;
+        if (best_chunks == 0 || chunks < best_chunks) {
+            best_chunks = chunks;
+            a.nstages = S;
+            a.rows_per_stage = (int)rps;
+            a.stage_bytes = (uint32_t)(((size_t)rps * K + 127) & ~(size_t)127);
+        }
+    }
+    a.rows_per_cta = (int)rpc;
+    return best_chunks > 0;
+}
+
 template <int LOGN>
 int launch_gemv_t(const GemvArgs &base, int num_sms, cudaStream_t st) {
     constexpr int TPG = RotGeom<LOGN>::TPG;
@@ -857,15 +883,8 @@ int launch_gemv_t(const GemvArgs &base, int num_sms, cudaStream_t st) {
     const size_t fixed = ((x_bytes + 127) & ~(size_t)127) + ((t_bytes + 127) & ~(size_t)127) + 128 + xb_bytes +
                          gv_ep_bytes(rpc);
     if (fixed + (size_t)kGvStages * a.K > kGvSmem) return GBQ_ENOTSUP;
-    const int64_t rps_cap = (int64_t)((kGvSmem - fixed) / kGvStages) / a.K;
-    // Rows per stage: the whole slice over the ring when it fits (no more shared memory than needed),
-    // else as many as fit.
-    const int64_t rps_fit = (rpc + kGvStages - 1) / kGvStages;
-    const int64_t rps = std::min<int64_t>(std::min(rps_fit, rps_cap), 32 / gv_pad_m(a.M));
-    a.rows_per_cta = (int)rpc;
-    a.rows_per_stage = (int)rps;
-    a.stage_bytes = (uint32_t)(((size_t)rps * a.K + 127) & ~(size_t)127);
-    a.x_off = (uint32_t)((size_t)kGvStages * a.stage_bytes);
+    if (!gv_plan_ring(a, rpc, a.K, fixed, gv_pad_m(a.M))) return GBQ_ENOTSUP;
+    a.x_off = (uint32_t)((size_t)a.nstages * a.stage_bytes);
     a.t_off = a.x_off + (uint32_t)((x_bytes + 127) & ~(size_t)127);
     a.misc_off = a.t_off + (uint32_t)((t_bytes + 127) & ~(size_t)127);
     a.xb_off = 0;
@@ -918,7 +937,7 @@ __global__ void __launch_bounds__(kGvThreads, 2) gemv_gen_kernel(GemvArgs p, gen
         for (int s2 = 0; s2 < kGvStages; ++s2) mbar_init(&full[s2], 1);
         *abort_flag = 0;
         fence_mbar_init();
-        for (int c = 0; c < nchunks && c < kGvStages; ++c) {
+        for (int c = 0; c < nchunks && c < p.nstages; ++c) {
             const int rows = min(p.rows_per_stage, nrows - c * p.rows_per_stage);
             mbar_arrive_expect_tx(&full[c], (uint32_t)rows * (uint32_t)p.K);
             gv_copy_rows(p, stages + (size_t)c * p.stage_bytes, r0 + (int64_t)c * p.rows_per_stage, rows, &full[c]);
@@ -973,7 +992,7 @@ __global__ void __launch_bounds__(kGvThreads, 2) gemv_gen_kernel(GemvArgs p, gen
     gemv_dot_phase<kGvGenMaxM>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
     if (tid == 0 && *(volatile int *)abort_flag) {
         // A wait gave up: let the copies issued at entry land (bounded) before the CTA leaves.
-        for (int c = 0; c < min(nchunks, kGvStages); ++c) {
+        for (int c = 0; c < min(nchunks, p.nstages); ++c) {
             const uint64_t t0 = globaltimer();
             while (!mbar_try_wait(&full[c], 0) && globaltimer() - t0 < kWaitLimitNs) {
             }
@@ -1020,14 +1039,8 @@ int launch_gemv_codes2(const int8_t *codes, const float *scales, const int8_t *w
     const size_t fixed = gemv_codes_fixed(M, N, K, num_sms);
     const int64_t rpc = (N + num_sms - 1) / num_sms;
     const int64_t grid = (N + rpc - 1) / rpc;
-    // A stage is rows_per_stage weight rows rounded up to 128 bytes (K is a multiple of 16 only).
-    const int64_t rps_cap = (int64_t)((kGvSmem - fixed) / kGvStages - 127) / K;
-    const int64_t rps_fit = (rpc + kGvStages - 1) / kGvStages;
-    const int64_t rps = std::min<int64_t>(std::min(rps_fit, rps_cap), 32 / gv_pad_m(M));
-    a.rows_per_cta = (int)rpc;
-    a.rows_per_stage = (int)rps;
-    a.stage_bytes = (uint32_t)(((size_t)rps * K + 127) & ~(size_t)127);
-    a.x_off = (uint32_t)((size_t)kGvStages * a.stage_bytes);
+    if (!gv_plan_ring(a, rpc, K, fixed, gv_pad_m(M))) return GBQ_ENOTSUP;
+    a.x_off = (uint32_t)((size_t)a.nstages * a.stage_bytes);
     a.misc_off = a.x_off + (uint32_t)((x_bytes + 127) & ~(size_t)127);
     a.ep_off = a.misc_off + 128;  // scales, barriers, abort flag, codes barrier: < 128 bytes
     const size_t smem = a.ep_off + gv_ep_bytes(rpc);
@@ -1106,13 +1119,8 @@ int launch_gemv_gen(const void *x, const int8_t *w8, const float *w_scale, const
     const size_t fixed = gemv_gen_fixed(M, N, K, num_sms);
     const int64_t rpc = (N + num_sms - 1) / num_sms;
     const int64_t grid = (N + rpc - 1) / rpc;
-    const int64_t rps_cap = (int64_t)((kGvSmem - fixed) / kGvStages - 127) / K;
-    const int64_t rps_fit = (rpc + kGvStages - 1) / kGvStages;
-    const int64_t rps = std::min<int64_t>(std::min(rps_fit, rps_cap), 32 / gv_pad_m(M));
-    a.rows_per_cta = (int)rpc;
-    a.rows_per_stage = (int)rps;
-    a.stage_bytes = (uint32_t)(((size_t)rps * K + 127) & ~(size_t)127);
-    a.x_off = (uint32_t)((size_t)kGvStages * a.stage_bytes);
+    if (!gv_plan_ring(a, rpc, K, fixed, gv_pad_m(M))) return GBQ_ENOTSUP;
+    a.x_off = (uint32_t)((size_t)a.nstages * a.stage_bytes);
     a.misc_off = a.x_off + (uint32_t)(((size_t)M * K + 127) & ~(size_t)127);
     a.ep_off = a.misc_off + 128;  // token scales, row maxima, stage barriers, abort flag: < 128 bytes
     a.t_off = a.ep_off + (uint32_t)gv_ep_bytes(rpc);
