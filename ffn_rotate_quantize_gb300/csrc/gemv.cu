@@ -952,7 +952,7 @@ __global__ void __launch_bounds__(kGvThreads, 2) gemv_gen_kernel(GemvArgs p, gen
     const int K = g.K;
     const int E = (int)p.M * K;
     for (int u = tid; u < (E >> 3); u += kGvThreads) {
-        const int e = u * 8, row = e / K;
+        const int e = u * 8, row = gen::gen_row(g, e);
         float x[8];
         if (GBQ_IN_RANGE(p.status, row, 1, p.M) && GBQ_IN_RANGE(p.status, e - row * K, 8, K)) {
             gen::gen_load8<IN_BF16>(g, row, e - row * K, x);
@@ -978,7 +978,7 @@ __global__ void __launch_bounds__(kGvThreads, 2) gemv_gen_kernel(GemvArgs p, gen
     if (tid < p.M) xs_s[tid] = __fdiv_rn(__uint_as_float(rowmax[tid]), 127.0f);
     __syncthreads();
     for (int u = tid; u < (E >> 4); u += kGvThreads) {  // 16 contiguous codes per thread
-        const int e = u * 16, row = e / K;
+        const int e = u * 16, row = gen::gen_row(g, e);
         const float *t = T + gen::tix(e);
         float2 v[8];
 #pragma unroll
@@ -1085,6 +1085,7 @@ size_t gemv_gen_fixed(int64_t M, int64_t N, int64_t K, int num_sms) {
 
 bool gemv_gen_fits(int64_t M, int64_t N, int64_t K, int num_sms) {
     if (M < 1 || M > kGvGenMaxM || K < 16 || K % 16 != 0 || K > kGenMaxK || N < 1 || num_sms < 1) return false;
+    if ((uint64_t)M * (uint64_t)K * (uint64_t)K >= ((uint64_t)1 << 32)) return false;  // gen::gen_row's range
     const size_t fixed = gemv_gen_fixed(M, N, K, num_sms);
     return fixed < kGvSmem && (kGvSmem - fixed) / kGvStages >= (size_t)K + 127;  // one row per stage at least
 }
@@ -1112,7 +1113,7 @@ int launch_gemv_gen(const void *x, const int8_t *w8, const float *w_scale, const
     g.in0 = x;
     g.ld_in = K;
     g.M = M;
-    g.K = (int)K;
+    gen::gen_set_k(g, (int)K);
     g.R = (int)M;
     g.status = status;
     gen::gen_levels(la, lb, g);

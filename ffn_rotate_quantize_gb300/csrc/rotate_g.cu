@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kGenThreads, 3) rotg_kernel(const __grid_const
             for (int j = 0; j < 2; ++j) {
                 const int u = u0 + j * kGenThreads;
                 if (u < E8) {
-                    const int e = u * 8, row = e / K;
+                    const int e = u * 8, row = gen_row(p, e);
                     if (GBQ_IN_RANGE(p.status, r0 + row, 1, p.M) && GBQ_IN_RANGE(p.status, e - row * K, 8, K)) {
                         gen_load8<IN>(p, r0 + row, e - row * K, x[j]);
                     } else {
@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kGenThreads, 3) rotg_kernel(const __grid_const
                     float m = 0.0f;
 #pragma unroll
                     for (int k = 0; k < 16; ++k) m = fmaxf(m, fabsf(t[k]));
-                    const int row = (u * 16) / K;
+                    const int row = gen_row(p, u * 16);
                     const unsigned act = __activemask();
                     const int row0 = __shfl_sync(act, row, __ffs(act) - 1);
                     if (act == 0xffffffffu && __all_sync(act, row == row0)) {
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kGenThreads, 3) rotg_kernel(const __grid_const
 
         // ---- store phase: 16 contiguous values per thread
         for (int u = tid; u < (E >> 4); u += kGenThreads) {
-            const int e = u * 16, row = e / K;
+            const int e = u * 16, row = gen_row(p, e);
             const float *t = T + tix(e);
             float2 v[8];
 #pragma unroll
@@ -245,12 +245,13 @@ cudaError_t launch_rotg(int in_kind, int out_kind, const RotArgs &a, int la, int
     g.out_scale = a.out_scale;
     g.status = a.status;
     g.M = a.M;
-    g.K = (int)a.K;
+    gen_set_k(g, (int)a.K);
     int R = kGenTargetElems / g.K;
     if (R < 1) R = 1;
     if (R > kGenMaxRows) R = kGenMaxRows;
     if ((int64_t)R > a.M) R = (int)a.M;
     g.R = R;
+    if ((uint64_t)R * (uint64_t)g.K * (uint64_t)g.K >= ((uint64_t)1 << 32)) return cudaErrorNotSupported;  // gen_row
     if (la == 0 && lb == 0) {
         g.nlev = 0;
         g.post = 1.0f;

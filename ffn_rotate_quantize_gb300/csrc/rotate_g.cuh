@@ -32,6 +32,7 @@ struct GenArgs {
     float *out_scale;
     int64_t M;
     int K;       // row length (a multiple of 16)
+    uint32_t kdiv;  // ceil(2^32 / K) (gen_set_k): the row of chunk index e is umulhi(e, kdiv)
     int R;       // rows per chunk
     int nlev;    // levels in application order
     uint8_t pos[kGenMaxLevels];
@@ -43,6 +44,16 @@ struct GenArgs {
 };
 
 __device__ __forceinline__ int tix(int e) { return e + (e >> 5); }  // padded tile index
+
+// Row length and its reciprocal multiplier.  With kdiv = ceil(2^32 / K) = (2^32 + r) / K, 0 <= r < K,
+// e * kdiv / 2^32 = e / K + e r / (K 2^32), whose integer part is floor(e / K) whenever e r < 2^32;
+// r < K, so every chunk index e < 2^32 / K qualifies (chunks hold at most max(8192, K) values and
+// K <= kGenMaxK, so e K < 2^32 always).  One multiply-high replaces an integer division.
+inline void gen_set_k(GenArgs &g, int K) {
+    g.K = K;
+    g.kdiv = (uint32_t)((((uint64_t)1 << 32) + (uint64_t)K - 1) / (uint64_t)K);
+}
+__device__ __forceinline__ int gen_row(const GenArgs &p, int e) { return (int)__umulhi((unsigned)e, p.kdiv); }
 
 // ---- phase 0: eight contiguous input values (col a multiple of 8) as fp32, with the arithmetic
 // of the square kernels' loaders (load_in / staged_pair).
@@ -199,7 +210,7 @@ __device__ __forceinline__ void gen_pass(float *T, int E, int p1, int p2, const 
 #pragma unroll
                 for (int r = 0; r < NV; ++r) m = fmaxf(m, fabsf(v[r]));
                 // One atomic per warp when the warp's items lie in one row (wide rows), else one per item.
-                const int row = base / p.K;
+                const int row = gen_row(p, base);
                 const unsigned act = __activemask();
                 const int row0 = __shfl_sync(act, row, __ffs(act) - 1);
                 if (act == 0xffffffffu && __all_sync(act, row == row0)) {
