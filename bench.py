@@ -432,7 +432,7 @@ def run_ours(args):
             "ffn_decode_1x4096x16384": {
                 "ms": round(ffn_ms, 4), "achieved": round(ffn_bytes / (ffn_ms * 1e-3) * 1e-9, 1), "unit": "GB/s",
                 "frac": round(ffn_bytes / (ffn_ms * 1e-3) * 1e-9 / peaks["hbm"], 4),
-                "route": "x codes -> gate GEMV, up GEMV -> SiLU-GLU + H128(x)H128 codes -> down GEMV"},
+                "route": "x codes -> one gate|up GEMV over [W_gate; W_up] -> SiLU-GLU + H128(x)H128 codes -> down GEMV"},
             "linear_8x4096x4096": {
                 "ms": round(lin8_ms, 4), "achieved": round(lin8_bytes / (lin8_ms * 1e-3) * 1e-9, 1),
                 "unit": "GB/s", "frac": round(lin8_bytes / (lin8_ms * 1e-3) * 1e-9 / peaks["hbm"], 4),
