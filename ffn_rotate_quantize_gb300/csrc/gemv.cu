@@ -7,7 +7,7 @@
 // Design: one CTA per SM, each owning a contiguous slice of weight rows.  At
 // entry one thread issues bulk copies (cp.async.bulk, mbarrier-tracked) of the
 // slice into a shared-memory ring, so the HBM stream starts before any
-// arithmetic.  Three kernels share that structure:
+// arithmetic.  Four kernels share that structure:
 //   gemv_direct_kernel  n = 64, K = 4096, one or two tokens: the register-streaming
 //                       variant, consecutive calls overlapping (described below);
 //   gemv_kernel         other square shapes, one or two tokens: while the bytes
