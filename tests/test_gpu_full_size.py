@@ -65,6 +65,11 @@ def test_prefill_full_size_sampled(ops):
     # and the whole chain from x against the oracle's
     same = np.all(qg == q_r, axis=1)
     assert_rows_explained(y[rows], O.linear(c["x"][rows], w8, s, c["bias"], rot), same)
+    # the few-token routes on this weight (ring GEMV with the rotation inside for one or two tokens, the
+    # rotation kernel + codes GEMV up to 16): per row the same codes, sums and epilogue as the GEMM route
+    for m in (1, 2, 7, 16):
+        ym = bf16_np(ops.linear(x[:m], w8_d, s_d, bf16_dev(c["bias"]), rot))
+        assert np.array_equal(ym.view(np.uint16), y[:m].view(np.uint16)), f"{m}-token route != GEMM route"
 
 
 def test_ffn_full_size_sampled(ops):
@@ -95,6 +100,11 @@ def test_ffn_full_size_sampled(ops):
     assert_int8_parity(qh[same_x], mid["qh"][same_x], what="qh")
     same = same_x & np.all(qh == mid["qh"], axis=1)
     assert_rows_explained(bf16_np(y)[rows], y_r, same)
+    # the few-token route (int8 codes, gate|up GEMV over [W_gate; W_up], hidden codes, down GEMV) at the
+    # same sizes: per row the same codes, sums and epilogues, so the rows of the GEMM route's output
+    for m in (1, 2, 5):
+        ym = ops.ffn_fused(x[:m], wg8, sg, wu8, su, wd8, sd, rd, rh)
+        assert torch.equal(ym.view(torch.int16), y[:m].view(torch.int16)), f"{m}-token FFN != GEMM route"
 
 
 def test_backward_full_size_sampled(ops):
