@@ -67,16 +67,19 @@ constexpr int kGvWarps = kGvThreads / 32;
 constexpr int kGcMaxM = 16;  // tokens of the codes GEMV (the kernels that rotate in-kernel take kGvMaxM)
 constexpr int kGvGenMaxM = 2;  // tokens of the GEMV with the generic rotation inside
 
-// Tokens padded to a power of two; the dot phase keeps 32 / MP rows of a stage in flight per lane.
+// Tokens padded to a power of two; the dot phase keeps up to NV / MP rows of a stage in flight per lane
+// (NV partial sums per lane: kGvNV for the kernels that rotate in-kernel, kGcNV for the codes GEMV).
 __host__ __device__ constexpr int gv_pad_m(int64_t M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
+constexpr int kGvNV = 32;
+constexpr int kGcNV = 64;
 // The ring kernels' misc block (token scales, amax slots, stage barriers, abort flag, token barrier)
 // fits in the 128 bytes before the epilogue operands.
 static_assert(2 * kGvMaxM * 4 + (kGvStages + 2) * 8 + 16 <= 128, "misc block exceeds 128 bytes");
 
 // Shared memory of the ring kernels' epilogue operands: w_scale and bias (as fp32) of the CTA's rows,
-// then the warps' partial sums of one stage (32 per warp).
-__host__ __device__ constexpr size_t gv_ep_bytes(int64_t rows_per_cta) {
-    return ((size_t)rows_per_cta * 8 + kGvWarps * 32 * 4 + 127) & ~(size_t)127;
+// then the warps' partial sums of two consecutive stages (nv per warp and stage).
+__host__ __device__ constexpr size_t gv_ep_bytes(int64_t rows_per_cta, int nv) {
+    return ((size_t)rows_per_cta * 8 + 2 * kGvWarps * (size_t)nv * 4 + 127) & ~(size_t)127;
 }
 
 // The slice's w_scale and bias into shared memory (read before the dot products need them; the first
@@ -114,24 +117,29 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
 // stride K) and the dequant epilogue; every thread of the CTA takes part.  Warp w
 // owns the same 1/8 of the K columns (16-byte groups) in every stage: per group it
 // reads the tokens' codes once and the group of each of the stage's rows (at most
-// 32 / MP rows, MP = the token count padded to a power of two), so each weight
+// PS / MP rows, MP = the token count padded to a power of two), so each weight
 // byte is read from shared memory once, with independent dp4a chains per row and
-// token.  A transposing shuffle reduction leaves lane l of every warp with the
-// warp's sum for row l / MP and token l % MP; the eight warps' partial sums are
-// added after the stage's barrier (exact integers: the order does not matter).
-// w_scale and bias come from shared memory (gv_load_epilogue).
-template <int MP, int RB>  // tokens and rows per stage, each padded to a power of two (>= p.M, rows_per_stage)
+// token.  A transposing shuffle reduction leaves every lane of every warp with
+// NV / 32 of the warp's sums (NV >= 32) or every NV-th lane group with one; the
+// eight warps' partial sums are added after the stage's barrier (exact integers:
+// the order does not matter) by NV threads, which run the epilogue while the other
+// warps go on with the next stage.  One CTA barrier per stage: it also carries the
+// vote on the stage wait, and the partial sums alternate between two buffers, so a
+// stage's sums are never overwritten before its epilogue has read them.  w_scale
+// and bias come from shared memory (gv_load_epilogue).
+template <int MP, int RB, int PS>  // tokens and rows per stage padded to powers of two; PS >= MP * RB slots
 __device__ __forceinline__ void gemv_dot_phase_t(const GemvArgs &p, uint8_t *stages, const int8_t *xq,
                                                  const float *xs_s, uint64_t *full, int *abort_flag, int64_t r0,
                                                  int nrows, int nchunks, float *ep) {
-    constexpr int NV = MP * RB;  // partial sums per lane, a power of two <= 32
-    static_assert(NV >= 2 && NV <= 32, "2..32 partial sums per lane");
-    constexpr int LANES_PER_V = 32 / NV;  // lanes that end up holding one value's total
+    constexpr int NV = MP * RB;  // partial sums per lane before the reduction
+    static_assert(NV >= 2 && NV <= PS && PS <= 64, "2..64 partial sums per lane");
+    constexpr int VPL = NV > 32 ? NV / 32 : 1;            // sums a lane holds after the transposing levels
+    constexpr int LANES_PER_V = NV < 32 ? 32 / NV : 1;     // lanes that end up holding one value's total
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const float *ep_ws = ep;
     const float *ep_b = ep + p.rows_per_cta;
-    int *part = reinterpret_cast<int *>(ep + 2 * p.rows_per_cta);  // [kGvWarps][32]
+    int *part_base = reinterpret_cast<int *>(ep + 2 * p.rows_per_cta);  // [2][kGvWarps][PS]
     auto issue = [&](int c) {
         const int rows = min(p.rows_per_stage, nrows - c * p.rows_per_stage);
         const uint32_t bytes = (uint32_t)rows * (uint32_t)p.K;
@@ -146,13 +154,12 @@ __device__ __forceinline__ void gemv_dot_phase_t(const GemvArgs &p, uint8_t *sta
     const uint32_t xq_s = smem_u32(xq), kb = (uint32_t)p.K;
     for (int c = 0; c < nchunks; ++c) {
         const bool ok = mbar_wait(&full[c % p.nstages], (uint32_t)((c / p.nstages) & 1), p.status, abort_flag);
-        if (!__syncthreads_and(ok)) break;  // every thread leaves together
         const int rows = min(p.rows_per_stage, nrows - c * p.rows_per_stage);
         const uint32_t st_s = smem_u32(stages + (size_t)(c % p.nstages) * p.stage_bytes);
         int acc[NV];  // [row j][token m] at j * MP + m
 #pragma unroll
         for (int q = 0; q < NV; ++q) acc[q] = 0;
-        for (int i = i0; i < i1; i += 32) {
+        for (int i = ok ? i0 : i1; i < i1; i += 32) {  // a stage whose wait gave up is not read
             uint4 xv[MP];
 #pragma unroll
             for (int m = 0; m < MP; ++m)
@@ -182,11 +189,11 @@ __device__ __forceinline__ void gemv_dot_phase_t(const GemvArgs &p, uint8_t *sta
             }
         }
         // Transposing reduction over the lanes: at each level (lane bits 4, 3, ...) a lane keeps the half
-        // of its values selected by its lane bit and adds the partner's copy of that half; once one value
-        // is left, plain butterflies over the remaining lane bits.  Lane l ends with the total of value
-        // l / LANES_PER_V.
+        // of its values selected by its lane bit and adds the partner's copy of that half, until VPL values
+        // are left (lane l then holds values VPL l .. VPL l + VPL - 1); below 32 values, plain butterflies
+        // over the remaining lane bits, after which lane l holds the total of value l / LANES_PER_V.
 #pragma unroll
-        for (int o = 16, n = NV; n > 1; o >>= 1, n >>= 1) {
+        for (int o = 16, n = NV; n > VPL; o >>= 1, n >>= 1) {
             const bool up = (lane & o) != 0;
 #pragma unroll
             for (int q = 0; q < n / 2; ++q) {
@@ -197,14 +204,20 @@ __device__ __forceinline__ void gemv_dot_phase_t(const GemvArgs &p, uint8_t *sta
         }
 #pragma unroll
         for (int o = LANES_PER_V / 2; o >= 1; o >>= 1) acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], o);
-        if (lane % LANES_PER_V == 0) part[warp * 32 + lane / LANES_PER_V] = acc[0];
-        __syncthreads();
+        int *part = part_base + (c & 1) * (kGvWarps * PS);
+        if constexpr (VPL > 1) {
+#pragma unroll
+            for (int t = 0; t < VPL; ++t) part[warp * PS + VPL * lane + t] = acc[t];
+        } else {
+            if (lane % LANES_PER_V == 0) part[warp * PS + lane / LANES_PER_V] = acc[0];
+        }
+        if (!__syncthreads_and(ok)) break;  // every thread leaves together; the stage and its sums are complete
         if (tid < NV) {
             const int j = tid / MP, m = tid % MP;
             if (j < rows && m < p.M) {
                 int a = 0;
 #pragma unroll
-                for (int w = 0; w < kGvWarps; ++w) a += part[w * 32 + tid];
+                for (int w = 0; w < kGvWarps; ++w) a += part[w * PS + tid];
                 const int jr = c * p.rows_per_stage + j;  // row within the slice
                 const int64_t n = r0 + jr;
                 const float tv = __fmul_rn(__int2float_rn(a), xs_s[m]);
@@ -212,44 +225,52 @@ __device__ __forceinline__ void gemv_dot_phase_t(const GemvArgs &p, uint8_t *sta
                     p.y[(int64_t)m * p.ld_y + n] = __float2bfloat16_rn(__fmaf_rn(tv, ep_ws[jr], ep_b[jr]));
             }
         }
-        if (tid == 0 && c + p.nstages < nchunks) issue(c + p.nstages);
+        if (tid == 0 && c + p.nstages < nchunks) issue(c + p.nstages);  // every warp has read stage c
     }
 }
 
-// The dot phase for the launch's token count and rows per stage (MAXM: the most tokens the kernel takes).
-template <int MP>
+// Rows per stage padded to a power of two, capped at PS / MP (with at least two partial sums per lane).
+template <int MP, int PS, int WANT>
+constexpr int gv_rb() {
+    return WANT * MP <= PS ? WANT : (PS / MP >= 1 ? PS / MP : 1);
+}
+
+// The dot phase for the launch's token count and rows per stage (PS: partial-sum slots per warp).
+template <int MP, int PS>
 __device__ __forceinline__ void gemv_dot_phase_m(const GemvArgs &p, uint8_t *stages, const int8_t *xq,
                                                  const float *xs_s, uint64_t *full, int *abort_flag, int64_t r0,
                                                  int nrows, int nchunks, float *ep) {
-    const int rb = p.rows_per_stage;  // <= 32 / MP (launcher)
-    if (rb <= 2 || MP * 4 > 32)
-        gemv_dot_phase_t<MP, (MP * 2 <= 32 ? 2 : 1)>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
-    else if (rb <= 4 || MP * 8 > 32)
-        gemv_dot_phase_t<MP, (MP * 4 <= 32 ? 4 : 1)>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
-    else if (rb <= 8 || MP * 16 > 32)
-        gemv_dot_phase_t<MP, (MP * 8 <= 32 ? 8 : 1)>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
-    else if (rb <= 16 || MP * 32 > 32)
-        gemv_dot_phase_t<MP, (MP * 16 <= 32 ? 16 : 1)>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
+    const int rb = p.rows_per_stage;  // <= PS / MP (gv_plan_ring)
+    if (rb <= 2 || MP * 4 > PS)
+        gemv_dot_phase_t<MP, gv_rb<MP, PS, 2>(), PS>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
+    else if (rb <= 4 || MP * 8 > PS)
+        gemv_dot_phase_t<MP, gv_rb<MP, PS, 4>(), PS>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
+    else if (rb <= 8 || MP * 16 > PS)
+        gemv_dot_phase_t<MP, gv_rb<MP, PS, 8>(), PS>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
+    else if (rb <= 16 || MP * 32 > PS)
+        gemv_dot_phase_t<MP, gv_rb<MP, PS, 16>(), PS>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
+    else if (rb <= 32 || MP * 64 > PS)
+        gemv_dot_phase_t<MP, gv_rb<MP, PS, 32>(), PS>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
     else
-        gemv_dot_phase_t<MP, 32 / MP>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
+        gemv_dot_phase_t<MP, gv_rb<MP, PS, 64>(), PS>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
 }
 
-template <int MAXM>
+template <int MAXM, int PS>
 __device__ __forceinline__ void gemv_dot_phase(const GemvArgs &p, uint8_t *stages, const int8_t *xq,
                                                const float *xs_s, uint64_t *full, int *abort_flag, int64_t r0,
                                                int nrows, int nchunks, float *ep) {
     switch (gv_pad_m(p.M)) {
-        case 1: gemv_dot_phase_m<1>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep); break;
-        case 2: gemv_dot_phase_m<2>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep); break;
+        case 1: gemv_dot_phase_m<1, PS>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep); break;
+        case 2: gemv_dot_phase_m<2, PS>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep); break;
         case 4:
-            if constexpr (MAXM >= 4) gemv_dot_phase_m<4>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
+            if constexpr (MAXM >= 4) gemv_dot_phase_m<4, PS>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
             break;
         default:
             if constexpr (MAXM > 4) {
                 if (gv_pad_m(p.M) == 8)
-                    gemv_dot_phase_m<8>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
+                    gemv_dot_phase_m<8, PS>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
                 else
-                    gemv_dot_phase_m<16>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
+                    gemv_dot_phase_m<16, PS>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
             }
             break;
     }
@@ -352,7 +373,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(GemvArgs p) {
                 }
             }
             __syncthreads();
-            gemv_dot_phase<kGvMaxM>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
+            gemv_dot_phase<kGvMaxM, kGvNV>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
             if (tid == 0 && *(volatile int *)abort_flag) {
                 // A wait gave up: let the copies issued at entry land (bounded) before the CTA leaves.
                 for (int c = 0; c <= min(nchunks, p.nstages); ++c) {
@@ -396,7 +417,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_kernel(GemvArgs p) {
         __syncthreads();
     }
 
-    gemv_dot_phase<kGvMaxM>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
+    gemv_dot_phase<kGvMaxM, kGvNV>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
 }
 
 // ---------------------------------------------------------------------------
@@ -445,7 +466,7 @@ __global__ void __launch_bounds__(kGvThreads, 1) gemv_codes_kernel(GemvArgs p, c
     if (tid < p.M) xs_s[tid] = scales[tid];
     __syncthreads();  // barriers initialised, scales in place
     const bool xok = mbar_wait(xfull, 0, p.status, abort_flag);
-    if (__syncthreads_and(xok)) gemv_dot_phase<kGcMaxM>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
+    if (__syncthreads_and(xok)) gemv_dot_phase<kGcMaxM, kGcNV>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
     if (tid == 0 && *(volatile int *)abort_flag) {
         // A wait gave up: let the copies issued at entry land (bounded) before the CTA leaves.
         for (int c = 0; c <= min(nchunks, p.nstages); ++c) {
@@ -845,28 +866,35 @@ int launch_gemv_direct(const GemvArgs &base, int num_sms, cudaStream_t st) {
 }
 
 // Ring of a slice of rpc weight rows of K bytes beside `fixed` bytes of other shared memory: the number of
-// stages (kGvStages or 3) and rows per stage (at most 32 / MP for MP padded tokens), taking the plan with
-// fewer chunks -- each chunk costs ~1.8 K cycles of reduction, barriers and waits beside its dot products
-// (per-stage timestamps), so few large stages beat many small ones once both keep >= 3 stages in flight.
-// Sets nstages, rows_per_cta, rows_per_stage and stage_bytes; false when not one row fits per stage.
-bool gv_plan_ring(GemvArgs &a, int64_t rpc, int64_t K, size_t fixed, int mp) {
+// stages (kGvStages or 3) and rows per stage (at most nv / MP for MP padded tokens, and at most a 1/S share of
+// the slice so every stage is used).  A chunk costs ~1.5-1.8 K cycles of wait, reduction and epilogue (per-
+// stage timestamps) plus its dot products, which run over the rows padded to a power of two (the dot phase's
+// instantiations): ~16 MP K / 4096 cycles a padded row.  The plan with the least modelled time wins, so few
+// large stages beat many small ones, but not at the price of a half-empty power of two.  Sets nstages,
+// rows_per_cta, rows_per_stage and stage_bytes; false when not one row fits per stage.
+bool gv_plan_ring(GemvArgs &a, int64_t rpc, int64_t K, size_t fixed, int mp, int nv) {
     if (fixed >= kGvSmem) return false;
-    int64_t best_chunks = 0;
+    const double chunk_cycles = 1500.0, row_cycles = 16.0 * mp * (double)K / 4096.0;
+    double best = -1.0;
     for (int S = kGvStages; S >= 3; --S) {
         const int64_t per = (int64_t)((kGvSmem - fixed) / S) - 127;  // a stage is rounded up to 128 bytes
         const int64_t cap = per > 0 ? per / K : 0;
-        if (cap < 1) continue;
-        const int64_t rps = std::min<int64_t>(std::min<int64_t>((rpc + S - 1) / S, cap), 32 / mp);
-        const int64_t chunks = (rpc + rps - 1) / rps;
-        if (best_chunks == 0 || chunks < best_chunks) {
-            best_chunks = chunks;
-            a.nstages = S;
-            a.rows_per_stage = (int)rps;
-            a.stage_bytes = (uint32_t)(((size_t)rps * K + 127) & ~(size_t)127);
+        const int64_t hi = std::min<int64_t>(std::min<int64_t>((rpc + S - 1) / S, cap), nv / mp);
+        for (int64_t rps = 1; rps <= hi; ++rps) {
+            int64_t rb = 2;
+            while (rb < rps) rb *= 2;
+            const int64_t chunks = (rpc + rps - 1) / rps;
+            const double cost = (double)chunks * (chunk_cycles + (double)rb * row_cycles);
+            if (best < 0.0 || cost < best) {
+                best = cost;
+                a.nstages = S;
+                a.rows_per_stage = (int)rps;
+                a.stage_bytes = (uint32_t)(((size_t)rps * K + 127) & ~(size_t)127);
+            }
         }
     }
     a.rows_per_cta = (int)rpc;
-    return best_chunks > 0;
+    return best >= 0.0;
 }
 
 template <int LOGN>
@@ -881,15 +909,15 @@ int launch_gemv_t(const GemvArgs &base, int num_sms, cudaStream_t st) {
     int64_t rpc = (a.N + num_sms - 1) / num_sms;
     const int64_t grid = (a.N + rpc - 1) / rpc;
     const size_t fixed = ((x_bytes + 127) & ~(size_t)127) + ((t_bytes + 127) & ~(size_t)127) + 128 + xb_bytes +
-                         gv_ep_bytes(rpc);
+                         gv_ep_bytes(rpc, kGvNV);
     if (fixed + (size_t)kGvStages * a.K > kGvSmem) return GBQ_ENOTSUP;
-    if (!gv_plan_ring(a, rpc, a.K, fixed, gv_pad_m(a.M))) return GBQ_ENOTSUP;
+    if (!gv_plan_ring(a, rpc, a.K, fixed, gv_pad_m(a.M), kGvNV)) return GBQ_ENOTSUP;
     a.x_off = (uint32_t)((size_t)a.nstages * a.stage_bytes);
     a.t_off = a.x_off + (uint32_t)((x_bytes + 127) & ~(size_t)127);
     a.misc_off = a.t_off + (uint32_t)((t_bytes + 127) & ~(size_t)127);
     a.xb_off = 0;
     a.ep_off = a.misc_off + 128;  // misc <= 128 bytes
-    size_t smem = a.ep_off + gv_ep_bytes(rpc);
+    size_t smem = a.ep_off + gv_ep_bytes(rpc, kGvNV);
     if (LOGN == 6 && a.G == 1) {
         a.xb_off = (uint32_t)((smem + 127) & ~(size_t)127);
         smem = a.xb_off + (size_t)a.M * a.K * 2;
@@ -989,7 +1017,7 @@ __global__ void __launch_bounds__(kGvThreads, 2) gemv_gen_kernel(GemvArgs p, gen
     }
     __syncthreads();  // the codes are complete
 
-    gemv_dot_phase<kGvGenMaxM>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
+    gemv_dot_phase<kGvGenMaxM, kGvNV>(p, stages, xq, xs_s, full, abort_flag, r0, nrows, nchunks, ep);
     if (tid == 0 && *(volatile int *)abort_flag) {
         // A wait gave up: let the copies issued at entry land (bounded) before the CTA leaves.
         for (int c = 0; c < min(nchunks, p.nstages); ++c) {
@@ -1006,7 +1034,7 @@ __global__ void __launch_bounds__(kGvThreads, 2) gemv_gen_kernel(GemvArgs p, gen
 // epilogue operands.
 size_t gemv_codes_fixed(int64_t M, int64_t N, int64_t K, int num_sms) {
     const int64_t rpc = (N + num_sms - 1) / num_sms;
-    return (((size_t)M * K + 127) & ~(size_t)127) + 128 + gv_ep_bytes(rpc);
+    return (((size_t)M * K + 127) & ~(size_t)127) + 128 + gv_ep_bytes(rpc, kGcNV);
 }
 
 bool gemv_codes_fits(int64_t M, int64_t N, int64_t K, int num_sms) {
@@ -1039,11 +1067,11 @@ int launch_gemv_codes2(const int8_t *codes, const float *scales, const int8_t *w
     const size_t fixed = gemv_codes_fixed(M, N, K, num_sms);
     const int64_t rpc = (N + num_sms - 1) / num_sms;
     const int64_t grid = (N + rpc - 1) / rpc;
-    if (!gv_plan_ring(a, rpc, K, fixed, gv_pad_m(M))) return GBQ_ENOTSUP;
+    if (!gv_plan_ring(a, rpc, K, fixed, gv_pad_m(M), kGcNV)) return GBQ_ENOTSUP;
     a.x_off = (uint32_t)((size_t)a.nstages * a.stage_bytes);
     a.misc_off = a.x_off + (uint32_t)((x_bytes + 127) & ~(size_t)127);
     a.ep_off = a.misc_off + 128;  // scales, barriers, abort flag, codes barrier: < 128 bytes
-    const size_t smem = a.ep_off + gv_ep_bytes(rpc);
+    const size_t smem = a.ep_off + gv_ep_bytes(rpc, kGcNV);
     static bool attr = false;
     if (!attr) {
         if (cudaFuncSetAttribute(gemv_codes_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGvSmem) !=
@@ -1080,7 +1108,7 @@ int launch_gemv_codes(const int8_t *codes, const float *scales, const int8_t *w8
 size_t gemv_gen_fixed(int64_t M, int64_t N, int64_t K, int num_sms) {
     const int64_t rpc = (N + num_sms - 1) / num_sms;
     const size_t E = (size_t)M * K;
-    return ((E + 127) & ~(size_t)127) + 128 + gv_ep_bytes(rpc) + (((E + E / 32) * 4 + 127) & ~(size_t)127);
+    return ((E + 127) & ~(size_t)127) + 128 + gv_ep_bytes(rpc, kGvNV) + (((E + E / 32) * 4 + 127) & ~(size_t)127);
 }
 
 bool gemv_gen_fits(int64_t M, int64_t N, int64_t K, int num_sms) {
@@ -1120,11 +1148,11 @@ int launch_gemv_gen(const void *x, const int8_t *w8, const float *w_scale, const
     const size_t fixed = gemv_gen_fixed(M, N, K, num_sms);
     const int64_t rpc = (N + num_sms - 1) / num_sms;
     const int64_t grid = (N + rpc - 1) / rpc;
-    if (!gv_plan_ring(a, rpc, K, fixed, gv_pad_m(M))) return GBQ_ENOTSUP;
+    if (!gv_plan_ring(a, rpc, K, fixed, gv_pad_m(M), kGvNV)) return GBQ_ENOTSUP;
     a.x_off = (uint32_t)((size_t)a.nstages * a.stage_bytes);
     a.misc_off = a.x_off + (uint32_t)(((size_t)M * K + 127) & ~(size_t)127);
     a.ep_off = a.misc_off + 128;  // token scales, row maxima, stage barriers, abort flag: < 128 bytes
-    a.t_off = a.ep_off + (uint32_t)gv_ep_bytes(rpc);
+    a.t_off = a.ep_off + (uint32_t)gv_ep_bytes(rpc, kGvNV);
     const size_t E = (size_t)M * K;
     const size_t smem = a.t_off + (((E + E / 32) * 4 + 127) & ~(size_t)127);
     static bool attr = false;
