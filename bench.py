@@ -377,8 +377,8 @@ def run_ours(args):
         e2e = measure_e2e(G, torch, dev, x3, w83, s3, b3, ws_lin, args)
     if "decode_gemv" in opfn:
         # gbq_linear at M = 1 is one GEMV launch: time a chain of 32 dependent decode layers (call i reads
-        # call i-1's output; 16 weight copies, 268 MB) with one event pair, after checking the launch census
-        # of a call.
+        # call i-1's output; 16 weight copies, 268 MB) captured in a CUDA graph, one event pair per replay
+        # (median of five), after checking the launch census of a call.
         G.prof_enable(True)
         opfn["decode_gemv"](0)
         torch.cuda.synchronize()
@@ -398,7 +398,7 @@ def run_ours(args):
                "frac": round(ach_g / peaks["hbm"], 4), "ms": round(graph_ms, 4),
                "traffic": profiled_traffic("gemv_direct_kernel"),
                "mode": "CUDA-graph replay of 32 dependent decode layers (call i's x is call i-1's y; 16 weight "
-                       "copies, 268 MB), one event pair",
+                       "copies, 268 MB), one event pair per replay, median of 5 replays after L2 flushes",
                "eager": {"ms": round(gv_ms, 4), "achieved": round(ach, 1), "frac": round(ach / peaks["hbm"], 4),
                          "note": "the same chain launched from Python, one event pair (host launch rate bound)"}}
 
@@ -437,7 +437,8 @@ def run_ours(args):
                 "ms": round(lin8_ms, 4), "achieved": round(lin8_bytes / (lin8_ms * 1e-3) * 1e-9, 1),
                 "unit": "GB/s", "frac": round(lin8_bytes / (lin8_ms * 1e-3) * 1e-9 / peaks["hbm"], 4),
                 "route": "rotation kernel -> codes GEMV"},
-            "mode": "CUDA-graph replay of dependent layers (call i's x is call i-1's y), one event pair"}
+            "mode": "CUDA-graph replay of dependent layers (call i's x is call i-1's y), one event pair per "
+                    "replay, median of 5 replays after L2 flushes"}
         del layers
 
     out = {
@@ -492,9 +493,10 @@ def batch_ms(torch, flush, fn, reps=32):
     return e0.elapsed_time(e1) / reps
 
 
-def graph_batch_ms(torch, flush, fn, reps=32):
+def graph_batch_ms(torch, flush, fn, reps=32, samples=5):
     """batch_ms with the reps calls captured once in a CUDA graph (after an eager warm-up call) and the
-    replay timed: host launch overhead leaves the timed region, device-side launch gaps stay."""
+    replay timed: host launch overhead leaves the timed region, device-side launch gaps stay.  The median
+    of `samples` replays, each after an L2 flush."""
     fn(0)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
@@ -503,16 +505,19 @@ def graph_batch_ms(torch, flush, fn, reps=32):
             fn(i)
     g.replay()  # first replay uploads the graph
     torch.cuda.synchronize()
-    flush_l2(flush)
     st = torch.cuda.current_stream()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    g.replay()
-    e1.record(st)
-    torch.cuda.synchronize()
+    times = []
+    for _ in range(samples):
+        flush_l2(flush)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        g.replay()
+        e1.record(st)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) / reps)
     del g
-    return e0.elapsed_time(e1) / reps
+    return float(np.median(times))
 
 
 def kernel_ms(G, torch, flush, kind, fn, reps=10):

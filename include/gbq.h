@@ -187,7 +187,7 @@ int gbq_dequant(const int32_t *acc, int64_t ld_acc, const float *x_scale,
  * {16, 32, 64}, K <= 4096, and for every other descriptor (not the identity)
  * while M * K <= 8192; else over codes the rotation kernels write into the
  * workspace first (any descriptor, while M * K codes and four weight rows fit
- * in shared memory; at N = 4096: K <= 44672 at M = 1, 27904 at M = 4, 11168
+ * in shared memory; at N = 4096: K <= 44032 at M = 1, 27520 at M = 4, 11008
  * at M = 16); larger M or K runs the GEMM (same values).  Workspace:
  * GBQ_OP_LINEAR.
  * At K = 4096 (a = b = 64, one group) the decode kernel is launched with
