@@ -83,7 +83,7 @@ __host__ __device__ constexpr size_t gv_ep_bytes(int64_t rows_per_cta, int nv) {
 }
 
 // The slice's w_scale and bias into shared memory (read before the dot products need them; the first
-// stage wait's __syncthreads publishes them).
+// stage's barrier, at the latest, publishes them).
 __device__ __forceinline__ void gv_load_epilogue(const GemvArgs &p, float *ep, int64_t r0, int nrows) {
     for (int t = threadIdx.x; t < nrows; t += kGvThreads) {
         const int64_t n = r0 + t;
