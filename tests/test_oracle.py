@@ -118,6 +118,32 @@ def test_rotate_matches_explicit_kronecker(rot):
     assert _ulp_diff_f32(v, ref).max() <= 1
 
 
+def _digit_hadamard_any(n):
+    """H_n for a power of two n: the printed H4 on every base-4 digit, and an unnormalised H2 on the most
+    significant index bit when log2 n is odd (the reading of the H128 case taken for every odd size)."""
+    logn = int(np.log2(n))
+    H = _digit_hadamard(logn // 2)
+    if logn % 2:
+        H = np.kron(np.array([[1, 1], [1, -1]], np.int64), H)  # the first factor sits on the top bit
+    return H
+
+
+@pytest.mark.parametrize("rot", [(32, 64, 1), (64, 128, 1), (16, 32, 1), (2, 8, 1), (128, 64, 1)])
+def test_one_hot_rotates_to_pm_inv_sqrt_k_non_square(rot):
+    """a != b, including an odd total log2 (1 / sqrt(K) irrational): a one-hot row rotates to
+    fl32(+-1 / sqrt(K)) in the sign pattern of column k of H_a (x) H_b, built here from base-4 digits."""
+    a, b, _ = rot
+    K = a * b
+    Hfull = np.kron(_digit_hadamard_any(a), _digit_hadamard_any(b))
+    inv = np.float32(1.0 / np.sqrt(np.float64(K)))
+    for k in (0, 1, K // 3, K - 1):
+        x = np.zeros((1, K), np.float32)
+        x[0, k] = 1.0
+        v = O.rotate(x, rot)
+        assert np.all(np.abs(v) == inv)
+        assert np.array_equal(np.sign(v[0]).astype(np.int64), Hfull[:, k])
+
+
 @pytest.mark.parametrize("rot", [(16, 16, 1), (64, 64, 1), (128, 128, 1)])
 def test_one_hot_rotates_to_pm_inv_sqrt_k(rot):
     a, b, _ = rot
