@@ -144,6 +144,23 @@ def test_one_hot_rotates_to_pm_inv_sqrt_k_non_square(rot):
         assert np.array_equal(np.sign(v[0]).astype(np.int64), Hfull[:, k])
 
 
+@pytest.mark.parametrize("rot", [(16, 16, 3), (8, 8, 16), (32, 64, 2), (2, 32, 5)])
+def test_grouped_rotation_acts_on_each_group_alone(rot):
+    """groups = G is the block-diagonal I_G (x) R: each a*b-long group of a row is rotated by itself, as a
+    row of its own would be (the page's groupsize), and the quantizer then takes one scale over the row."""
+    a, b, g = rot
+    n = a * b
+    rng = np.random.default_rng(3)
+    x = I.bf16_to_float(I.bf16_bits(rng.standard_normal((3, n * g), dtype=np.float32)))
+    x[:, :n] *= 50.0  # groups of very different magnitude
+    v = O.rotate(x, rot)
+    for k in range(g):
+        assert np.array_equal(v[:, k * n:(k + 1) * n], O.rotate(np.ascontiguousarray(x[:, k * n:(k + 1) * n]),
+                                                                 (a, b, 1)))
+    q, s = O.quantize(v)
+    assert np.array_equal(s, (np.abs(v).max(axis=1) / np.float32(127.0)).astype(np.float32))
+
+
 @pytest.mark.parametrize("rot", [(16, 16, 1), (64, 64, 1), (128, 128, 1)])
 def test_one_hot_rotates_to_pm_inv_sqrt_k(rot):
     a, b, _ = rot
