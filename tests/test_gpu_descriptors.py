@@ -268,3 +268,19 @@ def test_linear_routes_agree_across_token_counts(ops, rot):
         y2 = ops.dequant(acc, xs, wsd, bias)
         torch.cuda.synchronize()
         assert torch.equal(y.view(torch.int16), y2.view(torch.int16)), (rot, M)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 19456, 1024), (2, 14592, 1024), (4, 7296, 1024), (3, 7296, 2048)])
+def test_codes_gemv_wide_stages(ops, M, N, K):
+    """The codes GEMV with many weight rows per stage (up to 64 / MP, padded to a power of two: 64 at one
+    token, 32 at two, 16 at four), on the identity descriptor that sends even one token through it: the same
+    bits as dequant(linear_acc), with bias."""
+    rot = (1, 1, K)
+    c = I.linear_case(M, K, N, n_outliers=max(1, K // 100), outlier_scale=30.0, bias_std=0.01, seed=N + M)
+    w8, ws = O.prepare_weight(c["w"], rot)
+    x, bias = bf16_dev(c["x"]), bf16_dev(c["bias"])
+    y = ops.linear(x, d(w8), d(ws), bias, rot)
+    acc, xs = ops.linear_acc(x, d(w8), rot)
+    y2 = ops.dequant(acc, xs, d(ws), bias)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
